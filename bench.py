@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark of the chunkwise KDA forward pass (tokens/s and % of the HBM roofline).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one call of the library's forward entry point over one batch of the
+B=2, T=8192, H=32, d_k=d_v=128, C=64 bf16 per-channel-gate workload with an initial
+state and the final state written. Inputs live in HBM before the timed region (816 MB
+per step, larger than the 129 MB L2, so no flush is needed between steps). Rank 0
+prints one JSON line. Under torchrun every rank runs its own batch (weak scaling; the
+(sequence, head) units are independent, so ranks exchange nothing but the timing).
+
+``--impl reference`` times the fp64 CPU oracle as it stands on this host's cores, each
+step a bounded sample of (sequence, head) units of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "kda_b2_t8192_h32_d128_bf16"
+METRIC = "chunk KDA fwd tokens/s at T=8192,H=32,d=128 bf16; % of roofline"
+
+# DRAM traffic per launch of the forward kernel, from an ncu capture of this workload
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of the kernel sources
+# it was taken on; any change to the sources makes the figure stale (reported as null).
+MEASURED_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "chunkwise_gated_linear_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic_bytes(x) -> int:
+    """HBM bytes the method must move: q, k once per key head; v, o, g, beta per value
+    head; h0 and ht once per (sequence, value head)."""
+    e = 2 if x.dtype == "bf16" else 4
+    T = x.T_total
+    gate = 4 * x.d_k if x.gate == "channel" else 4
+    per_tok = x.H_k * 2 * x.d_k * e + x.H_v * (2 * x.d_v * e + gate + 4)
+    state = x.N * x.H_v * 4 * x.d_k * x.d_v * ((x.h0 is not None) + 1)
+    return T * per_tok + state
+
+
+def algorithmic_flops(x, C=64) -> int:
+    """Useful FLOPs of the chunk algorithm (causal halves counted once), per token and
+    value head: Gram (strict lower) + Aqk (lower) + forward substitution on [Kp | V]
+    + W S + Qp S + Aqk Vt + Kbar^T Vt."""
+    dk, dv = x.d_k, x.d_v
+    lo, lo_d = C * (C - 1) // 2, C * (C + 1) // 2
+    per_chunk = 2 * (lo * dk + lo_d * dk + lo * (dk + dv) + 3 * C * dk * dv + lo_d * dv)
+    return int(round(per_chunk / C * x.T_total * x.H_v))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples taken during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value: float) -> float:
+    if pg is None:
+        return value
+    import torch
+
+    dev = "cuda" if torch.cuda.is_available() and pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(x, n_units, threads=0):
+    """Time the fp64 oracle on the first n_units (sequence, head) units; returns
+    (seconds, equivalent tokens, threads used)."""
+    from oracle import kda_recurrence, oracle_threads
+
+    units = [(n, h) for n in range(x.N) for h in range(x.H_v)][:n_units]
+    t0 = time.perf_counter()
+    kda_recurrence(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, x.scale, units=units, threads=threads)
+    dt = time.perf_counter() - t0
+    lens = x.lengths()
+    unit_tokens = sum(int(lens[n]) for n, _ in units)
+    used = min(threads if threads > 0 else oracle_threads(), len(units))
+    return dt, unit_tokens / x.H_v, used
+
+
+def run_reference(args, world, rank, pg):
+    """--impl reference: the oracle as it stands, on the host cores, bounded samples."""
+    from inputs import workload_inputs
+    from oracle import oracle_threads
+
+    if rank != 0:
+        return
+    x = workload_inputs(args.workload)
+    n_units = max(1, min(oracle_threads(), x.N * x.H_v))
+    for _ in range(args.warmup):
+        oracle_sample(x, n_units)
+    tot_t, tot_tok, used = 0.0, 0.0, 1
+    for _ in range(args.steps):
+        dt, tok, used = oracle_sample(x, n_units)
+        tot_t += dt
+        tot_tok += tok
+    value = tot_tok / tot_t
+    sample = (f"{n_units} of {x.N * x.H_v} (sequence, head) units of {args.workload} per step "
+              f"({x.lengths()[0]} tokens each), fp64 token recurrence")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local, pg):
+    import numpy as np
+    import torch
+
+    from chunkwise_gated_linear_gb300 import kda
+    from inputs import workload_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = kda.lib()
+
+    x = workload_inputs(args.workload, seed=1000 + rank)
+    B = x.N
+    T = x.T_total // B
+    dt_io = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+
+    def host(a, dtype, shape):
+        return torch.from_numpy(np.ascontiguousarray(a)).reshape(shape).to(dtype).pin_memory()
+
+    H = {
+        "q": host(x.q, dt_io, (B, T, x.H_k, x.d_k)), "k": host(x.k, dt_io, (B, T, x.H_k, x.d_k)),
+        "v": host(x.v, dt_io, (B, T, x.H_v, x.d_v)), "g": host(x.g, torch.float32, (B, T, x.H_v, x.d_k)),
+        "beta": host(x.beta, torch.float32, (B, T, x.H_v)),
+        "h0": host(x.h0, torch.float32, (B, x.H_v, x.d_k, x.d_v)),
+    }
+    D = {key: t.to(dev) for key, t in H.items()}
+    D["o"] = torch.empty((B, T, x.H_v, x.d_v), dtype=dt_io, device=dev)
+    D["ht"] = torch.empty((B, x.H_v, x.d_k, x.d_v), dtype=torch.float32, device=dev)
+    H["o"] = torch.empty_like(D["o"], device="cpu").pin_memory()
+    H["ht"] = torch.empty_like(D["ht"], device="cpu").pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    entry = lib.kda_chunk_fwd if x.dtype == "bf16" else lib.kda_chunk_fwd_f32
+
+    def call():
+        st = entry(D["q"].data_ptr(), D["k"].data_ptr(), D["v"].data_ptr(), D["g"].data_ptr(),
+                   D["beta"].data_ptr(), D["h0"].data_ptr(), D["o"].data_ptr(), D["ht"].data_ptr(),
+                   B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale, None, sh)
+        if st != 0:
+            raise RuntimeError(kda.status_string(st))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for key in ("q", "k", "v", "g", "beta", "h0"):
+                D[key].copy_(H[key], non_blocking=True)
+            call()
+            H["o"].copy_(D["o"], non_blocking=True)
+            H["ht"].copy_(D["ht"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+
+    # device-resident throughput: exactly K launches, CUDA events on the launch stream
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(pg)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            call()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(pg)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = clk.summary()
+    ms_max = max_over_ranks(pg, ms)
+    tokens = B * T
+    value = tokens * world / (ms_max / 1000.0)
+
+    # end to end through the C ABI with host buffers: H2D inputs, call, D2H results
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ev3.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    ms_e2e = max_over_ranks(pg, ev2.elapsed_time(ev3) / args.steps)
+    h2d = sum(H[key].numel() * H[key].element_size() for key in ("q", "k", "v", "g", "beta", "h0"))
+    d2h = H["o"].numel() * H["o"].element_size() + H["ht"].numel() * H["ht"].element_size()
+
+    peak, peak_kind = load_peaks()
+    abytes = algorithmic_bytes(x)
+    achieved = abytes / (ms / 1000.0) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = MEASURED_TRAFFIC.get((args.workload, src_hash))
+    flops = algorithmic_flops(x)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import oracle_threads
+
+        n_units = min(32, x.N * x.H_v)  # about 20-30 s of CPU work
+        dt_cpu, tok_cpu, used = oracle_sample(x, n_units)
+        cpu = {"value": tok_cpu / dt_cpu, "unit": "tokens/s", "cores": used, "kind": "oracle",
+               "sample": f"{n_units} of {x.N * x.H_v} (sequence, head) units of {args.workload} "
+                         f"({T} tokens each), fp64 token recurrence, {dt_cpu:.1f} s wall on "
+                         f"{oracle_threads()} host threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": x.dtype, "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "T": T, "H_k": x.H_k, "H_v": x.H_v, "d_k": x.d_k,
+                       "d_v": x.d_v, "C": 64, "gate": "per-channel", "h0": True, "ht": True,
+                       "global_batch": B * world, "seq_len": T, "parallelism": f"dp{world} (independent batches)",
+                       "l2": "inputs larger than L2 (816 MB per step), no flush"},
+            "e2e": {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": abytes, "kernel": "kda_fwd_bf16_kernel",
+                         "tflops": flops / (ms / 1000.0) / 1e12},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # the timing rules ask for at least 3 warm-up steps
+    world, rank, local, pg = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank, pg)
+        else:
+            run_ours(args, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

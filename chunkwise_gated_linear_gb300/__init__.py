@@ -1,0 +1,15 @@
+"""Chunkwise forward pass of the gated delta rule with a per-channel gate (Kimi Delta
+Attention) for GB300 (sm_103a): a C-ABI CUDA library (``include/kda.h``,
+``lib/libkda.so``) and its thin Python binding (:mod:`.kda`)."""
+
+from .kda import (  # noqa: F401
+    KdaError,
+    chunk_kda_fwd,
+    kda_chunk_fwd,
+    kda_chunk_fwd_ex,
+    kda_chunk_fwd_f32,
+    kda_fwd_params,
+    kda_get_device_error,
+    lib,
+    status_string,
+)

@@ -1,0 +1,152 @@
+// C ABI of the library (declared in include/kda.h): argument checks, dispatch to the
+// kernels, status strings and the device error word.
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
+}  // namespace kda
+
+namespace {
+
+// One error word per device; its device address is looked up once per device.
+__device__ unsigned int g_device_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+unsigned int *g_err_ptr[kMaxDevices] = {};
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+thread_local char t_msg[256];
+
+cudaError_t device_error_ptr(unsigned int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_err_mu);
+    if (g_err_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_error_word);
+        if (e != cudaSuccess) return e;
+        g_err_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int run(const kda_fwd_params &p, cudaStream_t stream) {
+    if (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr || p.beta == nullptr ||
+        p.o == nullptr)
+        return KDA_ERR_INVALID_ARG;
+    if (p.B < 1 || p.T < 0 || p.H_k < 1 || p.H_v < 1 || p.H_v % p.H_k != 0) return KDA_ERR_INVALID_ARG;
+    if (p.flags != 0) return KDA_ERR_INVALID_ARG;
+    if (p.dtype != KDA_DTYPE_BF16 && p.dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
+    if (p.gate_mode != KDA_GATE_PER_CHANNEL && p.gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_UNSUPPORTED;
+    if ((p.d_k != 64 && p.d_k != 128) || (p.d_v != 64 && p.d_v != 128) || p.C != kda::kChunk)
+        return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.o) || !aligned16(p.g) ||
+        !aligned16(p.beta) || !aligned16(p.h0) || !aligned16(p.ht))
+        return KDA_ERR_ALIGNMENT;
+    // Sizes must fit the kernels' 32-bit grid dimensions and the int32 offsets.
+    const int64_t N = p.B;
+    const int64_t total_tokens = p.cu_seqlens ? (int64_t)p.T : N * p.T;
+    if (total_tokens > INT32_MAX || N > 65535 || p.H_v > 65535) return KDA_ERR_UNSUPPORTED;
+
+    kda::FwdArgs a{};
+    a.q = p.q;
+    a.k = p.k;
+    a.v = p.v;
+    a.g = p.g;
+    a.beta = p.beta;
+    a.h0 = p.h0;
+    a.o = p.o;
+    a.ht = p.ht;
+    a.cu_seqlens = p.cu_seqlens;
+    a.N = p.B;
+    a.T = p.T;
+    a.H_k = p.H_k;
+    a.H_v = p.H_v;
+    a.d_k = p.d_k;
+    a.d_v = p.d_v;
+    a.group = p.H_v / p.H_k;
+    a.scale = p.scale;
+    a.gate_per_head = p.gate_mode == KDA_GATE_PER_HEAD ? 1 : 0;
+
+    cudaError_t e = device_error_ptr(&a.err);
+    if (e == cudaSuccess)
+        e = p.dtype == KDA_DTYPE_BF16 ? kda::launch_fwd_bf16(a, stream) : kda::launch_fwd_f32(a, stream);
+    if (e != cudaSuccess) {
+        t_last_cuda_error = e;
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const float *h0, void *o, float *ht, int B, int T, int H_k, int H_v, int d_k, int d_v,
+                  int C, float scale, const int32_t *cu_seqlens, cudaStream_t stream) {
+    kda_fwd_params p{q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
+                     KDA_DTYPE_BF16, KDA_GATE_PER_CHANNEL, 0};
+    return run(p, stream);
+}
+
+int kda_chunk_fwd_f32(const float *q, const float *k, const float *v, const float *g, const float *beta,
+                      const float *h0, float *o, float *ht, int B, int T, int H_k, int H_v, int d_k,
+                      int d_v, int C, float scale, const int32_t *cu_seqlens, cudaStream_t stream) {
+    kda_fwd_params p{q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
+                     KDA_DTYPE_F32, KDA_GATE_PER_CHANNEL, 0};
+    return run(p, stream);
+}
+
+int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) {
+    if (p == nullptr) return KDA_ERR_INVALID_ARG;
+    return run(*p, stream);
+}
+
+const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK:
+            return "KDA_OK";
+        case KDA_ERR_INVALID_ARG:
+            return "KDA_ERR_INVALID_ARG: a required pointer is NULL or a size is out of range";
+        case KDA_ERR_UNSUPPORTED:
+            return "KDA_ERR_UNSUPPORTED: d_k and d_v must be 64 or 128, C must be 64, and the dtype "
+                   "and gate mode must be known";
+        case KDA_ERR_ALIGNMENT:
+            return "KDA_ERR_ALIGNMENT: every tensor pointer must be 16-byte aligned";
+        case KDA_ERR_CUDA:
+            std::snprintf(t_msg, sizeof(t_msg), "KDA_ERR_CUDA: %s (%s)", cudaGetErrorName(t_last_cuda_error),
+                          cudaGetErrorString(t_last_cuda_error));
+            return t_msg;
+        default:
+            return "unknown kda status";
+    }
+}
+
+int kda_get_device_error(cudaStream_t stream) {
+    unsigned int *ptr = nullptr;
+    cudaError_t e = device_error_ptr(&ptr);
+    unsigned int host = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&host, ptr, sizeof(host), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ptr, 0, sizeof(unsigned int), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        t_last_cuda_error = e;
+        return KDA_ERR_CUDA;
+    }
+    return static_cast<int>(host);
+}
+
+}  // extern "C"

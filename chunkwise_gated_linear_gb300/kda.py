@@ -1,0 +1,182 @@
+"""Python binding of ``libkda.so`` (argument marshalling only).
+
+The raw functions below carry the C names and argument lists of ``include/kda.h`` and
+take device pointers as integers. :func:`chunk_kda_fwd` is the convenience call on torch
+CUDA tensors: it checks shapes and dtypes, allocates the outputs with torch and calls
+the C ABI on the current torch stream. Every step of the computation runs in the
+library's CUDA kernels; there is no other code path. If the library cannot be loaded
+the import fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_ALIGNMENT = -3
+KDA_ERR_CUDA = -4
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_F32 = 1
+KDA_GATE_PER_CHANNEL = 0
+KDA_GATE_PER_HEAD = 1
+KDA_DEVICE_ERR_SEQLENS = 1
+
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_ex", "kda_status_string",
+            "kda_get_device_error")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)}")
+        self.status = status
+
+
+class kda_fwd_params(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("ht", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("T", ctypes.c_int), ("H_k", ctypes.c_int), ("H_v", ctypes.c_int),
+        ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("C", ctypes.c_int),
+        ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p),
+        ("dtype", ctypes.c_int), ("gate_mode", ctypes.c_int), ("flags", ctypes.c_int),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libkda.so`` (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        if not os.path.exists(path):
+            raise ImportError(f"libkda.so is missing at {path}")
+        L = ctypes.CDLL(path)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        sig = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]
+        for name in ("kda_chunk_fwd", "kda_chunk_fwd_f32"):
+            fn = getattr(L, name)
+            fn.argtypes = sig
+            fn.restype = I
+        L.kda_chunk_fwd_ex.argtypes = [ctypes.POINTER(kda_fwd_params), P]
+        L.kda_chunk_fwd_ex.restype = I
+        L.kda_status_string.argtypes = [I]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_get_device_error.argtypes = [P]
+        L.kda_get_device_error.restype = I
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+# ---- raw C entry points (pointers as ints, 0 for NULL) -----------------------------------
+
+def kda_chunk_fwd(q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
+                  stream) -> int:
+    return lib().kda_chunk_fwd(q, k, v, g, beta, h0 or None, o, ht or None, B, T, H_k, H_v, d_k,
+                               d_v, C, scale, cu_seqlens or None, stream or None)
+
+
+def kda_chunk_fwd_f32(q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
+                      stream) -> int:
+    return lib().kda_chunk_fwd_f32(q, k, v, g, beta, h0 or None, o, ht or None, B, T, H_k, H_v,
+                                   d_k, d_v, C, scale, cu_seqlens or None, stream or None)
+
+
+def kda_chunk_fwd_ex(params: kda_fwd_params, stream) -> int:
+    return lib().kda_chunk_fwd_ex(ctypes.byref(params), stream or None)
+
+
+def kda_get_device_error(stream) -> int:
+    return lib().kda_get_device_error(stream or None)
+
+
+# ---- torch convenience ---------------------------------------------------------------------
+
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
+                  output_final_state=True, chunk_size=64, o=None, ht=None, stream=None):
+    """Chunkwise KDA forward on torch CUDA tensors; returns ``(o, ht)``.
+
+    q, k [B, T, H_k, d_k] and v [B, T, H_v, d_v], all bf16 or all fp32; g fp32
+    [B, T, H_v, d_k] (per-channel gate) or [B, T, H_v] (one gate per head); beta fp32
+    [B, T, H_v]; h0 fp32 [N, H_v, d_k, d_v] or None. With ``cu_seqlens`` (int32 [N + 1]
+    on the device) B must be 1 and the N sequences are packed along T. ``o`` and ``ht``
+    may be given to write into existing buffers. ``ht`` is None in the result when
+    ``output_final_state`` is False.
+    """
+    import torch
+
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4:
+        raise ValueError("q, k must be [B, T, H_k, d_k] and v [B, T, H_v, d_v]")
+    B, T, H_k, d_k = q.shape
+    _, _, H_v, d_v = v.shape
+    if v.shape[:2] != (B, T):
+        raise ValueError("v must share B and T with q")
+    if q.dtype == torch.bfloat16:
+        dtype = KDA_DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dtype = KDA_DTYPE_F32
+    else:
+        raise TypeError("q, k, v must be bf16 or fp32")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be fp32")
+    if g.shape == (B, T, H_v, d_k):
+        gate = KDA_GATE_PER_CHANNEL
+    elif g.shape == (B, T, H_v):
+        gate = KDA_GATE_PER_HEAD
+    else:
+        raise ValueError("g must be [B, T, H_v, d_k] or [B, T, H_v]")
+    if beta.shape != (B, T, H_v):
+        raise ValueError("beta must be [B, T, H_v]")
+    for t in (q, k, v, g, beta, h0, cu_seqlens):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("every tensor must be a contiguous CUDA tensor")
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("packed sequences need B == 1")
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        N = cu_seqlens.numel() - 1
+        nb, nt = N, T
+    else:
+        N = B
+        nb, nt = B, T
+    if h0 is not None and (h0.dtype != torch.float32 or tuple(h0.shape) != (N, H_v, d_k, d_v)):
+        raise ValueError("h0 must be fp32 [N, H_v, d_k, d_v]")
+    if o is None:
+        o = torch.empty((B, T, H_v, d_v), dtype=q.dtype, device=q.device)
+    if output_final_state and ht is None:
+        ht = torch.empty((N, H_v, d_k, d_v), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        ht = None
+    if scale is None:
+        scale = d_k ** -0.5
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    p = kda_fwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0) or None, _ptr(o),
+                       _ptr(ht) or None, nb, nt, H_k, H_v, d_k, d_v, chunk_size, float(scale),
+                       _ptr(cu_seqlens) or None, dtype, gate, 0)
+    st = kda_chunk_fwd_ex(p, stream)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_ex")
+    return o, ht

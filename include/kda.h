@@ -1,0 +1,142 @@
+/*
+ * kda.h — C ABI of the chunkwise forward pass of the gated delta rule with a
+ * per-channel gate (Kimi Delta Attention, KDA), for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("TileLang 实战：KDA 从零到一–Kimi Delta Attention", §0 and §3.1):
+ * for every sequence n and value head h, with state S in R^{d_k x d_v} (the transposed
+ * layout the kernels keep; "TileLang 实战：KDA 从零到一--标量衰减", §4.0),
+ *
+ *     S <- Diag(exp(g_t)) S                     decay, before the erase read
+ *     u <- beta_t (v_t - S^T k_t)               erase (delta rule)
+ *     S <- S + k_t u^T                          write
+ *     o_t = scale * S^T q_t
+ *
+ * i.e. S_t = S_{t-1} Diag(a_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T in the paper
+ * layout, a_t = exp(g_t). The scalar-gate Gated DeltaNet ("Gated DeltaNet", section
+ * "DeltaNet 与 Gated Delta Rule") is the case of one gate per (token, head) broadcast over
+ * the d_k channels. The library computes it chunk by chunk (C tokens per chunk), with
+ * the per-chunk equations of "RNN的复兴04:线性注意力并行计算DPLR", §5.3.5: a chunk-local
+ * cumulative log-gate, the separable decay-weighted Gram matrix, the UT-transform
+ * triangular solve giving the WY factors W and U, the serial chunk-to-chunk state step
+ * and the chunk-parallel output. The result equals the token recurrence up to rounding.
+ *
+ * Layouts (all pointers are DEVICE pointers; tensors are contiguous, token-major):
+ *   q, k   [B, T, H_k, d_k]     bf16 (kda_chunk_fwd) or fp32 (kda_chunk_fwd_f32)
+ *   v, o   [B, T, H_v, d_v]     same dtype as q
+ *   g      [B, T, H_v, d_k]     fp32 natural-log gates (g <= 0), per token, NOT cumsummed;
+ *                               [B, T, H_v] fp32 in the per-head gate mode of _ex
+ *   beta   [B, T, H_v]          fp32
+ *   h0, ht [N, H_v, d_k, d_v]   fp32 initial / final state, N = number of sequences
+ *   Value head h reads key head h / (H_v / H_k) (grouped heads; H_v % H_k == 0).
+ *
+ * Varlen packing ("Gated DeltaNet", chunk_local_cumsum: cu_seqlens and chunk indices):
+ *   if cu_seqlens != NULL the tensors hold N = B sequences packed along the token axis
+ *   with a physical batch of 1 ([1, T, ...], T = total tokens). cu_seqlens is a DEVICE
+ *   int32 array of B + 1 non-decreasing offsets, cu_seqlens[0] = 0 and cu_seqlens[B] = T.
+ *   Chunks never span two sequences. Its contents are read on the device only: a
+ *   malformed array is a precondition violation; the kernels skip a sequence whose
+ *   offsets are out of order or out of [0, T] and raise KDA_DEVICE_ERR_SEQLENS, which
+ *   kda_get_device_error reports.
+ *   if cu_seqlens == NULL the batch holds B sequences of T tokens each (N = B).
+ *
+ * NULL conventions: h0 == NULL means a zero initial state; ht == NULL means the final
+ *   state is not written. q, k, v, g, beta and o are required.
+ *
+ * Sizes supported: d_k, d_v in {64, 128}; C == 64; B >= 1; T >= 0; H_k >= 1; H_v >= 1.
+ *   T == 0 (or empty sequences) is valid: no o rows, ht = h0 (or 0).
+ *
+ * Ownership and semantics: the caller owns every buffer; the library allocates no
+ *   memory. Calls are asynchronous on `stream` (no host synchronisation). o and ht are
+ *   fully overwritten; o and ht must not alias any input. The same inputs give bitwise
+ *   equal outputs (no atomics on outputs). The entry points are thread-safe.
+ *
+ * Errors: 0 (KDA_OK) on success, otherwise a negative status; nothing is launched when
+ *   a status other than KDA_OK or KDA_ERR_CUDA is returned.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_OK 0
+#define KDA_ERR_INVALID_ARG (-1) /* a required pointer is NULL or a size is out of range */
+#define KDA_ERR_UNSUPPORTED (-2) /* d_k, d_v, C, dtype or gate mode not supported */
+#define KDA_ERR_ALIGNMENT (-3)   /* a tensor pointer is not 16-byte aligned */
+#define KDA_ERR_CUDA (-4)        /* a CUDA call failed; kda_status_string says which */
+
+#define KDA_DTYPE_BF16 0
+#define KDA_DTYPE_F32 1
+
+#define KDA_GATE_PER_CHANNEL 0 /* g [.., H_v, d_k] */
+#define KDA_GATE_PER_HEAD 1    /* g [.., H_v], one gate per (token, value head) */
+
+/* Device-side error bits returned by kda_get_device_error. */
+#define KDA_DEVICE_ERR_SEQLENS 1 /* cu_seqlens out of order or out of [0, T] */
+
+/*
+ * kda_chunk_fwd — bf16 q, k, v, o with fp32 accumulation.
+ *
+ * q, k: [B, T, H_k, d_k] bf16; v: [B, T, H_v, d_v] bf16; g: [B, T, H_v, d_k] fp32 log
+ * gates; beta: [B, T, H_v] fp32; h0: [N, H_v, d_k, d_v] fp32 or NULL; o: [B, T, H_v, d_v]
+ * bf16 (written, rounded to nearest even); ht: [N, H_v, d_k, d_v] fp32 or NULL (written);
+ * B: batch (or number of packed sequences when cu_seqlens != NULL); T: tokens per
+ * sequence (or total tokens when packed); C: chunk length, must be 64; scale: multiplies
+ * the output only (commonly d_k^-1/2); cu_seqlens: device int32 [B + 1] or NULL;
+ * stream: CUDA stream the work is ordered on (0 = the legacy default stream).
+ */
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                  const float *beta, const float *h0, void *o, float *ht, int B, int T,
+                  int H_k, int H_v, int d_k, int d_v, int C, float scale,
+                  const int32_t *cu_seqlens, cudaStream_t stream);
+
+/*
+ * kda_chunk_fwd_f32 — the same operation and argument list with fp32 q, k, v and o,
+ * computed in fp32 throughout (no bf16 rounding anywhere).
+ */
+int kda_chunk_fwd_f32(const float *q, const float *k, const float *v, const float *g,
+                      const float *beta, const float *h0, float *o, float *ht, int B,
+                      int T, int H_k, int H_v, int d_k, int d_v, int C, float scale,
+                      const int32_t *cu_seqlens, cudaStream_t stream);
+
+/* Every argument of the two calls above, plus the dtype and the gate mode. */
+typedef struct kda_fwd_params {
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    void *o;
+    float *ht;
+    int B, T, H_k, H_v, d_k, d_v, C;
+    float scale;
+    const int32_t *cu_seqlens;
+    int dtype;     /* KDA_DTYPE_BF16 or KDA_DTYPE_F32 */
+    int gate_mode; /* KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD */
+    int flags;     /* reserved, must be 0 */
+} kda_fwd_params;
+
+/*
+ * kda_chunk_fwd_ex — the general entry point: dtype and gate mode chosen by the struct.
+ * The per-head gate mode reads g as [B, T, H_v] (the scalar-gate Gated DeltaNet), so the
+ * gate costs 4 bytes per (token, head) instead of 4 * d_k.
+ */
+int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream);
+
+/* A static, human-readable description of a status (and of the last CUDA error for
+ * KDA_ERR_CUDA on this thread). */
+const char *kda_status_string(int status);
+
+/*
+ * kda_get_device_error — synchronises `stream`, returns the device-side error bits
+ * (KDA_DEVICE_ERR_*) raised by kernels of this library on the current device since the
+ * last call, and clears them. Returns KDA_ERR_CUDA if the query itself fails.
+ */
+int kda_get_device_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

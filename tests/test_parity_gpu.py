@@ -1,0 +1,139 @@
+"""GPU parity: the CUDA path against the fp64 oracle, element by element.
+
+Small cases span several 64-token chunks with ragged tails, grouped heads, both gate
+modes, both dtypes, every (d_k, d_v) pair and the degenerate inputs (empty sequences,
+one-token sequences, beta = 0). The tolerance is relative L2 over the whole o tensor and
+over the whole ht tensor: 2e-2 for bf16 inputs with fp32 accumulation, 1e-5 for fp32.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from conftest import rel_l2
+from inputs import make_inputs
+from kda_cases import TOL, run_gpu, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(x, tag=""):
+    o, ht = run_gpu(x)
+    o_r, ht_r = run_oracle(x)
+    assert np.isfinite(o).all() and np.isfinite(ht).all()
+    e_o, e_h = rel_l2(o, o_r), rel_l2(ht, ht_r)
+    print(f"{tag} rel_l2 o={e_o:.3e} ht={e_h:.3e}")
+    tol = TOL[x.dtype]
+    assert e_o <= tol, (tag, e_o)
+    assert e_h <= tol, (tag, e_h)
+    return o, ht
+
+
+@pytest.mark.parametrize("d_k,d_v", [(128, 128), (64, 64), (64, 128), (128, 64)])
+def test_bf16_per_channel_ragged(d_k, d_v):
+    x = make_inputs((200,), 2, 2, d_k, d_v, seed=101, h0=True)
+    _check(x, f"bf16 dk{d_k} dv{d_v}")
+
+
+def test_bf16_varlen_gqa_edge_lengths():
+    x = make_inputs((1, 63, 64, 65, 130, 0, 7, 200), 2, 4, 128, 128, seed=102, h0=True, varlen=True,
+                    a_lo=0.8)
+    _check(x, "bf16 varlen gqa")
+
+
+def test_bf16_per_head_gate_matches_broadcast_channel_gate():
+    x = make_inputs((150, 150), 2, 2, 128, 128, seed=103, gate="head")
+    o_h, ht_h = _check(x, "bf16 per-head gate")
+    xb = make_inputs((150, 150), 2, 2, 128, 128, seed=103, gate="head")
+    xb.g = np.ascontiguousarray(np.repeat(xb.g[:, :, None], 128, axis=2))
+    xb.gate = "channel"
+    o_c, ht_c = run_gpu(xb)
+    assert rel_l2(o_c, o_h) < 1e-6 and rel_l2(ht_c, ht_h) < 1e-6
+
+
+def test_bf16_strong_gates_and_no_initial_state():
+    x = make_inputs((333,), 1, 2, 128, 128, seed=104, a_lo=0.8)
+    _check(x, "bf16 a>=0.8")
+
+
+def test_bf16_beta_zero_is_decay_of_h0():
+    x = make_inputs((130,), 1, 1, 128, 128, seed=105, h0=True)
+    x.beta[:] = 0.0
+    _check(x, "bf16 beta=0")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_f32_path(d):
+    x = make_inputs((256,), 1, 1, d, d, seed=106, dtype="f32")
+    _check(x, f"f32 d{d}")
+    y = make_inputs((70, 1, 129), 1, 2, d, d, seed=107, dtype="f32", h0=True, varlen=True,
+                    gate="head")
+    _check(y, f"f32 varlen d{d}")
+
+
+def test_empty_batch_keeps_initial_state():
+    import torch
+
+    from chunkwise_gated_linear_gb300 import chunk_kda_fwd
+
+    x = make_inputs((0,), 1, 2, 128, 128, seed=108, h0=True)
+    d = to_device(x)
+    o, ht = chunk_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], scale=x.scale)
+    torch.cuda.synchronize()
+    assert o.numel() == 0
+    np.testing.assert_array_equal(ht.cpu().numpy(), x.h0)
+
+
+def test_deterministic_and_dv_slices_independent():
+    import torch
+
+    from chunkwise_gated_linear_gb300 import chunk_kda_fwd
+
+    x = make_inputs((190,), 2, 2, 128, 128, seed=109, h0=True)
+    d = to_device(x)
+    o1, h1 = chunk_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], scale=x.scale)
+    o2, h2 = chunk_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], scale=x.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    # the d_v halves computed on their own give the same bits ("TileLang 实战：KDA 从零到一–
+    # Kimi Delta Attention" §3.4: slicing d_v introduces no dependence)
+    for s in (slice(0, 64), slice(64, 128)):
+        vs = d["v"][..., s].contiguous()
+        hs = d["h0"][..., s].contiguous()
+        os_, hts = chunk_kda_fwd(d["q"], d["k"], vs, d["g"], d["beta"], h0=hs, scale=x.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(os_, o1[..., s]) and torch.equal(hts, h1[..., s])
+
+
+def test_resume_from_final_state():
+    import torch
+
+    from chunkwise_gated_linear_gb300 import chunk_kda_fwd
+
+    x = make_inputs((256,), 1, 1, 128, 128, seed=110, h0=True)
+    d = to_device(x)
+    o, ht = chunk_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], scale=x.scale)
+    T1 = 128  # a chunk boundary: the split run follows the same chunking
+    cut = lambda t, a, b: t[:, a:b].contiguous()  # noqa: E731
+    o1, h1 = chunk_kda_fwd(cut(d["q"], 0, T1), cut(d["k"], 0, T1), cut(d["v"], 0, T1),
+                           cut(d["g"], 0, T1), cut(d["beta"], 0, T1), h0=d["h0"], scale=x.scale)
+    o2, h2 = chunk_kda_fwd(cut(d["q"], T1, 256), cut(d["k"], T1, 256), cut(d["v"], T1, 256),
+                           cut(d["g"], T1, 256), cut(d["beta"], T1, 256), h0=h1, scale=x.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([o1, o2], dim=1), o) and torch.equal(h2, ht)
+
+
+def test_malformed_cu_seqlens_raise_the_device_error():
+    import torch
+
+    from chunkwise_gated_linear_gb300 import chunk_kda_fwd, kda_get_device_error
+
+    x = make_inputs((64, 36), 1, 1, 128, 128, seed=111, varlen=True)
+    d = to_device(x)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert kda_get_device_error(stream) == 0
+    bad = torch.tensor([0, 90, 60], dtype=torch.int32, device="cuda")  # decreasing
+    chunk_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x.scale, cu_seqlens=bad)
+    assert kda_get_device_error(stream) == 1
+    assert kda_get_device_error(stream) == 0  # the query clears it
