@@ -43,8 +43,10 @@ cudaError_t device_error_ptr(unsigned int **out) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int run(const kda_fwd_params &p, cudaStream_t stream) {
-    if (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr || p.beta == nullptr ||
-        p.o == nullptr)
+    // With no tokens there is nothing to read or write but the states, so the token
+    // tensors may be empty (NULL).
+    if (p.T != 0 && (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr ||
+                     p.beta == nullptr || p.o == nullptr))
         return KDA_ERR_INVALID_ARG;
     if (p.B < 1 || p.T < 0 || p.H_k < 1 || p.H_v < 1 || p.H_v % p.H_k != 0) return KDA_ERR_INVALID_ARG;
     if (p.flags != 0) return KDA_ERR_INVALID_ARG;

@@ -40,7 +40,7 @@
  *   if cu_seqlens == NULL the batch holds B sequences of T tokens each (N = B).
  *
  * NULL conventions: h0 == NULL means a zero initial state; ht == NULL means the final
- *   state is not written. q, k, v, g, beta and o are required.
+ *   state is not written. q, k, v, g, beta and o are required unless T == 0.
  *
  * Sizes supported: d_k, d_v in {64, 128}; C == 64; B >= 1; T >= 0; H_k >= 1; H_v >= 1.
  *   T == 0 (or empty sequences) is valid: no o rows, ht = h0 (or 0).
