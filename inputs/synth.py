@@ -71,6 +71,12 @@ WORKLOADS = {
 
 WORKLOAD_SEEDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
 
+# Smaller cases of the same kernels for profiler captures (inputs still larger than L2).
+PROFILE_WORKLOADS = {
+    "kda_b1_t8192_h32_d128_bf16": Workload(
+        "kda_b1_t8192_h32_d128_bf16", (8192,), 32, 32, 128, 128, h0=True),
+}
+
 
 @dataclass
 class Inputs:
@@ -190,8 +196,8 @@ def make_inputs(lengths, H_k, H_v, d_k, d_v, *, dtype="bf16", gate="channel", a_
 
 def workload_inputs(name: str, seed: int | None = None) -> Inputs:
     """Inputs of one named workload (seed defaults to the workload's fixed seed)."""
-    w = WORKLOADS[name]
-    s = WORKLOAD_SEEDS[name] if seed is None else seed
+    w = WORKLOADS[name] if name in WORKLOADS else PROFILE_WORKLOADS[name]
+    s = WORKLOAD_SEEDS.get(name, 99) if seed is None else seed
     x = make_inputs(w.lengths, w.H_k, w.H_v, w.d_k, w.d_v, dtype=w.dtype, gate=w.gate,
                     a_lo=w.a_lo, h0=w.h0, varlen=w.varlen, seed=s,
                     len_range=w.len_range, n_seqs=w.n_seqs)
