@@ -10,6 +10,7 @@
 namespace kda {
 cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -84,7 +85,9 @@ int run(const kda_fwd_params &p, cudaStream_t stream) {
 
     cudaError_t e = device_error_ptr(&a.err);
     if (e == cudaSuccess)
-        e = p.dtype == KDA_DTYPE_BF16 ? kda::launch_fwd_bf16(a, stream) : kda::launch_fwd_f32(a, stream);
+        e = p.dtype == KDA_DTYPE_F32                 ? kda::launch_fwd_f32(a, stream)
+            : (p.d_k == 128 && p.d_v == 128)         ? kda::launch_fwd_tc(a, stream)
+                                                     : kda::launch_fwd_bf16(a, stream);
     if (e != cudaSuccess) {
         t_last_cuda_error = e;
         return KDA_ERR_CUDA;

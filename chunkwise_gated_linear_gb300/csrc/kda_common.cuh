@@ -10,6 +10,10 @@ namespace kda {
 
 constexpr int kChunk = 64;  // tokens per chunk (the only chunk length supported)
 
+// Device error bits, the same values as KDA_DEVICE_ERR_* in kda.h.
+constexpr unsigned int kDeviceErrSeqlens = 1u;
+constexpr unsigned int kDeviceErrTimeout = 2u;
+
 // Everything a forward kernel needs, resolved on the host.
 struct FwdArgs {
     const void *q, *k, *v;
@@ -36,7 +40,7 @@ __device__ __forceinline__ bool seq_bounds(const FwdArgs &a, int n, int64_t &bos
     }
     const int s = a.cu_seqlens[n], e = a.cu_seqlens[n + 1];
     if (s < 0 || e < s || e > a.T) {
-        if (threadIdx.x == 0) atomicOr(a.err, 1u);
+        if (threadIdx.x == 0) atomicOr(a.err, kDeviceErrSeqlens);
         return false;
     }
     bos = s;

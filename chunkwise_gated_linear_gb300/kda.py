@@ -25,6 +25,7 @@ KDA_DTYPE_F32 = 1
 KDA_GATE_PER_CHANNEL = 0
 KDA_GATE_PER_HEAD = 1
 KDA_DEVICE_ERR_SEQLENS = 1
+KDA_DEVICE_ERR_TIMEOUT = 2
 
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_ex", "kda_status_string",
             "kda_get_device_error")

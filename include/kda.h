@@ -77,6 +77,7 @@ extern "C" {
 
 /* Device-side error bits returned by kda_get_device_error. */
 #define KDA_DEVICE_ERR_SEQLENS 1 /* cu_seqlens out of order or out of [0, T] */
+#define KDA_DEVICE_ERR_TIMEOUT 2 /* a bounded wait inside a kernel gave up (about 1 s) */
 
 /*
  * kda_chunk_fwd — bf16 q, k, v, o with fp32 accumulation.
