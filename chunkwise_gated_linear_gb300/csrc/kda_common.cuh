@@ -57,6 +57,11 @@ __device__ __forceinline__ void cp_async_16(void *smem, const void *gmem, int sr
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
                  "l"(gmem), "r"(src_bytes));
 }
+// 4-byte global->shared copy; zero-filled when src_bytes is 0.
+__device__ __forceinline__ void cp_async_4(void *smem, const void *gmem, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(src_bytes));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
 

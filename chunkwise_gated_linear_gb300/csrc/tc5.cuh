@@ -127,6 +127,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
     return true;
 }
 
+// Expect `bytes` more transaction bytes on the barrier and arrive once.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// ---- TMA: 2-D tiled load global -> shared, completion counted on an mbarrier -------------
+// `tmap` is the generic address of a CUtensorMap held in kernel parameter space; (x, y) is
+// the box origin in elements (x innermost; x * element size must be a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2^x on the special-function unit (approximate, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- swizzled addressing -------------------------------------------------------------------
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128B-swizzled atom.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
