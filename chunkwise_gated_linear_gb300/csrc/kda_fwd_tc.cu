@@ -1,31 +1,32 @@
 // Chunkwise KDA forward for d_k = d_v = 128, bf16 operands, on the 5th-generation tensor
-// cores (tcgen05) with accumulators in tensor memory (TMEM).
+// cores (tcgen05) with accumulators in tensor memory (TMEM), warp-specialised.
 //
-// One CTA of 256 threads runs one (sequence, value head) unit through all its chunks.
-// Every product is arranged so that the tensor core's M dimension is 128 (the d_k or d_v
-// axis, or the stacked [Kp; Qp] rows), so each MMA runs at full width:
+// One CTA of 384 threads runs one (sequence, value head) unit through all its chunks. Per
+// chunk ("RNN的复兴04:线性注意力并行计算DPLR", §5.3.5; "TileLang 实战：KDA 从零到一–Kimi
+// Delta Attention", §3.3) the work splits into a part that depends only on the chunk's own
+// inputs ("prep") and the serial step that carries the state. Eight prep warps build
+// chunk c + 1 while the four serial warps run chunk c:
 //
-//   Gram      D_G [128 x 64]  = [Qp; Kp] Km^T          rows 0-63: Aqk, rows 64-127: M
-//   WY        D_W [128 x 64]  = Kp^T T_beta^T           (W^T, d_k x tokens)
-//             D_U [128 x 64]  = V^T  T_beta^T           (U^T, d_v x tokens)
-//   serial    D_X [128 x 128] = S^T [W^T | Qp^T]         (one pass over S)
-//             Vt^T = U^T - D_X[:, :64]                   (in registers, then bf16)
-//             D_X[:, 64:] += Vt^T Aqk^T                  (O^T, d_v x tokens)
-//             D_S  = Kbar^T Vt                           (the chunk's state increment)
+//   prep (warps 4-11), chunk c:
+//     TMA    Q, K [64 x 128], V [64 x 128] (128-byte swizzled), G [64 x 128] fp32
+//     gate   gamma = chunk-local cumulative log2 gate; Qp = scale Q e^gamma, Kp = K e^gamma,
+//            Km = K e^-gamma, Kbar = Km e^gamma_n, all stored transposed [d][tok] in bf16
+//     Gram   D_G [128 x 64] = [Qp; Kp] Km^T   -> Aqk (lower) in bf16, L = diag(beta) M (strict)
+//     solve  T = (I + L)^-1: 16x16 diagonal blocks by forward substitution, off-diagonal
+//            blocks column by column on tf32 mma.sync; T_beta = T diag(beta) in bf16
+//     WY     D_W = Kp^T T_beta^T (W^T), D_U = V^T T_beta^T (U^T, left in TMEM)
+//   serial (warps 0-3, thread = d_v row), chunk c, state S^T [d_v x d_k] fp32 in TMEM:
+//     D_X [128 x 128] = S^T [W^T | Qp^T]           (S^T as a bf16 TMEM operand)
+//     S^T <- S^T Diag(e^gamma_n)                    (in TMEM, while D_X is computed)
+//     Vt^T = U^T - D_X[:, :64]  -> bf16 TMEM operand
+//     D_X[:, 64:] += Vt^T Aqk^T (= O^T);  S^T += Vt^T Kbar
 //
-// and S <- Diag(e^gamma_n) S + D_S is applied in fp32 registers by the 128 threads of
-// warpgroup 0, thread d owning row d of S (d_k x d_v) across the whole sequence. Per chunk
-// ("RNN的复兴04:线性注意力并行计算DPLR", §5.3.5; "TileLang 实战：KDA 从零到一–Kimi Delta
-// Attention", §3.3): the cumulative log2 gate and the decayed operands (gate pass), the
-// Gram matrix, the UT-transform inverse T = (I + diag(beta) M)^-1 (16x16 diagonal blocks by
-// forward substitution, then the off-diagonal blocks column by column with tf32 mma.sync,
-// one warp per 8 columns), T_beta = T diag(beta), the WY
-// factors, and the serial step. All operands live in shared memory in the 128-byte-swizzled
-// layouts the tensor core reads; nothing but q, k, v, g, beta, h0 (in) and o, ht (out)
-// touches HBM.
+// The prep -> serial hand-off (Qp^T, Kbar^T, Aqk, e^gamma_n, U^T) is double-buffered; W^T
+// is single-buffered behind a release barrier. All operands stay in shared memory or TMEM;
+// only q, k, v, g, beta, h0 (in) and o, ht (out) touch HBM.
 //
 // Every mbarrier wait is bounded (about one second); on a timeout the CTA raises
-// KDA_DEVICE_ERR_TIMEOUT, waits (bounded) for its issued MMAs, frees its TMEM and returns.
+// KDA_DEVICE_ERR_TIMEOUT, waits (bounded) for the MMAs it issued, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -44,39 +45,60 @@ using namespace tc5;
 
 // Shared-memory plan (byte offsets from a 1024-byte aligned base). Tiles named [d][tok]
 // hold one row per d_k channel and 64 tokens per 128-byte row (one swizzle atom).
-struct TcLayout {
-    static constexpr int oRQ = 0;       // raw Q [64 tok][128] bf16 row-major
-    static constexpr int oRK = 16384;   // raw K
-    static constexpr int oRV = 32768;   // raw V, [2 atoms (d_v)][64 tok rows][128 B] (MN-major A of U^T)
-    static constexpr int oWT = 49152;   // W^T [d][tok]    } one N = 128 B operand (W^T | Qp^T)
-    static constexpr int oQP = 65536;   // Qp^T [d][tok]   } and one M = 128 A operand (Qp | Kp)
-    static constexpr int oKP = 81920;   // Kp^T [d][tok]   }
-    static constexpr int oKM = 98304;   // Km^T [d][tok]; then Aqk [tok][tok'] (8 KB) + T_beta (8 KB);
-    static constexpr int oAQ = oKM;     //   then the O staging tile [64 tok][128] bf16
-    static constexpr int oTB = oKM + 8192;
-    static constexpr int oOS = oKM;
-    static constexpr int oKB = 114688;  // Kbar^T [d][tok]
-    static constexpr int oSB = 131072;  // S in bf16: [2 atoms (d_v)][128 rows (d_k)][128 B]
-    static constexpr int oVB = 163840;  // Vt^T in bf16: [128 rows (d_v)][128 B (tok)]
-    static constexpr int oG = 180224;   // raw G fp32 [64][128]; then L and T fp32 [64][68]
+struct WsLayout {
+    static constexpr int oRQ = 0;        // raw Q [64 tok][128] bf16 row-major; then solve scratch
+    static constexpr int oRK = 16384;    // raw K
+    static constexpr int oRV = 32768;    // raw V [2 atoms (d_v)][64 tok][128 B] (MN-major A of U^T)
+    static constexpr int oG = 49152;     // raw G fp32 [64][128]; then L and T fp32 [64][68]
     static constexpr int oL = oG;
     static constexpr int oT = oG + 17408;
-    static constexpr int oBeta = oG + 34816;  // [64] fp32 (raw per-head gates follow at +256)
+    static constexpr int oWT = 83968;    // W^T [d][tok]        } WT, QP0, QP1, KP in this order:
+    static constexpr int oQP0 = 100352;  // Qp^T [d][tok], slot 0} serial B operand (WT | QP[b]),
+    static constexpr int oQP1 = 116736;  // Qp^T, slot 1          } Gram A operand (QP[b] | KP)
+    static constexpr int oKP = 133120;   // Kp^T [d][tok]
+    static constexpr int oKM = 149504;   // Km^T [d][tok]; after the Gram, T_beta at +8192
+    static constexpr int oTB = oKM + 8192;
+    static constexpr int oKB0 = 165888;  // Kbar^T [d][tok], slots 0 and 1
+    static constexpr int oKB1 = 182272;
+    static constexpr int oAQ0 = 198656;  // Aqk [tok][tok'] bf16 (K-major B), slots 0 and 1
+    static constexpr int oAQ1 = 206848;
+    static constexpr int oBeta = 215040;  // [64] fp32
     static constexpr int oGh = oBeta + 256;   // [64] fp32 per-head gates
     static constexpr int oTot = oGh + 256;    // [4][128] fp32 partial gate sums
-    static constexpr int oEg = oTot + 2048;   // [128] fp32 e^gamma_n
-    static constexpr int oBar = oEg + 512;
-    static constexpr int oTmemAddr = oBar + 64;
-    static constexpr int kBytes = oTmemAddr + 16 + 1024;  // + slack to align the base
+    static constexpr int oEG0 = oTot + 2048;  // [128] fp32 e^gamma_n, slots 0 and 1
+    static constexpr int oEG1 = oEG0 + 512;
+    static constexpr int oBar = oEG1 + 512;   // mbarriers
+    static constexpr int oTmemAddr = oBar + 256;
+    static constexpr int oFlag = oTmemAddr + 16;  // abort flag
+    static constexpr int kBytes = oFlag + 16 + 1024;  // + slack to align the base
 };
 constexpr int LDF = 68;  // fp32 row stride of L and T
 
-// TMEM columns: Gram, W^T, U^T, [S^T W^T | O^T], state increment
-constexpr uint32_t tG = 0, tW = 64, tU = 128, tX = 192, tO = 256, tS = 320;
+// TMEM columns (512 allocated)
+constexpr uint32_t tGW = 0;    // Gram D_G, then W^T (prep)
+constexpr uint32_t tU0 = 64;   // U^T, slot 0 (64) ; slot 1 at tU1
+constexpr uint32_t tX = 128;   // [S^T W^T | O^T] (128); Vt^T in bf16 overwrites cols 0-31
+constexpr uint32_t tSA = 256;  // S^T in bf16 (64 packed columns)
+constexpr uint32_t tS = 320;   // S^T fp32 (128)
+constexpr uint32_t tU1 = 448;  // U^T, slot 1 (64)
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 1ll << 31;  // about one second
 
-enum { BAR_G = 0, BAR_W, BAR_V, BAR_S, BAR_Z, BAR_L, kNumBars };
+enum {
+    BAR_L = 0,   // TMA tiles of the next chunk
+    BAR_G,       // Gram MMA done
+    BAR_W,       // WY MMAs done
+    BAR_FULL0,   // hand-off slot 0 / 1 ready (prep -> serial)
+    BAR_FULL1,
+    BAR_FREE0,   // hand-off slot 0 / 1 consumed (serial -> prep)
+    BAR_FREE1,
+    BAR_WT,      // W^T consumed (serial -> prep)
+    BAR_X,       // serial product D_X done
+    BAR_S2,      // serial products O^T, S^T done
+    BAR_Z0,      // drains after a timeout (one per MMA-issuing thread)
+    BAR_Z1,
+    kNumBars
+};
 
 // Tensor maps of the per-chunk tiles (TMA): q, k [tokens][H_k*128] bf16 (box 128 x 64),
 // v [tokens][H_v*128] bf16 (box 64 x 64, 128-byte swizzle), g [tokens][H_v*128] fp32 (box 128 x 64).
@@ -143,12 +165,63 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     }
 }
 
+__device__ __forceinline__ void bar_serial() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait on an mbarrier phase; gives up early when the CTA is aborting. On its own
+// timeout it marks the CTA as aborting. Returns false when the phase did not complete.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+// OR of `v` over the `count` threads of named barrier `id` (all of them take the same branch).
+__device__ __forceinline__ bool bar_or(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t"
+        "}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+struct Unit {
+    unsigned char *sm;
+    uint32_t sbase, tmem;
+    int h, hk, n, len, nchunks;
+    int64_t bos;
+    uint64_t *bars;
+    volatile int *abort_flag;
+};
+
+// ---------------------------------------------------------------------------------------
+// prep warps (4-11): TMA staging, gate pass, Gram, solve, WY factors for every chunk.
+// Returns the mbarrier parity of a TMA that may still be in flight, or -1 (abort path).
+// ---------------------------------------------------------------------------------------
 template <bool GATE_HEAD>
-__global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, const __grid_constant__ TcMaps maps) {
-    using Lay = TcLayout;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sbase = smem_u32(sm);
+__device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, const Unit &u) {
+    using Lay = WsLayout;
+    unsigned char *sm = u.sm;
+    const uint32_t sbase = u.sbase, tmem = u.tmem;
+    uint64_t *bars = u.bars;
+    const int ptid = threadIdx.x - 128, pw = ptid >> 5, lane = ptid & 31, warp = threadIdx.x >> 5;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
+    const uint32_t half = (uint32_t)(pw >> 2) * 32u;                // column half of a 64-wide readback
     const bf16 *RQ = reinterpret_cast<const bf16 *>(sm + Lay::oRQ);
     const bf16 *RK = reinterpret_cast<const bf16 *>(sm + Lay::oRK);
     float *G = reinterpret_cast<float *>(sm + Lay::oG);
@@ -157,68 +230,16 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
     float *Bs = reinterpret_cast<float *>(sm + Lay::oBeta);
     float *Gh = reinterpret_cast<float *>(sm + Lay::oGh);
     float *Tot = reinterpret_cast<float *>(sm + Lay::oTot);
-    float *Eg = reinterpret_cast<float *>(sm + Lay::oEg);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::oBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::oTmemAddr);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y, n = blockIdx.z;
-    const int hk = h / a.group;
-
-    int64_t bos;
-    int len;
-    if (!seq_bounds(a, n, bos, len)) return;
-    const int nchunks = (len + kChunk - 1) / kChunk;
-
-    bf16 *o = static_cast<bf16 *>(a.o);
-    const int64_t sv = (int64_t)a.H_v * 128;
+    const int h = u.h, hk = u.hk, len = u.len, nchunks = u.nchunks;
+    const int64_t bos = u.bos;
     const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * 128;
-
-    if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
-        mbar_fence_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-
-    // State: warpgroup 0, thread d owns row d of S (fp32, d_v = 128 values).
-    float S[128];
-    if (tid < 128) {
-        if (a.h0 != nullptr) {
-            const float4 *h0 = reinterpret_cast<const float4 *>(a.h0 + (((int64_t)n * a.H_v + h) * 128 + tid) * 128);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float4 x = h0[j];
-                S[4 * j] = x.x;
-                S[4 * j + 1] = x.y;
-                S[4 * j + 2] = x.z;
-                S[4 * j + 3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 128; ++j) S[j] = 0.f;
-        }
-    }
-    // S in bf16, MN-major A operand of S^T: element (m = dv, k = d) at atom dv/64, row d.
-    auto write_SB = [&]() {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = S[8 * c + e];
-            *reinterpret_cast<uint4 *>(sm + Lay::oSB + (c >> 3) * 16384 + sw128(tid, c & 7)) = pack8(x);
-        }
-    };
-    if (tid < 128) write_SB();
-
-    // Stage chunk c: Q, K, V and G by TMA (thread 0), beta and per-head gates by cp.async.
     constexpr uint32_t kTileBytes = 3 * 16384 + (GATE_HEAD ? 0 : 32768);
+
+    // Stage chunk c: Q, K, V and G by TMA (one thread), beta and per-head gates by cp.async.
     auto stage = [&](int c) {
         const int row0 = c * kChunk;
         const int nvalid = min(kChunk, len - row0);
-        if (tid == 0) {
+        if (ptid == 0) {
             const int y = (int)(bos + row0);
             mbar_arrive_expect_tx(&bars[BAR_L], kTileBytes);
             tma_load_2d(sm + Lay::oRQ, &maps.q, &bars[BAR_L], hk * 128, y);
@@ -227,12 +248,12 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
             tma_load_2d(sm + Lay::oRV + 8192, &maps.v, &bars[BAR_L], h * 128 + 64, y);
             if constexpr (!GATE_HEAD) tma_load_2d(sm + Lay::oG, &maps.g, &bars[BAR_L], h * 128, y);
         }
-        if (tid < 64) {
-            const bool ok = tid < nvalid;
-            const int64_t ob = ok ? (bos + row0 + tid) * a.H_v + h : 0;
-            cp_async_4(Bs + tid, a.beta + ob, ok ? 4 : 0);
-        } else if (GATE_HEAD && tid < 128) {
-            const int r = tid - 64;
+        if (ptid < 64) {
+            const bool ok = ptid < nvalid;
+            const int64_t ob = ok ? (bos + row0 + ptid) * a.H_v + h : 0;
+            cp_async_4(Bs + ptid, a.beta + ob, ok ? 4 : 0);
+        } else if (GATE_HEAD && ptid < 128) {
+            const int r = ptid - 64;
             const bool ok = r < nvalid;
             const int64_t og = ok ? (bos + row0 + r) * sg + h : 0;
             cp_async_4(Gh + r, a.g + og, ok ? 4 : 0);
@@ -240,28 +261,34 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
         cp_async_commit();
     };
 
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (nchunks > 0) stage(0);
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
-    const uint32_t half = (uint32_t)(warp >> 2) * 32u;              // column half of a 64-wide readback
     bool failed = false;
-
-    for (int c = 0; c < nchunks && !failed; ++c) {
-        const int row0 = c * kChunk;
+    int tma_pending = -1;  // parity of the staged chunk not yet waited for
+    if (nchunks > 0) {
+        stage(0);
+        tma_pending = 0;
+    }
+    for (int p = 0; p < nchunks; ++p) {
+        const int row0 = p * kChunk;
         const int nvalid = min(kChunk, len - row0);
-        const uint32_t par = (uint32_t)(c & 1);
+        const int b = p & 1;
+        const uint32_t oQP = b ? Lay::oQP1 : Lay::oQP0;
+        const uint32_t oKB = b ? Lay::oKB1 : Lay::oKB0;
+        const uint32_t oAQ = b ? Lay::oAQ1 : Lay::oAQ0;
+        float *EG = reinterpret_cast<float *>(sm + (b ? Lay::oEG1 : Lay::oEG0));
+        const uint32_t tU = b ? tU1 : tU0;
+
+        // tiles of chunk p, and hand-off slot b released by the serial step of chunk p - 2
         cp_async_wait_all();
-        failed = !mbar_wait(&bars[BAR_L], par, kWaitCycles);
-        if (__syncthreads_or(failed)) { failed = true; break; }
+        failed = !wait_bar(&bars[BAR_L], (uint32_t)(p & 1), u.abort_flag);
+        if (!failed && p >= 2)
+            failed = !wait_bar(&bars[b ? BAR_FREE1 : BAR_FREE0], (uint32_t)(((p >> 1) - 1) & 1), u.abort_flag);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
+        tma_pending = -1;
         if (nvalid < kChunk) {
             // the boxes read on past the sequence end (the next sequence, or zeros past the
             // tensor): those rows must be zero in every operand
             const int nz = kChunk - nvalid;
-            for (int i = tid; i < nz * 16; i += 256) {
+            for (int i = ptid; i < nz * 16; i += 256) {
                 const int r = nvalid + (i >> 4), c16 = i & 15;
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4 *>(sm + Lay::oRQ + r * 256 + c16 * 16) = z;
@@ -273,14 +300,14 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
                 }
             }
             fence_proxy_async();
-            __syncthreads();
+            bar_prep();
         }
 
         // ---- gate pass ---------------------------------------------------------------------
-        // warp w: rows 16 (w >> 1) .. +15, channels c0 = 64 (w & 1) + lane and c1 = c0 + 32.
+        // prep warp pw: rows 16 (pw >> 1) .. +15, channels c0 = 64 (pw & 1) + lane and c0 + 32.
         {
-            const int qr = warp >> 1;
-            const int c0 = 64 * (warp & 1) + lane, c1 = c0 + 32;
+            const int qr = pw >> 1;
+            const int c0 = 64 * (pw & 1) + lane, c1 = c0 + 32;
             float gl0[16], gl1[16];
             float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
@@ -299,7 +326,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
             }
             Tot[qr * 128 + c0] = acc0;
             Tot[qr * 128 + c1] = acc1;
-            __syncthreads();
+            bar_prep();
             float off0 = 0.f, off1 = 0.f, gn0 = 0.f, gn1 = 0.f;
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
@@ -313,12 +340,12 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
             }
             const float eg0 = ex2(gn0), eg1 = ex2(gn1);
             if (qr == 0) {
-                Eg[c0] = eg0;
-                Eg[c1] = eg1;
+                EG[c0] = eg0;
+                EG[c1] = eg1;
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int tc = 2 * qr + j;  // 16-byte chunk (8 tokens) within a 64-token row
+                const int tc = 2 * qr + j;  // 16-byte chunk (8 tokens) of a 64-token row
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     const int cc = ch ? c1 : c0;
@@ -338,32 +365,33 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
                     }
                     const uint32_t sw = sw128(cc, tc);
                     *reinterpret_cast<uint4 *>(sm + Lay::oKP + sw) = pack8(kp);
-                    *reinterpret_cast<uint4 *>(sm + Lay::oQP + sw) = pack8(qp);
+                    *reinterpret_cast<uint4 *>(sm + oQP + sw) = pack8(qp);
                     *reinterpret_cast<uint4 *>(sm + Lay::oKM + sw) = pack8(km);
-                    *reinterpret_cast<uint4 *>(sm + Lay::oKB + sw) = pack8(kb);
+                    *reinterpret_cast<uint4 *>(sm + oKB + sw) = pack8(kb);
                 }
             }
         }
         fence_proxy_async();
-        __syncthreads();
+        bar_prep();
 
         // ---- Gram: D_G = [Qp; Kp] Km^T  (rows 0-63: Aqk, rows 64-127: M) --------------------
-        if (tid == 0) {
+        if (ptid == 0) {
             fence_after_sync();
             const uint32_t id = idesc_bf16(128, 64, true, true, false);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma(tmem + tG, dMN(sbase + Lay::oQP, 16384, s), dMN(sbase + Lay::oKM, 16384, s), id, s > 0);
+                mma(tmem + tGW, dMN(sbase + oQP, (uint32_t)(Lay::oKP - oQP), s), dMN(sbase + Lay::oKM, 16384, s), id,
+                    s > 0);
             commit(&bars[BAR_G]);
         }
-        failed = !mbar_wait(&bars[BAR_G], par, kWaitCycles);
+        failed = !wait_bar(&bars[BAR_G], (uint32_t)(p & 1), u.abort_flag);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
         fence_after_sync();
-        if (__syncthreads_or(failed)) { failed = true; break; }
         {
-            // each warpgroup reads 32 of the 64 columns of its lane's row
-            const int row = tid & 127;
+            // each warp half reads 32 of the 64 columns of its lane's row
+            const int row = 32 * (warp & 3) + lane;
             float x[32];
-            tmem_ld32(tmem + lane_off + tG + half, x);
+            tmem_ld32(tmem + lane_off + tGW + half, x);
             if (row < 64) {
                 // Aqk (lower, diagonal included) -> bf16 [tok][tok'], K-major B operand
 #pragma unroll
@@ -374,7 +402,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
                         const int col = (int)half + 8 * c8 + e;
                         y[e] = col <= row ? x[8 * c8 + e] : 0.f;
                     }
-                    *reinterpret_cast<uint4 *>(sm + Lay::oAQ + sw128(row, (int)(half >> 3) + c8)) = pack8(y);
+                    *reinterpret_cast<uint4 *>(sm + oAQ + sw128(row, (int)(half >> 3) + c8)) = pack8(y);
                 }
             } else {
                 // L = diag(beta) strict_lower(M), fp32
@@ -394,12 +422,12 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
         }
         fence_proxy_async();
         fence_before_sync();
-        __syncthreads();
+        bar_prep();
 
         // ---- solve: T = (I + L)^-1 -----------------------------------------------------------
-        // D = blockdiag of the 16x16 diagonal inverses (forward substitution, one column per lane)
-        if (warp < 4 && lane < 16) {
-            const int b0 = 16 * warp, j = lane;
+        // the 16x16 diagonal inverses by forward substitution, one column per lane
+        if (pw < 4 && lane < 16) {
+            const int b0 = 16 * pw, j = lane;
             float x[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
@@ -411,25 +439,31 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
 #pragma unroll
             for (int r = 0; r < 16; ++r) Tm[(b0 + r) * LDF + b0 + j] = x[r];
         }
-        __syncthreads();
-        // Off-diagonal blocks column by column: warp w owns the 8 columns col0..col0+7 of T
-        // (column block j = w / 2). T_jj = D_j, and for i > j
+        bar_prep();
+        // Off-diagonal blocks column by column: prep warp pw owns the 8 columns col0..col0+7
+        // of T (column block j = pw / 2). T_jj = D_j, and for i > j
         //   T_ij = -D_i sum_{k=j}^{i-1} L_ik T_kj
-        // (tf32 mma.sync, fp32 accumulation). The warp then writes its columns of
-        // T_beta = T diag(beta) (lower triangle) in bf16. No CTA-wide barrier is needed:
-        // each warp only reads L, the diagonal blocks and its own columns.
+        // (tf32 mma.sync, fp32 accumulation, one accumulator per k so that the products of a
+        // step run side by side). The warp then writes its columns of T_beta = T diag(beta)
+        // (lower triangle) in bf16. Each warp reads only L, the diagonal blocks and its own
+        // columns, so no CTA-wide barrier is needed inside.
         {
-            const int j = warp >> 1, col0 = 16 * j + 8 * (warp & 1);
+            const int j = pw >> 1, col0 = 16 * j + 8 * (pw & 1);
             const int g8 = lane >> 2, t4 = lane & 3;
-            float *P = reinterpret_cast<float *>(sm + Lay::oRQ) + warp * 128;  // 16x8 scratch
+            float *P = reinterpret_cast<float *>(sm + Lay::oRQ) + pw * 128;  // 16x8 scratch
             for (int i = j + 1; i < 4; ++i) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int kb = j; kb < i; ++kb)
-                    mm16x8_tf32(acc, L + (16 * i) * LDF + 16 * kb, LDF, Tm + (16 * kb) * LDF + col0, LDF, lane);
-                P[g8 * 8 + 2 * t4] = acc[0];
-                P[g8 * 8 + 2 * t4 + 1] = acc[1];
-                P[(g8 + 8) * 8 + 2 * t4] = acc[2];
-                P[(g8 + 8) * 8 + 2 * t4 + 1] = acc[3];
+                float acc[3][4];
+#pragma unroll
+                for (int kk = 0; kk < 3; ++kk) acc[kk][0] = acc[kk][1] = acc[kk][2] = acc[kk][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 3; ++kk)
+                    if (j + kk < i)
+                        mm16x8_tf32(acc[kk], L + (16 * i) * LDF + 16 * (j + kk), LDF, Tm + (16 * (j + kk)) * LDF + col0,
+                                    LDF, lane);
+                P[g8 * 8 + 2 * t4] = acc[0][0] + acc[1][0] + acc[2][0];
+                P[g8 * 8 + 2 * t4 + 1] = acc[0][1] + acc[1][1] + acc[2][1];
+                P[(g8 + 8) * 8 + 2 * t4] = acc[0][2] + acc[1][2] + acc[2][2];
+                P[(g8 + 8) * 8 + 2 * t4 + 1] = acc[0][3] + acc[1][3] + acc[2][3];
                 __syncwarp();
                 float acc2[4] = {0.f, 0.f, 0.f, 0.f};
                 mm16x8_tf32(acc2, Tm + (16 * i) * LDF + 16 * i, LDF, P, 8, lane);
@@ -461,29 +495,31 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
             }
         }
         fence_proxy_async();
-        __syncthreads();
+        bar_prep();
 
         // ---- WY factors: D_W = Kp^T T_beta^T, D_U = V^T T_beta^T ------------------------------
-        if (tid == 0) {
+        if (ptid == 0) {
             fence_after_sync();
             const uint32_t idw = idesc_bf16(128, 64, false, false, false);
             const uint32_t idu = idesc_bf16(128, 64, true, false, false);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint64_t b = dK(sbase + Lay::oTB, 8192, s);
-                mma(tmem + tW, dK(sbase + Lay::oKP, 16384, s), b, idw, s > 0);
-                mma(tmem + tU, dMN(sbase + Lay::oRV, 8192, s), b, idu, s > 0);
+                const uint64_t bd = dK(sbase + Lay::oTB, 8192, s);
+                mma(tmem + tGW, dK(sbase + Lay::oKP, 16384, s), bd, idw, s > 0);
+                mma(tmem + tU, dMN(sbase + Lay::oRV, 8192, s), bd, idu, s > 0);
             }
             commit(&bars[BAR_W]);
         }
-        failed = !mbar_wait(&bars[BAR_W], par, kWaitCycles);
+        // W^T is single-buffered: the serial product of chunk p - 1 must have read it
+        failed = !wait_bar(&bars[BAR_W], (uint32_t)(p & 1), u.abort_flag);
+        if (!failed && p >= 1) failed = !wait_bar(&bars[BAR_WT], (uint32_t)((p - 1) & 1), u.abort_flag);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
         fence_after_sync();
-        if (__syncthreads_or(failed)) { failed = true; break; }
         {
-            // W^T row d -> bf16 [d][tok] (MN-major B); each warpgroup writes 32 of the 64 tokens
-            const int d = tid & 127;
+            // W^T row d -> bf16 [d][tok] (MN-major B); each warp half writes 32 of the 64 tokens
+            const int d = 32 * (warp & 3) + lane;
             float x[32];
-            tmem_ld32(tmem + lane_off + tW + half, x);
+            tmem_ld32(tmem + lane_off + tGW + half, x);
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
                 float y[8];
@@ -494,119 +530,234 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_tc_kernel(const FwdArgs a, con
         }
         fence_before_sync();
         fence_proxy_async();
-        __syncthreads();
-        // every raw tile is consumed: stage the next chunk behind the serial step
-        if (c + 1 < nchunks) stage(c + 1);
+        bar_prep();
+        // every raw tile is consumed: stage the next chunk, then hand chunk p to the serial warps
+        if (p + 1 < nchunks) {
+            stage(p + 1);
+            tma_pending = (p + 1) & 1;
+        }
+        if (ptid == 0) mbar_arrive(&bars[b ? BAR_FULL1 : BAR_FULL0]);
+    }
+    if (failed) *u.abort_flag = 1;
+    return tma_pending;
+}
 
-        // ---- serial step, part 1: D_X = S^T [W^T | Qp^T] -----------------------------------
-        if (tid == 0) {
-            fence_after_sync();
-            const uint32_t id = idesc_bf16(128, 128, true, true, false);
+// ---------------------------------------------------------------------------------------
+// serial warps (0-3): thread dv owns row dv of S^T (fp32 in TMEM) for the whole sequence.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void serial_role(const FwdArgs &a, const Unit &u) {
+    using Lay = WsLayout;
+    unsigned char *sm = u.sm;
+    const uint32_t sbase = u.sbase, tmem = u.tmem;
+    uint64_t *bars = u.bars;
+    const int dv = threadIdx.x, warp = dv >> 5;
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const int h = u.h, n = u.n, len = u.len, nchunks = u.nchunks;
+    const int64_t bos = u.bos;
+    const int64_t sv = (int64_t)a.H_v * 128;
+    bf16 *o = static_cast<bf16 *>(a.o);
+
+    // S^T row dv (from h0, or zero) -> TMEM fp32, and its bf16 copy (the MMA operand)
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int d = 32 * pass + e;
+            x[e] = a.h0 ? a.h0[(((int64_t)n * a.H_v + h) * 128 + d) * 128 + dv] : 0.f;
+        }
+        uint32_t f0[16], f1[16], p16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            f0[e] = __float_as_uint(x[e]);
+            f1[e] = __float_as_uint(x[16 + e]);
+            p16[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+        }
+        tmem_st16(tmem + lane_off + tS + 32 * pass, f0);
+        tmem_st16(tmem + lane_off + tS + 32 * pass + 16, f1);
+        tmem_st16(tmem + lane_off + tSA + 16 * pass, p16);
+    }
+    tmem_st_wait();
+    fence_before_sync();
+    bar_serial();
+
+    bool failed = false;
+    for (int c = 0; c < nchunks; ++c) {
+        const int row0 = c * kChunk;
+        const int nvalid = min(kChunk, len - row0);
+        const int b = c & 1;
+        const uint32_t oQP = b ? Lay::oQP1 : Lay::oQP0;
+        const uint32_t oKB = b ? Lay::oKB1 : Lay::oKB0;
+        const uint32_t oAQ = b ? Lay::oAQ1 : Lay::oAQ0;
+        const float *EG = reinterpret_cast<const float *>(sm + (b ? Lay::oEG1 : Lay::oEG0));
+        const uint32_t tU = b ? tU1 : tU0;
+
+        failed = !wait_bar(&bars[b ? BAR_FULL1 : BAR_FULL0], (uint32_t)((c >> 1) & 1), u.abort_flag);
+        if (bar_or(1, 128, failed)) { failed = true; break; }
+        fence_after_sync();
+
+        // D_X = S^T [W^T | Qp^T]  (A: S^T bf16 in TMEM; B: the W^T and Qp^T tiles, MN-major)
+        if (dv == 0) {
+            const uint32_t id = idesc_bf16(128, 128, false, true, false);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma(tmem + tX, dMN(sbase + Lay::oSB, 16384, s), dMN(sbase + Lay::oWT, 16384, s), id, s > 0);
-            commit(&bars[BAR_V]);
+                mma_ts(tmem + tX, tmem + tSA + 8 * s, dMN(sbase + Lay::oWT, (uint32_t)(oQP - Lay::oWT), s), id,
+                       s > 0);
+            commit(&bars[BAR_X]);
         }
-        failed = !mbar_wait(&bars[BAR_V], par, kWaitCycles);
-        fence_after_sync();
-        if (__syncthreads_or(failed)) { failed = true; break; }
-        {
-            // Vt^T = U^T - S^T W^T, row dv -> bf16 [dv][tok]; each warpgroup does 32 tokens
-            const int dv = tid & 127;
-            float u[32], p[32];
-            tmem_ld32(tmem + lane_off + tU + half, u);
-            tmem_ld32(tmem + lane_off + tX + half, p);
+        // meanwhile S^T <- S^T Diag(e^gamma_n): column d of S^T scales by e^gamma_n[d]
+#pragma unroll 1
+        for (int pass = 0; pass < 4; ++pass) {
+            float x[32];
+            tmem_ld32(tmem + lane_off + tS + 32 * pass, x);
+            uint32_t y0[16], y1[16];
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = u[8 * c8 + e] - p[8 * c8 + e];
-                *reinterpret_cast<uint4 *>(sm + Lay::oVB + sw128(dv, (int)(half >> 3) + c8)) = pack8(y);
+            for (int e = 0; e < 16; ++e) {
+                y0[e] = __float_as_uint(x[e] * EG[32 * pass + e]);
+                y1[e] = __float_as_uint(x[16 + e] * EG[32 * pass + 16 + e]);
             }
+            tmem_st16(tmem + lane_off + tS + 32 * pass, y0);
+            tmem_st16(tmem + lane_off + tS + 32 * pass + 16, y1);
         }
-        fence_before_sync();
-        fence_proxy_async();
-        __syncthreads();
+        tmem_st_wait();
 
-        // ---- serial step, part 2: O^T += Vt^T Aqk^T;  D_S = Kbar^T Vt -----------------------
-        if (tid == 0) {
+        failed = !wait_bar(&bars[BAR_X], (uint32_t)(c & 1), u.abort_flag);
+        if (bar_or(1, 128, failed)) { failed = true; break; }
+        fence_after_sync();
+        if (dv == 0) mbar_arrive(&bars[BAR_WT]);  // W^T is no longer needed
+        // Vt^T = U^T - S^T W^T -> bf16 pairs over tokens, written over D_X columns 0-31
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            float uu[32], pp[32];
+            tmem_ld32(tmem + lane_off + tU + 32 * pass, uu);
+            tmem_ld32(tmem + lane_off + tX + 32 * pass, pp);
+            uint32_t v16[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v16[e] = pack_bf16(uu[2 * e] - pp[2 * e], uu[2 * e + 1] - pp[2 * e + 1]);
+            tmem_st16(tmem + lane_off + tX + 16 * pass, v16);
+        }
+        tmem_st_wait();
+        fence_before_sync();
+        bar_serial();
+
+        // O^T += Vt^T Aqk^T;  S^T += Vt^T Kbar  (A: Vt^T bf16 in TMEM)
+        if (dv == 0) {
             fence_after_sync();
             const uint32_t ido = idesc_bf16(128, 64, false, false, false);
             const uint32_t ids = idesc_bf16(128, 128, false, false, false);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint64_t vb = dK(sbase + Lay::oVB, 16384, s);
-                mma(tmem + tO, vb, dK(sbase + Lay::oAQ, 8192, s), ido, 1);
-                mma(tmem + tS, dK(sbase + Lay::oKB, 16384, s), vb, ids, s > 0);
+                mma_ts(tmem + tX + 64, tmem + tX + 8 * s, dK(sbase + oAQ, 8192, s), ido, 1);
+                mma_ts(tmem + tS, tmem + tX + 8 * s, dK(sbase + oKB, 16384, s), ids, 1);
             }
-            commit(&bars[BAR_S]);
+            commit(&bars[BAR_S2]);
         }
-        failed = !mbar_wait(&bars[BAR_S], par, kWaitCycles);
+        failed = !wait_bar(&bars[BAR_S2], (uint32_t)(c & 1), u.abort_flag);
+        if (bar_or(1, 128, failed)) { failed = true; break; }
         fence_after_sync();
-        if (__syncthreads_or(failed)) { failed = true; break; }
-        if (tid < 128) {
-            // S <- Diag(e^gamma_n) S + D_S, then S in bf16 for the next chunk
-            const float e = Eg[tid];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float t0[16], t1[16], t2[16], t3[16];
-                tmem_ld16(tmem + lane_off + tS + 64 * j, t0);
-                tmem_ld16(tmem + lane_off + tS + 64 * j + 16, t1);
-                tmem_ld16(tmem + lane_off + tS + 64 * j + 32, t2);
-                tmem_ld16(tmem + lane_off + tS + 64 * j + 48, t3);
-                tmem_ld_wait();
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    S[64 * j + x] = fmaf(e, S[64 * j + x], t0[x]);
-                    S[64 * j + 16 + x] = fmaf(e, S[64 * j + 16 + x], t1[x]);
-                    S[64 * j + 32 + x] = fmaf(e, S[64 * j + 32 + x], t2[x]);
-                    S[64 * j + 48 + x] = fmaf(e, S[64 * j + 48 + x], t3[x]);
-                }
-            }
-            write_SB();
-        } else {
-            // O^T row dv (64 tokens) -> O staging [token][dv] -> global, valid rows only
-            const int dv = tid - 128;
-            bf16 *OS = reinterpret_cast<bf16 *>(sm + Lay::oOS);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float t32[32];
-                tmem_ld32(tmem + lane_off + tO + 32 * j, t32);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) OS[(32 * j + x) * 128 + dv] = __float2bfloat16_rn(t32[x]);
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            for (int i = dv; i < 1024; i += 128) {
-                const int r = i >> 4, c8 = i & 15;
-                if (r < nvalid)
-                    *reinterpret_cast<uint4 *>(o + (bos + row0 + r) * sv + (int64_t)h * 128 + c8 * 8) =
-                        *reinterpret_cast<const uint4 *>(sm + Lay::oOS + r * 256 + c8 * 16);
-            }
-        }
-        fence_before_sync();
-        fence_proxy_async();
-        __syncthreads();
-    }
+        if (dv == 0) mbar_arrive(&bars[b ? BAR_FREE1 : BAR_FREE0]);  // hand-off slot b consumed
 
-    if (failed) {
-        if (tid == 0) {
-            atomicOr(a.err, kDeviceErrTimeout);
-            // wait (bounded) for every MMA this CTA issued before freeing TMEM
-            fence_after_sync();
-            commit(&bars[BAR_Z]);
-            mbar_wait(&bars[BAR_Z], 0, kWaitCycles);
-        }
-        cp_async_wait_all();
-    } else if (a.ht != nullptr && tid < 128) {
-        float4 *ht = reinterpret_cast<float4 *>(a.ht + (((int64_t)n * a.H_v + h) * 128 + tid) * 128);
+        // S^T -> bf16 operand for the next chunk
+#pragma unroll 1
+        for (int pass = 0; pass < 4; ++pass) {
+            float x[32];
+            tmem_ld32(tmem + lane_off + tS + 32 * pass, x);
+            uint32_t p16[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ht[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+            for (int e = 0; e < 16; ++e) p16[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+            tmem_st16(tmem + lane_off + tSA + 16 * pass, p16);
+        }
+        // O^T row dv -> o[token][dv], valid tokens only
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            float x[32];
+            tmem_ld32(tmem + lane_off + tX + 64 + 32 * pass, x);
+            bf16 *orow = o + (bos + row0 + 32 * pass) * sv + (int64_t)h * 128 + dv;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (32 * pass + e < nvalid) orow[(int64_t)e * sv] = __float2bfloat16_rn(x[e]);
+        }
+        tmem_st_wait();
+        fence_before_sync();
+        bar_serial();
+    }
+    if (failed) {
+        *u.abort_flag = 1;
+        return;
+    }
+    if (a.ht != nullptr) {
+        float *ht = a.ht + ((int64_t)n * a.H_v + h) * 128 * 128 + dv;
+#pragma unroll 1
+        for (int pass = 0; pass < 4; ++pass) {
+            float x[32];
+            tmem_ld32(tmem + lane_off + tS + 32 * pass, x);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ht[(int64_t)(32 * pass + e) * 128] = x[e];
+        }
+    }
+}
+
+template <bool GATE_HEAD>
+__global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, const __grid_constant__ TcMaps maps) {
+    using Lay = WsLayout;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::oBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::oTmemAddr);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Lay::oFlag);
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    Unit u;
+    u.sm = sm;
+    u.sbase = smem_u32(sm);
+    u.h = blockIdx.y;
+    u.n = blockIdx.z;
+    u.hk = u.h / a.group;
+    if (!seq_bounds(a, u.n, u.bos, u.len)) return;
+    u.nchunks = (u.len + kChunk - 1) / kChunk;
+    u.bars = bars;
+    u.abort_flag = abort_flag;
+
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
     }
     fence_before_sync();
     __syncthreads();
+    fence_after_sync();
+    u.tmem = *tmem_slot;
+
+    int tma_pending = -1;
+    if (tid < 128)
+        serial_role(a, u);
+    else
+        tma_pending = prep_role<GATE_HEAD>(a, maps, u);
+
+    fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) {
+        // drain: every MMA and TMA this CTA issued must land before TMEM is freed and the
+        // CTA exits (bounded waits)
+        if (tid == 0 || tid == 128) {
+            atomicOr(a.err, kDeviceErrTimeout);
+            fence_after_sync();
+            uint64_t *z = &bars[tid == 0 ? BAR_Z0 : BAR_Z1];
+            commit(z);
+            mbar_wait(z, 0, kWaitCycles);
+        }
+        if (tid == 128 && tma_pending >= 0) mbar_wait(&bars[BAR_L], (uint32_t)tma_pending, kWaitCycles);
+        cp_async_wait_all();
+        fence_before_sync();
+        __syncthreads();
+    }
     if (warp == 0) {
         fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(u.tmem, kTmemCols);
     }
 }
 
@@ -639,7 +790,7 @@ bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_
 
 template <bool GATE_HEAD>
 cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
-    constexpr int kSmem = TcLayout::kBytes;
+    constexpr int kSmem = WsLayout::kBytes;
     auto kern = kda_fwd_tc_kernel<GATE_HEAD>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
@@ -659,7 +810,7 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
         if (!ok) return cudaErrorInvalidValue;
     }
     const dim3 grid(1, a.H_v, a.N);
-    kern<<<grid, 256, kSmem, stream>>>(a, maps);
+    kern<<<grid, 384, kSmem, stream>>>(a, maps);
     return cudaGetLastError();
 }
 
