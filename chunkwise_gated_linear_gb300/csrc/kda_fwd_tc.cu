@@ -46,7 +46,7 @@ using namespace tc5;
 // Shared-memory plan (byte offsets from a 1024-byte aligned base). Tiles named [d][tok]
 // hold one row per d_k channel and 64 tokens per 128-byte row (one swizzle atom).
 struct WsLayout {
-    static constexpr int oRQ = 0;        // raw Q [64 tok][128] bf16 row-major; then solve scratch
+    static constexpr int oRQ = 0;        // raw Q [64 tok][128] bf16 row-major
     static constexpr int oRK = 16384;    // raw K
     static constexpr int oRV = 32768;    // raw V [2 atoms (d_v)][64 tok][128 B] (MN-major A of U^T)
     static constexpr int oG = 49152;     // raw G fp32 [64][128]; then L and T fp32 [64][68]
@@ -70,7 +70,9 @@ struct WsLayout {
     static constexpr int oBar = oEG1 + 512;   // mbarriers
     static constexpr int oTmemAddr = oBar + 256;
     static constexpr int oFlag = oTmemAddr + 16;  // abort flag
-    static constexpr int kBytes = oFlag + 16 + 1024;  // + slack to align the base
+    static constexpr int oPS = oFlag + 16;        // solve scratch, 8 warps x 16x8 fp32
+    static constexpr int oOS = oPS + 4096;        // O staging [32 tok][128] bf16 (serial)
+    static constexpr int kBytes = oOS + 8192 + 1024;  // + slack to align the base
 };
 constexpr int LDF = 68;  // fp32 row stride of L and T
 
@@ -85,7 +87,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 1ll << 31;  // about one second
 
 enum {
-    BAR_L = 0,   // TMA tiles of the next chunk
+    BAR_LQK = 0, // TMA tiles of a chunk: Q and K
+    BAR_LG,      //   G
+    BAR_LV,      //   V
     BAR_G,       // Gram MMA done
     BAR_W,       // WY MMAs done
     BAR_FULL0,   // hand-off slot 0 / 1 ready (prep -> serial)
@@ -211,7 +215,8 @@ struct Unit {
 
 // ---------------------------------------------------------------------------------------
 // prep warps (4-11): TMA staging, gate pass, Gram, solve, WY factors for every chunk.
-// Returns the mbarrier parity of a TMA that may still be in flight, or -1 (abort path).
+// Returns the loads that may still be in flight (abort path): for Q/K, G and V, two bits
+// each holding 1 + the parity of the pending chunk, or 0.
 // ---------------------------------------------------------------------------------------
 template <bool GATE_HEAD>
 __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, const Unit &u) {
@@ -233,20 +238,37 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
     const int h = u.h, hk = u.hk, len = u.len, nchunks = u.nchunks;
     const int64_t bos = u.bos;
     const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * 128;
-    constexpr uint32_t kTileBytes = 3 * 16384 + (GATE_HEAD ? 0 : 32768);
-
-    // Stage chunk c: Q, K, V and G by TMA (one thread), beta and per-head gates by cp.async.
-    auto stage = [&](int c) {
+    // TMA tiles that may still be in flight, as the parity of their chunk (or -1)
+    int pend_qk = -1, pend_g = -1, pend_v = -1;
+    // Stage chunk c's tiles, each as soon as its buffer is free: Q and K after the gate pass,
+    // G (with beta and the per-head gates, by cp.async) after the solve, V after the WY MMAs.
+    auto stage_qk = [&](int c) {
+        if (ptid == 0) {
+            const int y = (int)(bos + c * kChunk);
+            mbar_arrive_expect_tx(&bars[BAR_LQK], 32768);
+            tma_load_2d(sm + Lay::oRQ, &maps.q, &bars[BAR_LQK], hk * 128, y);
+            tma_load_2d(sm + Lay::oRK, &maps.k, &bars[BAR_LQK], hk * 128, y);
+        }
+        pend_qk = c & 1;
+    };
+    auto stage_v = [&](int c) {
+        if (ptid == 0) {
+            const int y = (int)(bos + c * kChunk);
+            mbar_arrive_expect_tx(&bars[BAR_LV], 16384);
+            tma_load_2d(sm + Lay::oRV, &maps.v, &bars[BAR_LV], h * 128, y);
+            tma_load_2d(sm + Lay::oRV + 8192, &maps.v, &bars[BAR_LV], h * 128 + 64, y);
+        }
+        pend_v = c & 1;
+    };
+    auto stage_g = [&](int c) {
         const int row0 = c * kChunk;
         const int nvalid = min(kChunk, len - row0);
-        if (ptid == 0) {
-            const int y = (int)(bos + row0);
-            mbar_arrive_expect_tx(&bars[BAR_L], kTileBytes);
-            tma_load_2d(sm + Lay::oRQ, &maps.q, &bars[BAR_L], hk * 128, y);
-            tma_load_2d(sm + Lay::oRK, &maps.k, &bars[BAR_L], hk * 128, y);
-            tma_load_2d(sm + Lay::oRV, &maps.v, &bars[BAR_L], h * 128, y);
-            tma_load_2d(sm + Lay::oRV + 8192, &maps.v, &bars[BAR_L], h * 128 + 64, y);
-            if constexpr (!GATE_HEAD) tma_load_2d(sm + Lay::oG, &maps.g, &bars[BAR_L], h * 128, y);
+        if constexpr (!GATE_HEAD) {
+            if (ptid == 0) {
+                mbar_arrive_expect_tx(&bars[BAR_LG], 32768);
+                tma_load_2d(sm + Lay::oG, &maps.g, &bars[BAR_LG], h * 128, (int)(bos + row0));
+            }
+            pend_g = c & 1;
         }
         if (ptid < 64) {
             const bool ok = ptid < nvalid;
@@ -262,10 +284,10 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
     };
 
     bool failed = false;
-    int tma_pending = -1;  // parity of the staged chunk not yet waited for
     if (nchunks > 0) {
-        stage(0);
-        tma_pending = 0;
+        stage_g(0);
+        stage_qk(0);
+        stage_v(0);
     }
     for (int p = 0; p < nchunks; ++p) {
         const int row0 = p * kChunk;
@@ -276,30 +298,22 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         const uint32_t oAQ = b ? Lay::oAQ1 : Lay::oAQ0;
         float *EG = reinterpret_cast<float *>(sm + (b ? Lay::oEG1 : Lay::oEG0));
         const uint32_t tU = b ? tU1 : tU0;
+        // rows past the sequence end hold the next sequence (or zeros past the tensor) and
+        // must be zero in every operand
+        const int nz = kChunk - nvalid;
 
-        // tiles of chunk p, and hand-off slot b released by the serial step of chunk p - 2
+        // G, beta of chunk p, and hand-off slot b released by the serial step of chunk p - 2
         cp_async_wait_all();
-        failed = !wait_bar(&bars[BAR_L], (uint32_t)(p & 1), u.abort_flag);
+        if constexpr (!GATE_HEAD) failed = !wait_bar(&bars[BAR_LG], (uint32_t)(p & 1), u.abort_flag);
         if (!failed && p >= 2)
             failed = !wait_bar(&bars[b ? BAR_FREE1 : BAR_FREE0], (uint32_t)(((p >> 1) - 1) & 1), u.abort_flag);
         if (bar_or(2, 256, failed)) { failed = true; break; }
-        tma_pending = -1;
-        if (nvalid < kChunk) {
-            // the boxes read on past the sequence end (the next sequence, or zeros past the
-            // tensor): those rows must be zero in every operand
-            const int nz = kChunk - nvalid;
-            for (int i = ptid; i < nz * 16; i += 256) {
-                const int r = nvalid + (i >> 4), c16 = i & 15;
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(sm + Lay::oRQ + r * 256 + c16 * 16) = z;
-                *reinterpret_cast<uint4 *>(sm + Lay::oRK + r * 256 + c16 * 16) = z;
-                *reinterpret_cast<uint4 *>(sm + Lay::oRV + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) = z;
-                if constexpr (!GATE_HEAD) {
-                    *reinterpret_cast<uint4 *>(sm + Lay::oG + r * 512 + c16 * 32) = z;
-                    *reinterpret_cast<uint4 *>(sm + Lay::oG + r * 512 + c16 * 32 + 16) = z;
-                }
+        pend_g = -1;
+        if (!GATE_HEAD && nz > 0) {
+            for (int i = ptid; i < nz * 32; i += 256) {
+                const int r = nvalid + (i >> 5), c16 = i & 31;
+                *reinterpret_cast<uint4 *>(sm + Lay::oG + r * 512 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
-            fence_proxy_async();
             bar_prep();
         }
 
@@ -326,7 +340,17 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
             }
             Tot[qr * 128 + c0] = acc0;
             Tot[qr * 128 + c1] = acc1;
-            bar_prep();
+            failed = !wait_bar(&bars[BAR_LQK], (uint32_t)(p & 1), u.abort_flag);
+            if (bar_or(2, 256, failed)) { failed = true; break; }
+            pend_qk = -1;
+            if (nz > 0) {
+                for (int i = ptid; i < nz * 16; i += 256) {
+                    const int r = nvalid + (i >> 4), c16 = i & 15;
+                    *reinterpret_cast<uint4 *>(sm + Lay::oRQ + r * 256 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(sm + Lay::oRK + r * 256 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                bar_prep();
+            }
             float off0 = 0.f, off1 = 0.f, gn0 = 0.f, gn1 = 0.f;
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
@@ -373,6 +397,7 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         }
         fence_proxy_async();
         bar_prep();
+        if (p + 1 < nchunks) stage_qk(p + 1);  // the raw Q and K tiles are consumed
 
         // ---- Gram: D_G = [Qp; Kp] Km^T  (rows 0-63: Aqk, rows 64-127: M) --------------------
         if (ptid == 0) {
@@ -450,7 +475,7 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         {
             const int j = pw >> 1, col0 = 16 * j + 8 * (pw & 1);
             const int g8 = lane >> 2, t4 = lane & 3;
-            float *P = reinterpret_cast<float *>(sm + Lay::oRQ) + pw * 128;  // 16x8 scratch
+            float *P = reinterpret_cast<float *>(sm + Lay::oPS) + pw * 128;  // 16x8 scratch
             for (int i = j + 1; i < 4; ++i) {
                 float acc[3][4];
 #pragma unroll
@@ -496,6 +521,19 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         }
         fence_proxy_async();
         bar_prep();
+        if (p + 1 < nchunks) stage_g(p + 1);  // G, L, T and beta are consumed
+        failed = !wait_bar(&bars[BAR_LV], (uint32_t)(p & 1), u.abort_flag);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
+        pend_v = -1;
+        if (nz > 0) {
+            for (int i = ptid; i < nz * 16; i += 256) {
+                const int r = nvalid + (i >> 4), c16 = i & 15;
+                *reinterpret_cast<uint4 *>(sm + Lay::oRV + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async();
+            bar_prep();
+        }
 
         // ---- WY factors: D_W = Kp^T T_beta^T, D_U = V^T T_beta^T ------------------------------
         if (ptid == 0) {
@@ -514,6 +552,7 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         failed = !wait_bar(&bars[BAR_W], (uint32_t)(p & 1), u.abort_flag);
         if (!failed && p >= 1) failed = !wait_bar(&bars[BAR_WT], (uint32_t)((p - 1) & 1), u.abort_flag);
         if (bar_or(2, 256, failed)) { failed = true; break; }
+        if (p + 1 < nchunks) stage_v(p + 1);  // the U MMA has read V
         fence_after_sync();
         {
             // W^T row d -> bf16 [d][tok] (MN-major B); each warp half writes 32 of the 64 tokens
@@ -531,15 +570,11 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         fence_before_sync();
         fence_proxy_async();
         bar_prep();
-        // every raw tile is consumed: stage the next chunk, then hand chunk p to the serial warps
-        if (p + 1 < nchunks) {
-            stage(p + 1);
-            tma_pending = (p + 1) & 1;
-        }
+        // hand chunk p to the serial warps
         if (ptid == 0) mbar_arrive(&bars[b ? BAR_FULL1 : BAR_FULL0]);
     }
     if (failed) *u.abort_flag = 1;
-    return tma_pending;
+    return (pend_qk + 1) | ((pend_g + 1) << 2) | ((pend_v + 1) << 4);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -667,19 +702,28 @@ __device__ __forceinline__ void serial_role(const FwdArgs &a, const Unit &u) {
             for (int e = 0; e < 16; ++e) p16[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
             tmem_st16(tmem + lane_off + tSA + 16 * pass, p16);
         }
-        // O^T row dv -> o[token][dv], valid tokens only
+        tmem_st_wait();
+        // O^T row dv -> o[token][dv], valid tokens only: 32 tokens at a time through a
+        // [32 tok][128 dv] staging tile so that global stores are 16 bytes wide
+        bf16 *OS = reinterpret_cast<bf16 *>(sm + Lay::oOS);
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
             float x[32];
             tmem_ld32(tmem + lane_off + tX + 64 + 32 * pass, x);
-            bf16 *orow = o + (bos + row0 + 32 * pass) * sv + (int64_t)h * 128 + dv;
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-                if (32 * pass + e < nvalid) orow[(int64_t)e * sv] = __float2bfloat16_rn(x[e]);
+            for (int e = 0; e < 32; ++e) OS[e * 128 + dv] = __float2bfloat16_rn(x[e]);
+            bar_serial();
+#pragma unroll
+            for (int i = dv; i < 512; i += 128) {
+                const int r = i >> 4, c16 = i & 15;
+                const int tok = 32 * pass + r;
+                if (tok < nvalid)
+                    *reinterpret_cast<uint4 *>(o + (bos + row0 + tok) * sv + (int64_t)h * 128 + c16 * 8) =
+                        *reinterpret_cast<const uint4 *>(sm + Lay::oOS + r * 256 + c16 * 16);
+            }
+            bar_serial();
         }
-        tmem_st_wait();
         fence_before_sync();
-        bar_serial();
     }
     if (failed) {
         *u.abort_flag = 1;
@@ -732,7 +776,7 @@ __global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, con
     fence_after_sync();
     u.tmem = *tmem_slot;
 
-    int tma_pending = -1;
+    int tma_pending = 0;
     if (tid < 128)
         serial_role(a, u);
     else
@@ -750,7 +794,12 @@ __global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, con
             commit(z);
             mbar_wait(z, 0, kWaitCycles);
         }
-        if (tid == 128 && tma_pending >= 0) mbar_wait(&bars[BAR_L], (uint32_t)tma_pending, kWaitCycles);
+        if (tid == 128) {
+            const int pq = (tma_pending & 3) - 1, pg = ((tma_pending >> 2) & 3) - 1, pv = ((tma_pending >> 4) & 3) - 1;
+            if (pq >= 0) mbar_wait(&bars[BAR_LQK], (uint32_t)pq, kWaitCycles);
+            if (pg >= 0) mbar_wait(&bars[BAR_LG], (uint32_t)pg, kWaitCycles);
+            if (pv >= 0) mbar_wait(&bars[BAR_LV], (uint32_t)pv, kWaitCycles);
+        }
         cp_async_wait_all();
         fence_before_sync();
         __syncthreads();
