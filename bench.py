@@ -36,7 +36,11 @@ METRIC = "chunk KDA fwd tokens/s at T=8192,H=32,d=128 bf16; % of roofline"
 # DRAM traffic per launch of the forward kernel, from an ncu capture of this workload
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of the kernel sources
 # it was taken on; any change to the sources makes the figure stale (reported as null).
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # profiles/kda_fwd_tc_b2_t8192_h32_d128.md: 393.16 MB on the half-size case (32 units),
+    # scaled by 2 to the 64 units of this workload
+    ("kda_b2_t8192_h32_d128_bf16", "eed5b62972917fb8"): 786_319_360,
+}
 
 
 def kernel_source_hash() -> str:
@@ -332,7 +336,7 @@ def run_ours(args, world, rank, local, pg):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": abytes, "kernel": "kda_fwd_bf16_kernel",
+                         "algorithmic_bytes_per_launch": abytes, "kernel": "kda_fwd_tc_kernel",
                          "tflops": flops / (ms / 1000.0) / 1e12},
             "cpu_baseline": cpu,
             "clocks": clocks,
