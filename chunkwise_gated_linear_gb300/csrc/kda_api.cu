@@ -11,6 +11,7 @@ namespace kda {
 cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched);
 }  // namespace kda
 
 namespace {
@@ -50,7 +51,7 @@ int run(const kda_fwd_params &p, cudaStream_t stream) {
                      p.beta == nullptr || p.o == nullptr))
         return KDA_ERR_INVALID_ARG;
     if (p.B < 1 || p.T < 0 || p.H_k < 1 || p.H_v < 1 || p.H_v % p.H_k != 0) return KDA_ERR_INVALID_ARG;
-    if (p.flags != 0) return KDA_ERR_INVALID_ARG;
+    if ((p.flags & ~KDA_FLAG_ONE_CTA_PER_UNIT) != 0) return KDA_ERR_INVALID_ARG;
     if (p.dtype != KDA_DTYPE_BF16 && p.dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (p.gate_mode != KDA_GATE_PER_CHANNEL && p.gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_UNSUPPORTED;
     if ((p.d_k != 64 && p.d_k != 128) || (p.d_v != 64 && p.d_v != 128) || p.C != kda::kChunk)
@@ -84,10 +85,18 @@ int run(const kda_fwd_params &p, cudaStream_t stream) {
     a.gate_per_head = p.gate_mode == KDA_GATE_PER_HEAD ? 1 : 0;
 
     cudaError_t e = device_error_ptr(&a.err);
-    if (e == cudaSuccess)
-        e = p.dtype == KDA_DTYPE_F32                 ? kda::launch_fwd_f32(a, stream)
-            : (p.d_k == 128 && p.d_v == 128)         ? kda::launch_fwd_tc(a, stream)
-                                                     : kda::launch_fwd_bf16(a, stream);
+    if (e == cudaSuccess) {
+        if (p.dtype == KDA_DTYPE_F32) {
+            e = kda::launch_fwd_f32(a, stream);
+        } else if (p.d_k == 128 && p.d_v == 128) {
+            // few units: the persistent producer/consumer kernel, else one CTA per unit
+            bool launched = false;
+            if (!(p.flags & KDA_FLAG_ONE_CTA_PER_UNIT)) e = kda::launch_fwd_pc(a, stream, &launched);
+            if (e == cudaSuccess && !launched) e = kda::launch_fwd_tc(a, stream);
+        } else {
+            e = kda::launch_fwd_bf16(a, stream);
+        }
+    }
     if (e != cudaSuccess) {
         t_last_cuda_error = e;
         return KDA_ERR_CUDA;

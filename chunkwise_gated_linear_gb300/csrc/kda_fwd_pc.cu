@@ -1,0 +1,1149 @@
+// Chunkwise KDA forward for d_k = d_v = 128, bf16 operands: a persistent kernel in which
+// some CTAs (producers) build the per-chunk factors of every (sequence, value head) unit
+// in parallel, and one CTA per unit (its consumer) runs the serial chunk-to-chunk step.
+//
+// The chunk equations ("RNN的复兴04:线性注意力并行计算DPLR", §5.3.5; "TileLang 实战：KDA
+// 从零到一–Kimi Delta Attention", §3.3) split into a part that depends only on the chunk's
+// own inputs and the state recurrence. Only the second is serial, so with fewer units than
+// SMs the first runs on the SMs that would otherwise idle:
+//
+//   producer CTA, one chunk job after another, two stages working on consecutive jobs:
+//     front (warps 0-7)   TMA Q, K, G; gamma = chunk-local cumulative log2 gate;
+//                         Qp = scale Q e^gamma, Kp = K e^gamma, Km = K e^-gamma,
+//                         Kbar = Km e^gamma_n (transposed, bf16);
+//                         Gram D_G = [Qp; Kp] Km^T -> Aqk (lower), L = diag(beta) M (strict)
+//     back  (warps 8-15)  T = (I + L)^-1 (16x16 diagonal blocks by substitution, the rest
+//                         on tf32 mma.sync); D_W = Kp^T (T diag beta)^T, D_U = V^T (T diag beta)^T
+//     -> the chunk's slot in a per-unit ring in global memory: W^T, Qp^T, Kbar^T, Aqk (bf16,
+//        in the consumer's 128-byte swizzled shared-memory image), U^T (bf16), e^gamma_n.
+//   consumer CTA (unit u), state S^T [d_v x d_k] fp32 in TMEM, thread = d_v row:
+//     one bulk copy per chunk brings the slot into shared memory (double-buffered), then
+//     D_X = S^T [W^T | Qp^T];  S^T <- S^T Diag(e^gamma_n);  Vt^T = U^T - D_X[:, :64];
+//     O^T = D_X[:, 64:] + Vt^T Aqk^T;  S^T += Vt^T Kbar.
+//
+// Hand-offs through global memory use per-slot sequence numbers: a producer publishes
+// chunk c of unit u by a release store of c + 1 into ready[u][c % R] after its writes;
+// the consumer releases the slot by storing c + 1 into done[u] once the bulk copy has
+// landed. Producers take jobs in (chunk, unit) order, so the oldest unfinished job
+// never waits on a later one. The launch is cooperative (every CTA resident). Every
+// wait is bounded (about one second) and watches a global abort word, so a failure
+// anywhere ends all CTAs with KDA_DEVICE_ERR_TIMEOUT.
+#include <cstring>
+
+#include "tc_util.cuh"
+
+namespace kda {
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+using namespace tc5;
+using namespace tcu;
+
+constexpr int kMaxUnits = 76;       // units served by one launch (at most half the SMs)
+constexpr int kRing = 8;            // ring slots per unit
+constexpr int kThreads = 512;
+
+// Slot image (global ring and consumer shared memory). [d][tok] tiles hold one row per
+// d_k channel and 64 tokens per 128-byte row (one swizzle atom).
+struct Slot {
+    static constexpr int oWT = 0;       // W^T [d][tok] bf16     } adjacent: one N = 128
+    static constexpr int oQP = 16384;   // Qp^T [d][tok] bf16    } MN-major B operand
+    static constexpr int oKB = 32768;   // Kbar^T [d][tok] bf16 (K-major B)
+    static constexpr int oAQ = 49152;   // Aqk [tok][tok'] bf16 (K-major B)
+    static constexpr int oEG = 57344;   // e^gamma_n [128] fp32
+    static constexpr int oU = 57856;    // U^T as bf16 token pairs: u32 [tok / 2][d_v]
+    static constexpr int kBytes = 74240;
+    static constexpr int kStride = 74752;  // 1024-byte multiple
+    // the front stage writes [oQP, oU) as one image, the back stage W^T and U^T
+    static constexpr int kFrontBytes = oU - oQP;
+};
+
+// Producer shared memory (offsets from a 1024-byte aligned base).
+struct Prod {
+    static constexpr int oRQ = 0;          // raw Q [64 tok][128] bf16 row-major
+    static constexpr int oRK = 16384;      // raw K
+    static constexpr int oG = 32768;       // raw G fp32 [64][128]
+    static constexpr int oIMG = 65536;     // the front part of the slot image (Slot::oQP ..
+                                           // Slot::oU); its Qp^T is also the Gram A operand
+    static constexpr int oQP = oIMG;
+    static constexpr int oKB = oIMG + (Slot::oKB - Slot::oQP);
+    static constexpr int oAQ = oIMG + (Slot::oAQ - Slot::oQP);
+    static constexpr int oEG = oIMG + (Slot::oEG - Slot::oQP);
+    static constexpr int oKP0 = 107520;    // Kp^T [d][tok], hand-off slots 0 / 1 (Gram A atom 1)
+    static constexpr int oKP1 = 123904;
+    static constexpr int oKM = 140288;     // Km^T [d][tok]
+    static constexpr int oL = 156672;      // L fp32 [64][68] (front -> back)
+    static constexpr int oT = 174080;      // T fp32 [64][68]; then W^T staging [d][tok] bf16
+    static constexpr int oTB = 191488;     // T_beta [tok][tok'] bf16 (K-major B)
+    static constexpr int oRV = 199680;     // raw V [2 atoms (d_v)][64 tok][128 B]; then U^T staging
+    static constexpr int oBF0 = 216064;    // beta as loaded, job parity 0 / 1
+    static constexpr int oBF1 = 216320;
+    static constexpr int oBH = 216576;     // beta handed to the back stage
+    static constexpr int oGh0 = 216832;    // per-head gates, job parity 0 / 1
+    static constexpr int oGh1 = 217088;
+    static constexpr int oTot = 217344;    // [4][128] fp32 partial gate sums
+    static constexpr int oPS = 219392;     // solve scratch, 8 warps x 16x8 fp32
+    static constexpr int kEnd = oPS + 4096;
+};
+static_assert(Prod::oEG + 512 <= Prod::oKP0, "image overlaps");
+// Consumer shared memory.
+struct Cons {
+    static constexpr int oBuf0 = 0;        // slot images, buffers 0 / 1
+    static constexpr int oBuf1 = Slot::kStride;
+    static constexpr int oOS = 2 * Slot::kStride;  // O staging, 2 x [32 tok][128] bf16
+};
+// Both roles.
+struct Common {
+    static constexpr int oBar = Prod::kEnd;  // mbarriers
+    static constexpr int oTmemAddr = oBar + 256;
+    static constexpr int oFlag = oTmemAddr + 16;   // CTA abort flag
+    static constexpr int oUnits = oFlag + 16;      // UnitInfo [kMaxUnits]
+    static constexpr int kEnd = oUnits + 16 * kMaxUnits;
+    static constexpr int kBytes = kEnd + 1024;      // + slack to align the base
+};
+static_assert(Cons::oOS + 16384 <= Common::oBar, "consumer layout overlaps");
+static_assert(Common::kBytes <= 232448, "shared memory");
+
+// TMEM columns
+constexpr uint32_t tGram = 0, tW = 64, tU = 128, kTmemProd = 256;     // producer
+constexpr uint32_t tX = 0, tSA = 128, tV = 192, tS = 256, kTmemCons = 512;  // consumer
+
+enum {
+    // producer
+    B_LQK = 0, B_LG, B_LV,   // TMA tiles: Q and K, G, V
+    B_GRAM, B_WMMA,          // MMA completion: Gram, WY
+    B_HFULL0, B_HFULL1,      // front -> back hand-off slot 0 / 1 written
+    B_HEMPTY0, B_HEMPTY1,    // back -> front: Kp^T of hand-off slot 0 / 1 consumed
+    B_LFREE,                 // back -> front: L and beta consumed by the solve
+    B_PZ0, B_PZ1,            // drains after a failure (one per MMA-issuing thread)
+    // consumer
+    B_FULL0, B_FULL1,        // slot image in buffer 0 / 1 landed
+    B_EMPTY0, B_EMPTY1,      // buffer 0 / 1 consumed by the serial step
+    B_X, B_S2,               // serial products
+    B_CZ,
+    kNumBars
+};
+
+struct UnitInfo {
+    long long bos;
+    int len, nch;
+};
+
+// Ring and flags in global memory; ready/done/abort start at zero for every launch.
+struct PcArgs {
+    unsigned char *ring;   // [U][kRing] slots of Slot::kStride bytes
+    int *ready;            // [U][kRing]: c + 1 once chunk c is in slot c % kRing
+    int *done;             // [U]: chunks whose slot image has been copied out
+    int *abort;            // set by any CTA that gave up
+    int U, P;              // units (= consumer CTAs), producer CTAs
+};
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// 1-D bulk copy global -> shared, completing on an mbarrier of this CTA.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+// 1-D bulk copy shared -> global (bulk async-group of the issuing thread).
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the issuing thread's bulk stores have completed (written) / have read their source
+__device__ __forceinline__ void bulk_wait_done() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Raise the abort word (once) and the device error bit.
+__device__ __forceinline__ void raise_abort(const FwdArgs &a, const PcArgs &pc, volatile int *cta_flag) {
+    *cta_flag = 1;
+    if (atomicExch(pc.abort, 1) == 0) atomicOr(a.err, kDeviceErrTimeout);
+}
+// Bounded wait on an mbarrier phase of this CTA; gives up when this CTA or any other is
+// aborting.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *cta_flag, const FwdArgs &a,
+                                         const PcArgs &pc) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    int spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if (*cta_flag) return false;
+        if ((++spins & 63) == 0 && *(volatile int *)pc.abort) {
+            *cta_flag = 1;
+            return false;
+        }
+        if (clock64() - t0 > kWaitCycles) {
+            raise_abort(a, pc, cta_flag);
+            return false;
+        }
+    }
+    return true;
+}
+// Bounded wait until the global word *p reaches at least `target` (acquire).
+__device__ __forceinline__ bool wait_geq(const int *p, int target, volatile int *cta_flag, const FwdArgs &a,
+                                         const PcArgs &pc) {
+    if (ld_acquire(p) >= target) return true;
+    const long long t0 = clock64();
+    while (ld_acquire(p) < target) {
+        if (*cta_flag) return false;
+        if (*(volatile int *)pc.abort) {
+            *cta_flag = 1;
+            return false;
+        }
+        if (clock64() - t0 > kWaitCycles) {
+            raise_abort(a, pc, cta_flag);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Per-CTA context shared by the roles.
+struct Ctx {
+    unsigned char *sm;
+    uint32_t sbase, tmem;
+    uint64_t *bars;
+    volatile int *flag;     // this CTA is aborting
+    volatile int *stored;   // producer: jobs whose front image is written to the ring
+    const UnitInfo *units;  // [U]
+    int maxc, uniform;      // over the units of this launch
+    int p;                  // producer index (producer CTAs)
+};
+
+// Bounded wait until the shared-memory counter *p reaches at least `target`.
+__device__ __forceinline__ bool wait_count(const volatile int *p, int target, volatile int *cta_flag,
+                                           const FwdArgs &a, const PcArgs &pc) {
+    const long long t0 = clock64();
+    while (*p < target) {
+        if (*cta_flag) return false;
+        if (*(volatile int *)pc.abort) {
+            *cta_flag = 1;
+            return false;
+        }
+        if (clock64() - t0 > kWaitCycles) {
+            raise_abort(a, pc, cta_flag);
+            return false;
+        }
+    }
+    return true;
+}
+
+// The jobs of producer p: the (chunk c, unit u) pairs with c < nch[u], ordered by c then
+// u, every P-th one starting at the p-th. Every thread of a stage steps its own copy.
+struct JobIt {
+    int c, u, k;  // current pair and its index among all jobs
+};
+__device__ __forceinline__ bool next_job(JobIt &it, const Ctx &x, const PcArgs &pc) {
+    if (x.uniform) {
+        it.k = it.k < 0 ? x.p : it.k + pc.P;
+        it.c = it.k / pc.U;
+        it.u = it.k - it.c * pc.U;
+        return it.c < x.maxc;
+    }
+    const int want = it.k < 0 ? x.p : it.k + pc.P;
+    while (true) {
+        if (++it.u == pc.U) {
+            it.u = 0;
+            if (++it.c >= x.maxc) return false;
+        }
+        if (x.units[it.u].nch > it.c && ++it.k == want) return true;
+    }
+}
+
+__device__ __forceinline__ unsigned char *slot_ptr(const PcArgs &pc, int u, int c) {
+    return pc.ring + ((int64_t)u * kRing + c % kRing) * Slot::kStride;
+}
+
+// ---------------------------------------------------------------------------------------
+// producer, front stage (warps 0-7): tiles, gate pass, Gram; the front image of the slot
+// goes to the ring by one bulk store. Returns the TMA loads that may still be in flight
+// (abort path): bit 0 Q/K, bit 1 G; bits 4 and 5 their parities.
+// ---------------------------------------------------------------------------------------
+template <bool GATE_HEAD>
+__device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMaps &maps, const PcArgs &pc,
+                                                   const Ctx &x) {
+    unsigned char *sm = x.sm;
+    uint64_t *bars = x.bars;
+    const int ptid = threadIdx.x, pw = ptid >> 5, lane = ptid & 31;
+    const uint32_t lane_off = (uint32_t)(32 * (pw & 3)) << 16;  // this warp's TMEM lane quarter
+    const uint32_t half = (uint32_t)(pw >> 2) * 32u;             // column half of a 64-wide readback
+    const bf16 *RQ = reinterpret_cast<const bf16 *>(sm + Prod::oRQ);
+    const bf16 *RK = reinterpret_cast<const bf16 *>(sm + Prod::oRK);
+    float *G = reinterpret_cast<float *>(sm + Prod::oG);
+    float *Tot = reinterpret_cast<float *>(sm + Prod::oTot);
+    float *EG = reinterpret_cast<float *>(sm + Prod::oEG);
+    float *L = reinterpret_cast<float *>(sm + Prod::oL);
+    const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * 128;
+    uint32_t pend = 0;
+
+    // Bulk copies issued by one thread are served one after another; the copies of a job
+    // are spread over the lane 0 of different warps so that they overlap.
+    constexpr int kIssQ = 0, kIssK = 32, kIssG = 64, kIssImg = 96;
+    auto stage_qk = [&](const JobIt &j, int jo) {
+        if (ptid == kIssQ || ptid == kIssK) {
+            const int hk = (j.u % a.H_v) / a.group;
+            const int y = (int)(x.units[j.u].bos + (int64_t)j.c * kChunk);
+            if (ptid == kIssQ) {
+                // the barrier expects both tiles; K may land first (transaction counts may
+                // run ahead of the expectation within a phase)
+                mbar_arrive_expect_tx(&bars[B_LQK], 32768);
+                tma_load_2d(sm + Prod::oRQ, &maps.q, &bars[B_LQK], hk * 128, y);
+            } else {
+                tma_load_2d(sm + Prod::oRK, &maps.k, &bars[B_LQK], hk * 128, y);
+            }
+        }
+        pend = (pend & ~0x11u) | 1u | ((uint32_t)(jo & 1) << 4);
+    };
+    // G by TMA; beta (and the per-head gates) by cp.async into the job-parity buffers
+    auto stage_g = [&](const JobIt &j, int jo) {
+        const int h = j.u % a.H_v;
+        const int64_t bos = x.units[j.u].bos;
+        const int row0 = j.c * kChunk;
+        const int nvalid = min(kChunk, x.units[j.u].len - row0);
+        if constexpr (!GATE_HEAD) {
+            if (ptid == kIssG) {
+                mbar_arrive_expect_tx(&bars[B_LG], 32768);
+                tma_load_2d(sm + Prod::oG, &maps.g, &bars[B_LG], h * 128, (int)(bos + row0));
+            }
+            pend = (pend & ~0x22u) | 2u | ((uint32_t)(jo & 1) << 5);
+        }
+        float *Bf = reinterpret_cast<float *>(sm + ((jo & 1) ? Prod::oBF1 : Prod::oBF0));
+        float *Gh = reinterpret_cast<float *>(sm + ((jo & 1) ? Prod::oGh1 : Prod::oGh0));
+        if (ptid < 64) {
+            const bool ok = ptid < nvalid;
+            const int64_t ob = ok ? (bos + row0 + ptid) * a.H_v + h : 0;
+            cp_async_4(Bf + ptid, a.beta + ob, ok ? 4 : 0);
+        } else if (GATE_HEAD && ptid < 128) {
+            const int r = ptid - 64;
+            const bool ok = r < nvalid;
+            const int64_t og = ok ? (bos + row0 + r) * sg + h : 0;
+            cp_async_4(Gh + r, a.g + og, ok ? 4 : 0);
+        }
+        cp_async_commit();
+    };
+
+    JobIt it{0, -1, -1};
+    bool have = next_job(it, x, pc);
+    if (have) {
+        stage_g(it, 0);
+        stage_qk(it, 0);
+    }
+    bool failed = false;
+    int jo = 0;
+    for (; have; ++jo) {
+        const int u = it.u, c = it.c, b = jo & 1;
+        const int row0 = c * kChunk;
+        const int nvalid = min(kChunk, x.units[u].len - row0);
+        const int nz = kChunk - nvalid;  // rows past the sequence end: zero in every operand
+        JobIt nx = it;
+        const bool have_next = next_job(nx, x, pc);
+        const uint32_t oKP = b ? Prod::oKP1 : Prod::oKP0;
+        const float *Bf = reinterpret_cast<const float *>(sm + (b ? Prod::oBF1 : Prod::oBF0));
+        const float *Gh = reinterpret_cast<const float *>(sm + (b ? Prod::oGh1 : Prod::oGh0));
+
+        cp_async_wait_all();
+        if constexpr (!GATE_HEAD) failed = !wait_bar(&bars[B_LG], (uint32_t)(jo & 1), x.flag, a, pc);
+        if (bar_or(1, 256, failed)) { failed = true; break; }
+        pend &= ~2u;
+        if (!GATE_HEAD && nz > 0) {
+            for (int i = ptid; i < nz * 32; i += 256) {
+                const int r = nvalid + (i >> 5), c16 = i & 31;
+                *reinterpret_cast<uint4 *>(sm + Prod::oG + r * 512 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            bar_named(1, 256);
+        }
+
+        // ---- gate pass ---------------------------------------------------------------------
+        // warp pw: rows 16 (pw >> 1) .. +15, channels c0 = 64 (pw & 1) + lane and c0 + 32.
+        const int qr = pw >> 1;
+        const int c0 = 64 * (pw & 1) + lane, c1 = c0 + 32;
+        float gl0[16], gl1[16];
+        {
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int r = 16 * qr + e;
+                if constexpr (!GATE_HEAD) {
+                    acc0 += G[r * 128 + c0] * kLog2e;
+                    acc1 += G[r * 128 + c1] * kLog2e;
+                } else {
+                    const float gr = Gh[r] * kLog2e;
+                    acc0 += gr;
+                    acc1 += gr;
+                }
+                gl0[e] = acc0;
+                gl1[e] = acc1;
+            }
+            Tot[qr * 128 + c0] = acc0;
+            Tot[qr * 128 + c1] = acc1;
+        }
+        failed = !wait_bar(&bars[B_LQK], (uint32_t)(jo & 1), x.flag, a, pc);
+        // the ring slot holds chunk c - kRing until the consumer has copied it out
+        if (!failed && ptid == 0 && c >= kRing) failed = !wait_geq(&pc.done[u], c - kRing + 1, x.flag, a, pc);
+        // hand-off slot b (Kp^T) is free once the back stage has multiplied job jo - 2
+        if (!failed && jo >= 2)
+            failed = !wait_bar(&bars[B_HEMPTY0 + b], (uint32_t)(((jo >> 1) - 1) & 1), x.flag, a, pc);
+        if (bar_or(1, 256, failed)) { failed = true; break; }
+        pend &= ~1u;
+        if (have_next) stage_g(nx, jo + 1);  // G and the per-head gates are consumed
+        if (nz > 0) {
+            for (int i = ptid; i < nz * 16; i += 256) {
+                const int r = nvalid + (i >> 4), c16 = i & 15;
+                *reinterpret_cast<uint4 *>(sm + Prod::oRQ + r * 256 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sm + Prod::oRK + r * 256 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            bar_named(1, 256);
+        }
+        {
+            float off0 = 0.f, off1 = 0.f, gn0 = 0.f, gn1 = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const float t0 = Tot[qq * 128 + c0], t1 = Tot[qq * 128 + c1];
+                if (qq < qr) {
+                    off0 += t0;
+                    off1 += t1;
+                }
+                gn0 += t0;
+                gn1 += t1;
+            }
+            const float eg0 = ex2(gn0), eg1 = ex2(gn1);
+            if (qr == 0) {
+                EG[c0] = eg0;
+                EG[c1] = eg1;
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int tc = 2 * qr + j;  // 16-byte chunk (8 tokens) of a 64-token row
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int cc = ch ? c1 : c0;
+                    const float off = ch ? off1 : off0, eg = ch ? eg1 : eg0;
+                    float kp[8], km[8], qp[8], kb[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int r = 16 * qr + 8 * j + e;
+                        const float gm = off + (ch ? gl1[8 * j + e] : gl0[8 * j + e]);
+                        const float ep = ex2(gm), em = ex2(-gm);
+                        const float kv = __bfloat162float(RK[r * 128 + cc]);
+                        const float qv = __bfloat162float(RQ[r * 128 + cc]);
+                        kp[e] = kv * ep;
+                        km[e] = kv * em;
+                        qp[e] = a.scale * qv * ep;
+                        kb[e] = km[e] * eg;
+                    }
+                    const uint32_t sw = sw128(cc, tc);
+                    *reinterpret_cast<uint4 *>(sm + Prod::oQP + sw) = pack8(qp);
+                    *reinterpret_cast<uint4 *>(sm + oKP + sw) = pack8(kp);
+                    *reinterpret_cast<uint4 *>(sm + Prod::oKM + sw) = pack8(km);
+                    *reinterpret_cast<uint4 *>(sm + Prod::oKB + sw) = pack8(kb);
+                }
+            }
+        }
+        fence_proxy_async();
+        bar_named(1, 256);
+        if (have_next) stage_qk(nx, jo + 1);  // the raw Q and K tiles are consumed
+
+        // ---- Gram: D_G = [Qp; Kp] Km^T  (rows 0-63: Aqk, rows 64-127: M) --------------------
+        if (ptid == 0) {
+            fence_after_sync();
+            const uint32_t id = idesc_bf16(128, 64, true, true, false);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma(x.tmem + tGram, dMN(x.sbase + Prod::oQP, oKP - (uint32_t)Prod::oQP, s),
+                    dMN(x.sbase + Prod::oKM, 16384, s), id, s > 0);
+            commit(&bars[B_GRAM]);
+        }
+        failed = !wait_bar(&bars[B_GRAM], (uint32_t)(jo & 1), x.flag, a, pc);
+        // L and beta of the back stage's current job are consumed once its solve is done
+        if (!failed && jo >= 1) failed = !wait_bar(&bars[B_LFREE], (uint32_t)((jo - 1) & 1), x.flag, a, pc);
+        if (bar_or(1, 256, failed)) { failed = true; break; }
+        fence_after_sync();
+        {
+            // each warp half reads 32 of the 64 columns of its lane's row
+            const int row = 32 * (pw & 3) + lane;
+            float v[32];
+            tmem_ld32(x.tmem + lane_off + tGram + half, v);
+            if (row < 64) {
+                // Aqk (lower, diagonal included) -> bf16 [tok][tok'], K-major B operand
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int col = (int)half + 8 * c8 + e;
+                        y[e] = col <= row ? v[8 * c8 + e] : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + Prod::oAQ + sw128(row, (int)(half >> 3) + c8)) = pack8(y);
+                }
+            } else {
+                // L = diag(beta) strict_lower(M), fp32
+                const int r = row - 64;
+                const float br = Bf[r];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const int col = (int)half + e;
+                    float4 y;
+                    y.x = col < r ? br * v[e] : 0.f;
+                    y.y = col + 1 < r ? br * v[e + 1] : 0.f;
+                    y.z = col + 2 < r ? br * v[e + 2] : 0.f;
+                    y.w = col + 3 < r ? br * v[e + 3] : 0.f;
+                    *reinterpret_cast<float4 *>(L + r * LDF + col) = y;
+                }
+            }
+            if (ptid < 64) reinterpret_cast<float *>(sm + Prod::oBH)[ptid] = Bf[ptid];
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        bar_named(1, 256);
+        if (ptid == 0) mbar_arrive(&bars[B_HFULL0 + b]);
+        if (ptid == kIssImg) {
+            // Qp^T, Kbar^T, Aqk, e^gamma_n -> the ring slot, one bulk store; once it is
+            // written the image buffer is free and the back stage may publish the job
+            bulk_store(slot_ptr(pc, u, c) + Slot::oQP, sm + Prod::oIMG, Slot::kFrontBytes);
+            bulk_commit();
+            bulk_wait_done();
+            *x.stored = jo + 1;
+        }
+        it = nx;
+        have = have_next;
+    }
+    if (failed) *x.flag = 1;
+    return pend;
+}
+
+// ---------------------------------------------------------------------------------------
+// producer, back stage (warps 8-15): solve, WY factors, publication of the slot.
+// Returns 0, or 1 + the parity of a V load that may still be in flight (abort path).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &maps, const PcArgs &pc, const Ctx &x) {
+    unsigned char *sm = x.sm;
+    uint64_t *bars = x.bars;
+    const int ptid = threadIdx.x - 256, pw = ptid >> 5, lane = ptid & 31, warp = threadIdx.x >> 5;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
+    const uint32_t half = (uint32_t)(pw >> 2) * 32u;                // column half of a 64-wide readback
+    constexpr int kPublisher = 224;  // lane 0 of the last warp: stores and publishes the slot
+    float *Tm = reinterpret_cast<float *>(sm + Prod::oT);
+    const float *L = reinterpret_cast<const float *>(sm + Prod::oL);
+    const float *Bs = reinterpret_cast<const float *>(sm + Prod::oBH);
+    int pend_v = -1;
+    auto stage_v = [&](const JobIt &j, int jo) {
+        if (ptid == 0 || ptid == 32) {  // the two d_v halves from two warps
+            const int h = j.u % a.H_v;
+            const int y = (int)(x.units[j.u].bos + (int64_t)j.c * kChunk);
+            if (ptid == 0) {
+                mbar_arrive_expect_tx(&bars[B_LV], 16384);
+                tma_load_2d(sm + Prod::oRV, &maps.v, &bars[B_LV], h * 128, y);
+            } else {
+                tma_load_2d(sm + Prod::oRV + 8192, &maps.v, &bars[B_LV], h * 128 + 64, y);
+            }
+        }
+        pend_v = jo & 1;
+    };
+
+    // Publication of chunk pcn of unit pu, job ordinal pjo of this producer, once its W^T and
+    // U^T stores and its front image are written. It depends on nothing later than the job.
+    auto publish = [&](int pu, int pcn, int pjo) -> bool {
+        bulk_wait_done();
+        if (!wait_count(x.stored, pjo + 1, x.flag, a, pc)) return false;
+        fence_proxy_async_global();
+        st_release(&pc.ready[pu * kRing + pcn % kRing], pcn + 1);
+        return true;
+    };
+
+    JobIt it{0, -1, -1};
+    bool have = next_job(it, x, pc);
+    if (have) stage_v(it, 0);
+    bool failed = false;
+    int prev_u = -1, prev_c = 0;
+    int jo = 0;
+    for (; have; ++jo) {
+        const int u = it.u, c = it.c, b = jo & 1;
+        const int row0 = c * kChunk;
+        const int nvalid = min(kChunk, x.units[u].len - row0);
+        const int nz = kChunk - nvalid;
+        JobIt nx = it;
+        const bool have_next = next_job(nx, x, pc);
+        unsigned char *slot = slot_ptr(pc, u, c);
+        const uint32_t oKP = b ? Prod::oKP1 : Prod::oKP0;
+
+        // The previous job is published while this stage would wait for the front stage;
+        // when the front stage is already done with this job, the publisher does it during
+        // the diagonal solve instead (its warp is idle there). Either way it waits on
+        // nothing later than that job.
+        bool defer = false;
+        if (ptid == kPublisher && jo > 0) {
+            defer = mbar_try_wait(&bars[B_HFULL0 + b], (uint32_t)((jo >> 1) & 1));
+            if (!defer) failed = !publish(prev_u, prev_c, jo - 1);
+        }
+        if (!failed) failed = !wait_bar(&bars[B_HFULL0 + b], (uint32_t)((jo >> 1) & 1), x.flag, a, pc);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
+
+        // ---- solve: T = (I + L)^-1 -----------------------------------------------------------
+        // the 16x16 diagonal inverses by forward substitution, one column per lane
+        if (pw < 4 && lane < 16) {
+            const int b0 = 16 * pw, j = lane;
+            float v[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float s = (r == j) ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) s -= L[(b0 + r) * LDF + b0 + m] * v[m];
+                v[r] = s;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tm[(b0 + r) * LDF + b0 + j] = v[r];
+        }
+        if (defer) failed = !publish(prev_u, prev_c, jo - 1);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
+        // Off-diagonal blocks column by column: warp pw owns the 8 columns col0..col0+7 of T
+        // (column block j = pw / 2). T_jj = D_j, and for i > j
+        //   T_ij = -D_i sum_{k=j}^{i-1} L_ik T_kj
+        // (tf32 mma.sync, fp32 accumulation, one accumulator per k so that the products of a
+        // step run side by side). The warp then writes its columns of T_beta = T diag(beta)
+        // (lower triangle) in bf16. Each warp reads only L, the diagonal blocks and its own
+        // columns, so no barrier is needed inside.
+        {
+            const int j = pw >> 1, col0 = 16 * j + 8 * (pw & 1);
+            const int g8 = lane >> 2, t4 = lane & 3;
+            float *P = reinterpret_cast<float *>(sm + Prod::oPS) + pw * 128;  // 16x8 scratch
+            for (int i = j + 1; i < 4; ++i) {
+                float acc[3][4];
+#pragma unroll
+                for (int kk = 0; kk < 3; ++kk) acc[kk][0] = acc[kk][1] = acc[kk][2] = acc[kk][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 3; ++kk)
+                    if (j + kk < i)
+                        mm16x8_tf32(acc[kk], L + (16 * i) * LDF + 16 * (j + kk), LDF, Tm + (16 * (j + kk)) * LDF + col0,
+                                    LDF, lane);
+                P[g8 * 8 + 2 * t4] = acc[0][0] + acc[1][0] + acc[2][0];
+                P[g8 * 8 + 2 * t4 + 1] = acc[0][1] + acc[1][1] + acc[2][1];
+                P[(g8 + 8) * 8 + 2 * t4] = acc[0][2] + acc[1][2] + acc[2][2];
+                P[(g8 + 8) * 8 + 2 * t4 + 1] = acc[0][3] + acc[1][3] + acc[2][3];
+                __syncwarp();
+                float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+                mm16x8_tf32(acc2, Tm + (16 * i) * LDF + 16 * i, LDF, P, 8, lane);
+                float *Tij = Tm + (16 * i) * LDF + col0;
+                Tij[g8 * LDF + 2 * t4] = -acc2[0];
+                Tij[g8 * LDF + 2 * t4 + 1] = -acc2[1];
+                Tij[(g8 + 8) * LDF + 2 * t4] = -acc2[2];
+                Tij[(g8 + 8) * LDF + 2 * t4 + 1] = -acc2[3];
+                __syncwarp();
+            }
+            const float4 b0 = *reinterpret_cast<const float4 *>(Bs + col0);
+            const float4 b1 = *reinterpret_cast<const float4 *>(Bs + col0 + 4);
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = lane + 32 * hh;
+                float v[8];
+                if (r < 16 * j) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                } else {
+                    const float4 t0 = *reinterpret_cast<const float4 *>(Tm + r * LDF + col0);
+                    const float4 t1 = *reinterpret_cast<const float4 *>(Tm + r * LDF + col0 + 4);
+                    const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = (col0 + e) <= r ? tv[e] * bv[e] : 0.f;
+                }
+                *reinterpret_cast<uint4 *>(sm + Prod::oTB + sw128(r, col0 >> 3)) = pack8(v);
+            }
+        }
+        failed = !wait_bar(&bars[B_LV], (uint32_t)(jo & 1), x.flag, a, pc);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
+        pend_v = -1;
+        if (ptid == 0) mbar_arrive(&bars[B_LFREE]);  // L and beta are consumed
+        if (nz > 0) {
+            for (int i = ptid; i < nz * 16; i += 256) {
+                const int r = nvalid + (i >> 4), c16 = i & 15;
+                *reinterpret_cast<uint4 *>(sm + Prod::oRV + (c16 >> 3) * 8192 + r * 128 + (c16 & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_proxy_async();
+        bar_named(2, 256);
+
+        // ---- WY factors: D_W = Kp^T T_beta^T, D_U = V^T T_beta^T ------------------------------
+        if (ptid == 0) {
+            fence_after_sync();
+            const uint32_t idw = idesc_bf16(128, 64, false, false, false);
+            const uint32_t idu = idesc_bf16(128, 64, true, false, false);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t bd = dK(x.sbase + Prod::oTB, 8192, s);
+                mma(x.tmem + tW, dK(x.sbase + oKP, 16384, s), bd, idw, s > 0);
+                mma(x.tmem + tU, dMN(x.sbase + Prod::oRV, 8192, s), bd, idu, s > 0);
+            }
+            commit(&bars[B_WMMA]);
+        }
+        failed = !wait_bar(&bars[B_WMMA], (uint32_t)(jo & 1), x.flag, a, pc);
+        if (bar_or(2, 256, failed)) { failed = true; break; }
+        if (ptid == 0) mbar_arrive(&bars[B_HEMPTY0 + b]);  // Kp^T of slot b is consumed
+        fence_after_sync();
+        {
+            // row d of W^T and of U^T; each warp half takes 32 of the 64 tokens. W^T goes to
+            // the (now free) T buffer as the swizzled [d][tok] image, U^T to the V buffer as
+            // bf16 token pairs.
+            const int d = 32 * (warp & 3) + lane;
+            float v[32];
+            tmem_ld32(x.tmem + lane_off + tW + half, v);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = v[8 * c8 + e];
+                *reinterpret_cast<uint4 *>(sm + Prod::oT + sw128(d, (int)(half >> 3) + c8)) = pack8(y);
+            }
+            tmem_ld32(x.tmem + lane_off + tU + half, v);
+            uint32_t *U2 = reinterpret_cast<uint32_t *>(sm + Prod::oRV);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) U2[((int)(half >> 1) + e) * 128 + d] = pack_bf16(v[2 * e], v[2 * e + 1]);
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        bar_named(2, 256);
+        if (ptid == kPublisher) {
+            bulk_store(slot + Slot::oWT, sm + Prod::oT, 16384);
+            bulk_store(slot + Slot::oU, sm + Prod::oRV, 16384);
+            bulk_commit();
+            bulk_wait_read();
+        }
+        bar_named(2, 256);  // the T and V buffers are free again
+        if (have_next) stage_v(nx, jo + 1);
+        prev_u = u;
+        prev_c = c;
+        it = nx;
+        have = have_next;
+    }
+    if (!failed && ptid == kPublisher && prev_u >= 0) failed = !publish(prev_u, prev_c, jo - 1);
+    if (failed) *x.flag = 1;
+    return pend_v + 1;
+}
+
+// ---------------------------------------------------------------------------------------
+// consumer, loader (warps 4-7): slot images of unit u into the two shared buffers, each as
+// four bulk copies from four warps (so that they overlap). Returns, for thread 128, 0 or
+// 1 + 2 * buffer + parity of copies that may still be in flight.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &pc, const Ctx &x, int u, int nch) {
+    uint64_t *bars = x.bars;
+    const int lt = threadIdx.x - 128, lw = lt >> 5, lane = lt & 31;
+    constexpr uint32_t kPart = Slot::kBytes / 4;
+    static_assert(Slot::kBytes % 64 == 0, "four 16-byte aligned parts");
+    int pend = 0;
+    bool failed = false;
+    for (int c = 0; c < nch; ++c) {
+        const int b = c & 1;
+        if (lt == 0 && !failed) {
+            // buffer b held chunk c - 2 until the serial step released it
+            if (c >= 2) failed = !wait_bar(&bars[B_EMPTY0 + b], (uint32_t)(((c >> 1) - 1) & 1), x.flag, a, pc);
+            if (!failed) failed = !wait_geq(&pc.ready[u * kRing + c % kRing], c + 1, x.flag, a, pc);
+            if (!failed) mbar_arrive_expect_tx(&bars[B_FULL0 + b], Slot::kBytes);
+        }
+        if (bar_or(2, 128, failed)) {
+            failed = true;
+            break;
+        }
+        if (lane == 0) {
+            fence_proxy_async_global();  // the producers' generic writes, before the async-proxy read
+            bulk_load(x.sm + (b ? Cons::oBuf1 : Cons::oBuf0) + lw * kPart, slot_ptr(pc, u, c) + lw * kPart, kPart,
+                      &bars[B_FULL0 + b]);
+        }
+        pend = 1 + 2 * b + ((c >> 1) & 1);
+        if (lt == 0) {
+            failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c >> 1) & 1), x.flag, a, pc);
+            if (!failed) {
+                st_release(&pc.done[u], c + 1);  // the ring slot may be overwritten
+                pend = 0;
+            }
+        }
+    }
+    return lt == 0 ? pend : 0;
+}
+
+// ---------------------------------------------------------------------------------------
+// consumer, serial step (warps 0-3 and 8-11): row dv of S^T (fp32 in TMEM) belongs to lane
+// dv % 32 of warps dv / 32 and 8 + dv / 32, which take the column halves 0-63 and 64-127
+// of every element pass (the two warps reach the same TMEM lanes).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &pc, const Ctx &x, int u) {
+    unsigned char *sm = x.sm;
+    const uint32_t sbase = x.sbase, tmem = x.tmem;
+    uint64_t *bars = x.bars;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = warp >> 3;                 // column half
+    const int dv = 32 * (warp & 3) + lane;     // row of S^T and of O^T
+    const bool lead = threadIdx.x == 0;        // issues the MMAs
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int n = u / a.H_v, h = u % a.H_v;
+    const int len = x.units[u].len, nchunks = x.units[u].nch;
+    const int64_t bos = x.units[u].bos;
+    const int64_t sv = (int64_t)a.H_v * 128;
+    bf16 *o = static_cast<bf16 *>(a.o);
+    const uint32_t tSc = tS + 64 * grp, tSAc = tSA + 32 * grp;  // this thread's columns
+
+    // S^T row dv, columns 64 grp .. +63 (from h0, or zero) -> TMEM fp32 and its bf16 copy
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int d = 64 * grp + 32 * pass + e;
+            v[e] = a.h0 ? a.h0[(((int64_t)n * a.H_v + h) * 128 + d) * 128 + dv] : 0.f;
+        }
+        uint32_t f0[16], f1[16], p16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            f0[e] = __float_as_uint(v[e]);
+            f1[e] = __float_as_uint(v[16 + e]);
+            p16[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+        }
+        tmem_st16(tmem + lane_off + tSc + 32 * pass, f0);
+        tmem_st16(tmem + lane_off + tSc + 32 * pass + 16, f1);
+        tmem_st16(tmem + lane_off + tSAc + 16 * pass, p16);
+    }
+    tmem_st_wait();
+    fence_before_sync();
+    bar_named(1, 256);
+
+    bool failed = false;
+    for (int c = 0; c < nchunks; ++c) {
+        const int row0 = c * kChunk;
+        const int nvalid = min(kChunk, len - row0);
+        const int b = c & 1;
+        const uint32_t oB = b ? Cons::oBuf1 : Cons::oBuf0;
+        const float *EG = reinterpret_cast<const float *>(sm + oB + Slot::oEG);
+        const uint32_t *U2 = reinterpret_cast<const uint32_t *>(sm + oB + Slot::oU);
+
+        failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c >> 1) & 1), x.flag, a, pc);
+        if (bar_or(1, 256, failed)) { failed = true; break; }
+        fence_after_sync();
+
+        // D_X = S^T [W^T | Qp^T]  (A: S^T bf16 in TMEM; B: the W^T and Qp^T tiles, MN-major)
+        if (lead) {
+            const uint32_t id = idesc_bf16(128, 128, false, true, false);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_ts(tmem + tX, tmem + tSA + 8 * s, dMN(sbase + oB + Slot::oWT, Slot::oQP - Slot::oWT, s), id,
+                       s > 0);
+            commit(&bars[B_X]);
+        }
+        // meanwhile S^T <- S^T Diag(e^gamma_n): column d of S^T scales by e^gamma_n[d]
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            float v[32];
+            tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
+            const float *eg = EG + 64 * grp + 32 * pass;
+            uint32_t y0[16], y1[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                y0[e] = __float_as_uint(v[e] * eg[e]);
+                y1[e] = __float_as_uint(v[16 + e] * eg[16 + e]);
+            }
+            tmem_st16(tmem + lane_off + tSc + 32 * pass, y0);
+            tmem_st16(tmem + lane_off + tSc + 32 * pass + 16, y1);
+        }
+        tmem_st_wait();
+
+        failed = !wait_bar(&bars[B_X], (uint32_t)(c & 1), x.flag, a, pc);
+        if (bar_or(1, 256, failed)) { failed = true; break; }
+        fence_after_sync();
+        // Vt^T = U^T - S^T W^T for tokens 32 grp .. +31 -> bf16 token pairs at tV
+        {
+            float pp[32];
+            tmem_ld32(tmem + lane_off + tX + 32 * grp, pp);
+            uint32_t v16[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const uint32_t uw = U2[(16 * grp + e) * 128 + dv];  // tokens 32 grp + 2e, + 1
+                const float u0 = __uint_as_float(uw << 16), u1 = __uint_as_float(uw & 0xffff0000u);
+                v16[e] = pack_bf16(u0 - pp[2 * e], u1 - pp[2 * e + 1]);
+            }
+            tmem_st16(tmem + lane_off + tV + 16 * grp, v16);
+        }
+        tmem_st_wait();
+        fence_before_sync();
+        bar_named(1, 256);
+
+        // O^T += Vt^T Aqk^T;  S^T += Vt^T Kbar  (A: Vt^T bf16 in TMEM)
+        if (lead) {
+            fence_after_sync();
+            const uint32_t ido = idesc_bf16(128, 64, false, false, false);
+            const uint32_t ids = idesc_bf16(128, 128, false, false, false);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                mma_ts(tmem + tX + 64, tmem + tV + 8 * s, dK(sbase + oB + Slot::oAQ, 8192, s), ido, 1);
+                mma_ts(tmem + tS, tmem + tV + 8 * s, dK(sbase + oB + Slot::oKB, 16384, s), ids, 1);
+            }
+            commit(&bars[B_S2]);
+        }
+        failed = !wait_bar(&bars[B_S2], (uint32_t)(c & 1), x.flag, a, pc);
+        if (bar_or(1, 256, failed)) { failed = true; break; }
+        fence_after_sync();
+        if (lead) mbar_arrive(&bars[B_EMPTY0 + b]);  // buffer b consumed
+
+        // S^T -> bf16 operand for the next chunk
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            float v[32];
+            tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
+            uint32_t p16[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) p16[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            tmem_st16(tmem + lane_off + tSAc + 16 * pass, p16);
+        }
+        tmem_st_wait();
+        // O^T row dv, tokens 32 grp .. +31 -> o[token][dv] (valid tokens only) through a
+        // [32 tok][128 dv] staging tile per half so that global stores are 16 bytes wide
+        {
+            bf16 *OS = reinterpret_cast<bf16 *>(sm + Cons::oOS + grp * 8192);
+            float v[32];
+            tmem_ld32(tmem + lane_off + tX + 64 + 32 * grp, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) OS[e * 128 + dv] = __float2bfloat16_rn(v[e]);
+        }
+        bar_named(1, 256);
+        {
+            const int st = (grp << 7) + (threadIdx.x & 127);  // 0..255
+#pragma unroll
+            for (int i = st; i < 1024; i += 256) {
+                const int r = i >> 4, c16 = i & 15;  // r: token 0..63 of the chunk
+                if (r < nvalid)
+                    *reinterpret_cast<uint4 *>(o + (bos + row0 + r) * sv + (int64_t)h * 128 + c16 * 8) =
+                        *reinterpret_cast<const uint4 *>(sm + Cons::oOS + (r >> 5) * 8192 + (r & 31) * 256 + c16 * 16);
+            }
+        }
+        fence_before_sync();
+        bar_named(1, 256);  // the staging tiles and tX are free for the next chunk
+    }
+    if (failed) {
+        *x.flag = 1;
+        return;
+    }
+    if (a.ht != nullptr) {
+        float *ht = a.ht + ((int64_t)n * a.H_v + h) * 128 * 128 + dv;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            float v[32];
+            tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ht[(int64_t)(64 * grp + 32 * pass + e) * 128] = v[e];
+        }
+    }
+}
+
+template <bool GATE_HEAD>
+__global__ void __launch_bounds__(kThreads, 1)
+    kda_fwd_pc_kernel(const FwdArgs a, const __grid_constant__ TcMaps maps, const PcArgs pc) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Common::oBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Common::oTmemAddr);
+    volatile int *flag = reinterpret_cast<volatile int *>(sm + Common::oFlag);
+    int *stats = reinterpret_cast<int *>(sm + Common::oFlag + 4);  // most chunks, uniform
+    volatile int *stored = reinterpret_cast<volatile int *>(sm + Common::oFlag + 12);
+    UnitInfo *units = reinterpret_cast<UnitInfo *>(sm + Common::oUnits);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const bool consumer = (int)blockIdx.x < pc.U;
+    const uint32_t ncols = consumer ? kTmemCons : kTmemProd;
+
+    // unit table: sequence bounds of every unit (a malformed entry becomes len = -1)
+    for (int i = tid; i < pc.U; i += kThreads) {
+        const int n = i / a.H_v;
+        UnitInfo ui;
+        if (a.cu_seqlens == nullptr) {
+            ui.bos = (long long)n * a.T;
+            ui.len = a.T;
+        } else {
+            const int s = a.cu_seqlens[n], e = a.cu_seqlens[n + 1];
+            const bool ok = s >= 0 && e >= s && e <= a.T;
+            ui.bos = ok ? s : 0;
+            ui.len = ok ? e - s : -1;
+        }
+        ui.nch = ui.len > 0 ? (ui.len + kChunk - 1) / kChunk : 0;
+        units[i] = ui;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
+        *flag = 0;
+        *stored = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, ncols);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+        int mx = 0, uni = 1;
+        for (int i = 0; i < pc.U; ++i) mx = max(mx, units[i].nch);
+        for (int i = 0; i < pc.U; ++i) uni &= units[i].nch == mx ? 1 : 0;
+        stats[0] = mx;
+        stats[1] = uni;
+    }
+    __syncthreads();
+
+    Ctx x;
+    x.sm = sm;
+    x.sbase = smem_u32(sm);
+    x.tmem = *tmem_slot;
+    x.bars = bars;
+    x.flag = flag;
+    x.stored = stored;
+    x.units = units;
+    x.maxc = stats[0];
+    x.uniform = stats[1];
+    x.p = (int)blockIdx.x - pc.U;
+
+    uint32_t pend_front = 0;
+    int pend_back = 0, pend_load = 0;
+    if (consumer) {
+        const int u = blockIdx.x;
+        if (units[u].len < 0) {
+            if (tid == 0) atomicOr(a.err, kDeviceErrSeqlens);  // the unit is skipped, as in every kernel
+        } else if (warp < 4 || (warp >= 8 && warp < 12)) {
+            consumer_serial(a, pc, x, u);
+        } else if (warp < 8) {
+            pend_load = consumer_loader(a, pc, x, u, units[u].nch);
+        }
+    } else if (tid < 256) {
+        pend_front = producer_front<GATE_HEAD>(a, maps, pc, x);
+    } else {
+        pend_back = producer_back(a, maps, pc, x);
+    }
+
+    fence_before_sync();
+    if (__syncthreads_or(*flag != 0)) {
+        // drain: every MMA and copy this CTA issued must land before TMEM is freed and the
+        // CTA exits (bounded waits)
+        const bool issuer = tid == 0 || (!consumer && tid == 256);
+        if (issuer) {
+            fence_after_sync();
+            uint64_t *z = &bars[consumer ? B_CZ : (tid == 0 ? B_PZ0 : B_PZ1)];
+            commit(z);
+            mbar_wait(z, 0, kWaitCycles);
+        }
+        if (consumer && tid == 128 && pend_load > 0)
+            mbar_wait(&bars[B_FULL0 + ((pend_load - 1) >> 1)], (uint32_t)((pend_load - 1) & 1), kWaitCycles);
+        if (!consumer && tid == 0) {
+            if (pend_front & 1u) mbar_wait(&bars[B_LQK], (pend_front >> 4) & 1u, kWaitCycles);
+            if (pend_front & 2u) mbar_wait(&bars[B_LG], (pend_front >> 5) & 1u, kWaitCycles);
+        }
+        if (!consumer && tid == 256 && pend_back > 0) mbar_wait(&bars[B_LV], (uint32_t)(pend_back - 1), kWaitCycles);
+        cp_async_wait_all();
+        bulk_wait_done();
+        fence_before_sync();
+        __syncthreads();
+    }
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(x.tmem, ncols);
+    }
+}
+
+// Stream-ordered scratch (ring and flags) from a pool owned by the library, one per
+// device, that keeps its memory between calls.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t scratch_pool(int dev, cudaMemPool_t *out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (g_pool[dev] == nullptr) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return e;
+        }
+        g_pool[dev] = pool;
+    }
+    *out = g_pool[dev];
+    return cudaSuccess;
+}
+
+template <bool GATE_HEAD>
+cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
+    *launched = false;
+    int dev = 0, sms = 0, coop = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t U = (int64_t)a.N * a.H_v;
+    // worth it only when the units leave at least as many SMs idle as they occupy
+    if (!coop || U < 1 || U > kMaxUnits || 2 * U > sms) return cudaSuccess;
+    auto kern = kda_fwd_pc_kernel<GATE_HEAD>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Common::kBytes);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Common::kBytes);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaSuccess;
+
+    TcMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode_tile_maps(&maps, a, GATE_HEAD)) return cudaErrorInvalidValue;
+
+    const size_t ring_bytes = (size_t)U * kRing * Slot::kStride;
+    const size_t flag_words = (size_t)U * kRing + (size_t)U + 1;
+    const size_t flag_bytes = (flag_words * sizeof(int) + 255) & ~(size_t)255;
+    cudaMemPool_t pool = nullptr;
+    e = scratch_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    void *buf = nullptr;
+    e = cudaMallocFromPoolAsync(&buf, ring_bytes + flag_bytes, pool, stream);
+    if (e != cudaSuccess) return e;
+    PcArgs pc;
+    pc.ring = static_cast<unsigned char *>(buf);
+    pc.ready = reinterpret_cast<int *>(pc.ring + ring_bytes);
+    pc.done = pc.ready + (size_t)U * kRing;
+    pc.abort = pc.done + U;
+    pc.U = (int)U;
+    pc.P = sms - (int)U;
+    e = cudaMemsetAsync(pc.ready, 0, flag_bytes, stream);
+    if (e == cudaSuccess) {
+        void *args[] = {const_cast<FwdArgs *>(&a), &maps, &pc};
+        e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(sms), dim3(kThreads), args,
+                                        Common::kBytes, stream);
+        if (e == cudaSuccess) *launched = true;
+    }
+    const cudaError_t ef = cudaFreeAsync(buf, stream);
+    return e != cudaSuccess ? e : ef;
+}
+
+}  // namespace
+
+// The persistent kernel when the call has at most half as many units as the device has
+// SMs; *launched tells whether it ran (otherwise nothing was launched).
+cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
+    return a.gate_per_head ? launch_pc<true>(a, stream, launched) : launch_pc<false>(a, stream, launched);
+}
+
+}  // namespace kda

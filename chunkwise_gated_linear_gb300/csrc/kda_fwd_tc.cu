@@ -27,14 +27,9 @@
 //
 // Every mbarrier wait is bounded (about one second); on a timeout the CTA raises
 // KDA_DEVICE_ERR_TIMEOUT, waits (bounded) for the MMAs it issued, frees its TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cstring>
-#include <mutex>
 
-#include "kda_common.cuh"
-#include "tc5.cuh"
+#include "tc_util.cuh"
 
 namespace kda {
 
@@ -42,6 +37,7 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 using namespace tc5;
+using namespace tcu;
 
 // Shared-memory plan (byte offsets from a 1024-byte aligned base). Tiles named [d][tok]
 // hold one row per d_k channel and 64 tokens per 128-byte row (one swizzle atom).
@@ -74,7 +70,6 @@ struct WsLayout {
     static constexpr int oOS = oPS + 4096;        // O staging [32 tok][128] bf16 (serial)
     static constexpr int kBytes = oOS + 8192 + 1024;  // + slack to align the base
 };
-constexpr int LDF = 68;  // fp32 row stride of L and T
 
 // TMEM columns (512 allocated)
 constexpr uint32_t tGW = 0;    // Gram D_G, then W^T (prep)
@@ -84,7 +79,6 @@ constexpr uint32_t tSA = 256;  // S^T in bf16 (64 packed columns)
 constexpr uint32_t tS = 320;   // S^T fp32 (128)
 constexpr uint32_t tU1 = 448;  // U^T, slot 1 (64)
 constexpr uint32_t kTmemCols = 512;
-constexpr long long kWaitCycles = 1ll << 31;  // about one second
 
 enum {
     BAR_LQK = 0, // TMA tiles of a chunk: Q and K
@@ -104,76 +98,9 @@ enum {
     kNumBars
 };
 
-// Tensor maps of the per-chunk tiles (TMA): q, k [tokens][H_k*128] bf16 (box 128 x 64),
-// v [tokens][H_v*128] bf16 (box 64 x 64, 128-byte swizzle), g [tokens][H_v*128] fp32 (box 128 x 64).
-struct TcMaps {
-    CUtensorMap q, k, v, g;
-};
-
-__device__ __forceinline__ uint32_t tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// acc (16x8) += A (16x16, stride lda) * B (16x8, stride ldb); fp32 in smem, tf32 products.
-__device__ __forceinline__ void mm16x8_tf32(float (&acc)[4], const float *A, int lda, const float *B, int ldb,
-                                            int lane) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t a0 = tf32(A[g * lda + 8 * ks + t]);
-        const uint32_t a1 = tf32(A[(g + 8) * lda + 8 * ks + t]);
-        const uint32_t a2 = tf32(A[g * lda + 8 * ks + t + 4]);
-        const uint32_t a3 = tf32(A[(g + 8) * lda + 8 * ks + t + 4]);
-        const uint32_t b0 = tf32(B[(8 * ks + t) * ldb + g]);
-        const uint32_t b1 = tf32(B[(8 * ks + t + 4) * ldb + g]);
-        mma_tf32(acc, a0, a1, a2, a3, b0, b1);
-    }
-}
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-    uint4 u;
-    u.x = pack_bf16(x[0], x[1]);
-    u.y = pack_bf16(x[2], x[3]);
-    u.z = pack_bf16(x[4], x[5]);
-    u.w = pack_bf16(x[6], x[7]);
-    return u;
-}
-
-// K-major operand descriptor, K step s (16 elements) of a tile whose K atoms are `atom_bytes` apart.
-__device__ __forceinline__ uint64_t dK(uint32_t base, uint32_t atom_bytes, int s) {
-    return desc_sw128(base + (uint32_t)(s >> 2) * atom_bytes + (uint32_t)(s & 3) * 32u, 0, 1024);
-}
-// MN-major operand descriptor, K step s (16 rows) of a tile whose MN atoms are `atom_bytes` apart.
-__device__ __forceinline__ uint64_t dMN(uint32_t base, uint32_t atom_bytes, int s) {
-    return desc_sw128(base + (uint32_t)s * 2048u, atom_bytes, 1024);
-}
-
-// TMEM (this warp's 32 lanes, columns [col, col+32)) -> 32 floats.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    float a[16], b[16];
-    tmem_ld16(taddr, a);
-    tmem_ld16(taddr + 16, b);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        v[i] = a[i];
-        v[16 + i] = b[i];
-    }
-}
 
 __device__ __forceinline__ void bar_serial() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 __device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // Bounded wait on an mbarrier phase; gives up early when the CTA is aborting. On its own
 // timeout it marks the CTA as aborting. Returns false when the phase did not complete.
@@ -188,20 +115,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
         }
     }
     return true;
-}
-// OR of `v` over the `count` threads of named barrier `id` (all of them take the same branch).
-__device__ __forceinline__ bool bar_or(int id, int count, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t"
-        "}\n"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
 }
 
 struct Unit {
@@ -810,32 +723,6 @@ __global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, con
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2-D map over a [rows][inner] row-major tensor with a (box0 x 64-row) box.
-bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t rows,
-                uint64_t elem_bytes, uint32_t box0, CUtensorMapSwizzle sw) {
-    auto enc = tensor_map_encoder();
-    if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {inner * elem_bytes};
-    const cuuint32_t box[2] = {box0, 64};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <bool GATE_HEAD>
 cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
@@ -845,19 +732,7 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     TcMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    const uint64_t rows = a.cu_seqlens ? (uint64_t)a.T : (uint64_t)a.N * (uint64_t)a.T;
-    if (rows > 0) {
-        bool ok = encode_map(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, (uint64_t)a.H_k * 128, rows, 2, 128,
-                             CU_TENSOR_MAP_SWIZZLE_NONE) &&
-                  encode_map(&maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, (uint64_t)a.H_k * 128, rows, 2, 128,
-                             CU_TENSOR_MAP_SWIZZLE_NONE) &&
-                  encode_map(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v, (uint64_t)a.H_v * 128, rows, 2, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-        if (ok && !GATE_HEAD)
-            ok = encode_map(&maps.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.g, (uint64_t)a.H_v * 128, rows, 4, 128,
-                            CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (!ok) return cudaErrorInvalidValue;
-    }
+    if (!encode_tile_maps(&maps, a, GATE_HEAD)) return cudaErrorInvalidValue;
     const dim3 grid(1, a.H_v, a.N);
     kern<<<grid, 384, kSmem, stream>>>(a, maps);
     return cudaGetLastError();

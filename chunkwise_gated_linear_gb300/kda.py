@@ -24,6 +24,7 @@ KDA_DTYPE_BF16 = 0
 KDA_DTYPE_F32 = 1
 KDA_GATE_PER_CHANNEL = 0
 KDA_GATE_PER_HEAD = 1
+KDA_FLAG_ONE_CTA_PER_UNIT = 1
 KDA_DEVICE_ERR_SEQLENS = 1
 KDA_DEVICE_ERR_TIMEOUT = 2
 
@@ -113,7 +114,8 @@ def _ptr(t):
 
 
 def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
-                  output_final_state=True, chunk_size=64, o=None, ht=None, stream=None):
+                  output_final_state=True, chunk_size=64, o=None, ht=None, stream=None,
+                  one_cta_per_unit=False):
     """Chunkwise KDA forward on torch CUDA tensors; returns ``(o, ht)``.
 
     q, k [B, T, H_k, d_k] and v [B, T, H_v, d_v], all bf16 or all fp32; g fp32
@@ -121,7 +123,8 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
     [B, T, H_v]; h0 fp32 [N, H_v, d_k, d_v] or None. With ``cu_seqlens`` (int32 [N + 1]
     on the device) B must be 1 and the N sequences are packed along T. ``o`` and ``ht``
     may be given to write into existing buffers. ``ht`` is None in the result when
-    ``output_final_state`` is False.
+    ``output_final_state`` is False. ``one_cta_per_unit`` sets KDA_FLAG_ONE_CTA_PER_UNIT
+    (never the persistent kernel that occupies every SM).
     """
     import torch
 
@@ -176,7 +179,8 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
         stream = torch.cuda.current_stream(q.device).cuda_stream
     p = kda_fwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0) or None, _ptr(o),
                        _ptr(ht) or None, nb, nt, H_k, H_v, d_k, d_v, chunk_size, float(scale),
-                       _ptr(cu_seqlens) or None, dtype, gate, 0)
+                       _ptr(cu_seqlens) or None, dtype, gate,
+                       KDA_FLAG_ONE_CTA_PER_UNIT if one_cta_per_unit else 0)
     st = kda_chunk_fwd_ex(p, stream)
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd_ex")

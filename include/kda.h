@@ -46,7 +46,8 @@
  *   T == 0 (or empty sequences) is valid: no o rows, ht = h0 (or 0).
  *
  * Ownership and semantics: the caller owns every buffer; the library allocates no
- *   memory. Calls are asynchronous on `stream` (no host synchronisation). o and ht are
+ *   memory except the stream-ordered scratch of the persistent kernel (see
+ *   KDA_FLAG_ONE_CTA_PER_UNIT), which it frees on the same stream. Calls are asynchronous on `stream` (no host synchronisation). o and ht are
  *   fully overwritten; o and ht must not alias any input. The same inputs give bitwise
  *   equal outputs (no atomics on outputs). The entry points are thread-safe.
  *
@@ -115,8 +116,20 @@ typedef struct kda_fwd_params {
     const int32_t *cu_seqlens;
     int dtype;     /* KDA_DTYPE_BF16 or KDA_DTYPE_F32 */
     int gate_mode; /* KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD */
-    int flags;     /* reserved, must be 0 */
+    int flags;     /* 0 or KDA_FLAG_ONE_CTA_PER_UNIT */
 } kda_fwd_params;
+
+/*
+ * flags of kda_fwd_params. With d_k = d_v = 128 in bf16 and at most half as many
+ * (sequence, value head) units as the device has SMs (and at most 76 units), the library
+ * runs a persistent kernel that occupies every SM: the chunk-local factors of all units
+ * are built in parallel on the SMs the units leave free and handed to one SM per unit
+ * that runs the serial state step. It allocates about 220 KiB per unit of stream-ordered
+ * scratch from a memory pool the library owns (kept between calls). KDA_FLAG_ONE_CTA_PER_UNIT
+ * selects the kernel with one CTA per unit instead, which allocates nothing and leaves
+ * the other SMs free for concurrent work. Both give the same result up to rounding.
+ */
+#define KDA_FLAG_ONE_CTA_PER_UNIT 1
 
 /*
  * kda_chunk_fwd_ex — the general entry point: dtype and gate mode chosen by the struct.

@@ -18,8 +18,8 @@ from kda_cases import TOL, run_gpu, run_oracle, to_device
 pytestmark = pytest.mark.gpu
 
 
-def _check(x, tag=""):
-    o, ht = run_gpu(x)
+def _check(x, tag="", **kw):
+    o, ht = run_gpu(x, **kw)
     o_r, ht_r = run_oracle(x)
     assert np.isfinite(o).all() and np.isfinite(ht).all()
     e_o, e_h = rel_l2(o, o_r), rel_l2(ht, ht_r)
@@ -125,7 +125,8 @@ def test_resume_from_final_state():
     assert torch.equal(torch.cat([o1, o2], dim=1), o) and torch.equal(h2, ht)
 
 
-def test_malformed_cu_seqlens_raise_the_device_error():
+@pytest.mark.parametrize("one_cta", [False, True])
+def test_malformed_cu_seqlens_raise_the_device_error(one_cta):
     import torch
 
     from chunkwise_gated_linear_gb300 import chunk_kda_fwd, kda_get_device_error
@@ -135,6 +136,46 @@ def test_malformed_cu_seqlens_raise_the_device_error():
     stream = torch.cuda.current_stream().cuda_stream
     assert kda_get_device_error(stream) == 0
     bad = torch.tensor([0, 90, 60], dtype=torch.int32, device="cuda")  # decreasing
-    chunk_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x.scale, cu_seqlens=bad)
+    chunk_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x.scale, cu_seqlens=bad,
+                  one_cta_per_unit=one_cta)
     assert kda_get_device_error(stream) == 1
     assert kda_get_device_error(stream) == 0  # the query clears it
+
+
+# d_k = d_v = 128 in bf16 has two kernels: the persistent producer/consumer kernel (few
+# units) and one CTA per unit (many units, or KDA_FLAG_ONE_CTA_PER_UNIT). Both are held
+# to the oracle on the same inputs, and to each other.
+@pytest.mark.parametrize("one_cta", [False, True])
+@pytest.mark.parametrize("case", ["varlen_gqa", "head_gate", "long_ragged"])
+def test_bf16_d128_both_kernels(case, one_cta):
+    if case == "varlen_gqa":
+        x = make_inputs((1, 63, 64, 65, 130, 0, 7, 200), 2, 4, 128, 128, seed=112, h0=True,
+                        varlen=True)
+    elif case == "head_gate":
+        x = make_inputs((150, 150), 2, 2, 128, 128, seed=113, gate="head", h0=True)
+    else:
+        # 16 chunks per unit: the ring of chunk slots wraps several times
+        x = make_inputs((1000, 1000), 1, 1, 128, 128, seed=114, h0=True)
+    _check(x, f"{case} one_cta={one_cta}", one_cta_per_unit=one_cta)
+
+
+def test_bf16_d128_persistent_many_jobs_per_producer():
+    # 8 units x 64 chunks = 512 chunk jobs: every producer CTA takes several in a row, and
+    # its two stages and the ring run many laps
+    x = make_inputs((4096,), 8, 8, 128, 128, seed=116, h0=True)
+    _check(x, "persistent, many jobs")
+
+
+def test_bf16_d128_kernels_agree():
+    x = make_inputs((500, 77, 321), 2, 4, 128, 128, seed=115, h0=True, varlen=True)
+    o1, h1 = run_gpu(x)
+    o2, h2 = run_gpu(x, one_cta_per_unit=True)
+    o_r, h_r = run_oracle(x)
+    e1, e2 = rel_l2(o1, o_r), rel_l2(o2, o_r)
+    print(f"persistent o={e1:.3e} ht={rel_l2(h1, h_r):.3e}; one CTA per unit o={e2:.3e} "
+          f"ht={rel_l2(h2, h_r):.3e}; between them o={rel_l2(o1, o2):.3e}")
+    # the same products in bf16 with fp32 accumulation; the persistent kernel hands U^T
+    # from producer to consumer in bf16, one more rounding of the size of a bf16 operand,
+    # so the two differ by about the bf16 unit roundoff and are equally close to the oracle
+    assert rel_l2(o1, o2) < 8e-3 and rel_l2(h1, h2) < 8e-3
+    assert abs(e1 - e2) < 2e-3
