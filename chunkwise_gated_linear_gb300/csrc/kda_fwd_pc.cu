@@ -608,8 +608,16 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
 #pragma unroll
             for (int r = 0; r < 16; ++r) Tm[(b0 + r) * LDF + b0 + j] = v[r];
         }
-        if (defer) failed = !publish(prev_u, prev_c, jo - 1);
-        if (bar_or(2, 256, failed)) { failed = true; break; }
+        // Warps 0-6 go on with the off-diagonal blocks as soon as the diagonal ones are
+        // done; warp 7 (the publisher's) only needs the last diagonal block, from warp 3, and
+        // meets warp 3 on a barrier of their own after publishing.
+        if (pw == 3) asm volatile("bar.arrive 3, 64;" ::: "memory");
+        if (pw == 7) {
+            if (defer) failed = !publish(prev_u, prev_c, jo - 1);
+            bar_named(3, 64);
+        } else {
+            bar_named(4, 224);
+        }
         // Off-diagonal blocks column by column: warp pw owns the 8 columns col0..col0+7 of T
         // (column block j = pw / 2). T_jj = D_j, and for i > j
         //   T_ij = -D_i sum_{k=j}^{i-1} L_ik T_kj
