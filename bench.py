@@ -73,6 +73,18 @@ def algorithmic_flops(x, C=64) -> int:
     return int(round(per_chunk / C * x.T_total * x.H_v))
 
 
+def forward_kernel(x, sms: int) -> str:
+    """The kernel the library's dispatch runs for this workload (see kda_api.cu): with
+    d_k = d_v = 128 in bf16 the persistent producer/consumer kernel when the (sequence,
+    head) units are at most 76 and at most half the SMs, else one CTA per unit."""
+    units = x.N * x.H_v
+    if x.dtype == "f32":
+        return "kda_fwd_f32_kernel"
+    if x.d_k == 128 and x.d_v == 128:
+        return "kda_fwd_pc_kernel" if units <= 76 and 2 * units <= sms else "kda_fwd_tc_kernel"
+    return "kda_fwd_bf16_kernel"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -336,7 +348,8 @@ def run_ours(args, world, rank, local, pg):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": abytes, "kernel": "kda_fwd_tc_kernel",
+                         "algorithmic_bytes_per_launch": abytes,
+                         "kernel": forward_kernel(x, torch.cuda.get_device_properties(dev).multi_processor_count),
                          "tflops": flops / (ms / 1000.0) / 1e12},
             "cpu_baseline": cpu,
             "clocks": clocks,

@@ -70,13 +70,14 @@ struct Prod {
     static constexpr int oKB = oIMG + (Slot::oKB - Slot::oQP);
     static constexpr int oAQ = oIMG + (Slot::oAQ - Slot::oQP);
     static constexpr int oEG = oIMG + (Slot::oEG - Slot::oQP);
-    static constexpr int oKP0 = 107520;    // Kp^T [d][tok], hand-off slots 0 / 1 (Gram A atom 1)
+    static constexpr int oKP0 = 107520;    // Kp^T [d][tok], hand-off slots 0 / 1 (Gram A atom 1);
+                                           // then U^T staging of the back stage
     static constexpr int oKP1 = 123904;
     static constexpr int oKM = 140288;     // Km^T [d][tok]
     static constexpr int oL = 156672;      // L fp32 [64][68] (front -> back)
     static constexpr int oT = 174080;      // T fp32 [64][68]; then W^T staging [d][tok] bf16
     static constexpr int oTB = 191488;     // T_beta [tok][tok'] bf16 (K-major B)
-    static constexpr int oRV = 199680;     // raw V [2 atoms (d_v)][64 tok][128 B]; then U^T staging
+    static constexpr int oRV = 199680;     // raw V [2 atoms (d_v)][64 tok][128 B]
     static constexpr int oBF0 = 216064;    // beta as loaded, job parity 0 / 1
     static constexpr int oBF1 = 216320;
     static constexpr int oBH = 216576;     // beta handed to the back stage
@@ -114,7 +115,7 @@ enum {
     B_LQK = 0, B_LG, B_LV,   // TMA tiles: Q and K, G, V
     B_GRAM, B_WMMA,          // MMA completion: Gram, WY
     B_HFULL0, B_HFULL1,      // front -> back hand-off slot 0 / 1 written
-    B_HEMPTY0, B_HEMPTY1,    // back -> front: Kp^T of hand-off slot 0 / 1 consumed
+    B_HEMPTY0, B_HEMPTY1,    // back -> front: the Kp^T buffer of hand-off slot 0 / 1 is free
     B_LFREE,                 // back -> front: L and beta consumed by the solve
     B_PZ0, B_PZ1,            // drains after a failure (one per MMA-issuing thread)
     // consumer
@@ -393,6 +394,12 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             Tot[qr * 128 + c1] = acc1;
         }
         failed = !wait_bar(&bars[B_LQK], (uint32_t)(jo & 1), x.flag, a, pc);
+        if (!failed && ptid == kIssImg && jo > 0) {
+            // the previous image is written (long since): the image buffer is free, and the
+            // back stage may publish that job
+            bulk_wait_done();
+            *x.stored = jo;
+        }
         // the ring slot holds chunk c - kRing until the consumer has copied it out
         if (!failed && ptid == 0 && c >= kRing) failed = !wait_geq(&pc.done[u], c - kRing + 1, x.flag, a, pc);
         // hand-off slot b (Kp^T) is free once the back stage has multiplied job jo - 2
@@ -516,13 +523,16 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             // written the image buffer is free and the back stage may publish the job
             bulk_store(slot_ptr(pc, u, c) + Slot::oQP, sm + Prod::oIMG, Slot::kFrontBytes);
             bulk_commit();
-            bulk_wait_done();
-            *x.stored = jo + 1;
         }
         it = nx;
         have = have_next;
     }
-    if (failed) *x.flag = 1;
+    if (failed) {
+        *x.flag = 1;
+    } else if (ptid == kIssImg && jo > 0) {
+        bulk_wait_done();
+        *x.stored = jo;
+    }
     return pend;
 }
 
@@ -594,54 +604,40 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         if (bar_or(2, 256, failed)) { failed = true; break; }
 
         // ---- solve: T = (I + L)^-1 -----------------------------------------------------------
-        // the 16x16 diagonal inverses by forward substitution, one column per lane
-        if (pw < 4 && lane < 16) {
-            const int b0 = 16 * pw, j = lane;
-            float v[16];
+        // Warps 0-3 invert (I + L) as a 2 x 2 block matrix of 32 x 32 blocks A (tokens 0-31)
+        // and B (32-63), each itself 2 x 2 in 16 x 16 blocks:
+        //   D_k = (I + L_kk)^-1                      forward substitution, one column per lane
+        //   T_10 = -D_1 L_10 D_0,  T_32 = -D_3 L_32 D_2
+        //   Y = L_BA T_AA,  T_BA = -T_BB Y
+        // (tf32 mma.sync, fp32 accumulation; Y is kept in T's unused upper triangle). Warps
+        // 4-7, the publisher's among them, meet them at the T_beta step.
+        float *Y = Tm + 32;  // Y[r][c] at Tm[r * LDF + 32 + c], r, c < 32
+        if (pw < 4) {
+            if (lane < 16) {
+                const int b0 = 16 * pw, j = lane;
+                float v[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float s = (r == j) ? 1.f : 0.f;
+                for (int r = 0; r < 16; ++r) {
+                    float s = (r == j) ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < r; ++m) s -= L[(b0 + r) * LDF + b0 + m] * v[m];
-                v[r] = s;
+                    for (int m = 0; m < r; ++m) s -= L[(b0 + r) * LDF + b0 + m] * v[m];
+                    v[r] = s;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tm[(b0 + r) * LDF + b0 + j] = v[r];
             }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tm[(b0 + r) * LDF + b0 + j] = v[r];
-        }
-        // Warps 0-6 go on with the off-diagonal blocks as soon as the diagonal ones are
-        // done; warp 7 (the publisher's) only needs the last diagonal block, from warp 3, and
-        // meets warp 3 on a barrier of their own after publishing.
-        if (pw == 3) asm volatile("bar.arrive 3, 64;" ::: "memory");
-        if (pw == 7) {
-            if (defer) failed = !publish(prev_u, prev_c, jo - 1);
-            bar_named(3, 64);
-        } else {
-            bar_named(4, 224);
-        }
-        // Off-diagonal blocks column by column: warp pw owns the 8 columns col0..col0+7 of T
-        // (column block j = pw / 2). T_jj = D_j, and for i > j
-        //   T_ij = -D_i sum_{k=j}^{i-1} L_ik T_kj
-        // (tf32 mma.sync, fp32 accumulation, one accumulator per k so that the products of a
-        // step run side by side). The warp then writes its columns of T_beta = T diag(beta)
-        // (lower triangle) in bf16. Each warp reads only L, the diagonal blocks and its own
-        // columns, so no barrier is needed inside.
-        {
-            const int j = pw >> 1, col0 = 16 * j + 8 * (pw & 1);
+            bar_named(5, 128);
             const int g8 = lane >> 2, t4 = lane & 3;
-            float *P = reinterpret_cast<float *>(sm + Prod::oPS) + pw * 128;  // 16x8 scratch
-            for (int i = j + 1; i < 4; ++i) {
-                float acc[3][4];
-#pragma unroll
-                for (int kk = 0; kk < 3; ++kk) acc[kk][0] = acc[kk][1] = acc[kk][2] = acc[kk][3] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < 3; ++kk)
-                    if (j + kk < i)
-                        mm16x8_tf32(acc[kk], L + (16 * i) * LDF + 16 * (j + kk), LDF, Tm + (16 * (j + kk)) * LDF + col0,
-                                    LDF, lane);
-                P[g8 * 8 + 2 * t4] = acc[0][0] + acc[1][0] + acc[2][0];
-                P[g8 * 8 + 2 * t4 + 1] = acc[0][1] + acc[1][1] + acc[2][1];
-                P[(g8 + 8) * 8 + 2 * t4] = acc[0][2] + acc[1][2] + acc[2][2];
-                P[(g8 + 8) * 8 + 2 * t4 + 1] = acc[0][3] + acc[1][3] + acc[2][3];
+            // T_10 (warps 0, 1) and T_32 (warps 2, 3), 8 columns each: P = L_ij D_j, T_ij = -D_i P
+            {
+                const int i = (pw < 2) ? 1 : 3, jb = i - 1, col0 = 16 * jb + 8 * (pw & 1);
+                float *P = reinterpret_cast<float *>(sm + Prod::oPS) + pw * 128;  // 16x8 scratch
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                mm16x8_tf32(acc, L + (16 * i) * LDF + 16 * jb, LDF, Tm + (16 * jb) * LDF + col0, LDF, lane);
+                P[g8 * 8 + 2 * t4] = acc[0];
+                P[g8 * 8 + 2 * t4 + 1] = acc[1];
+                P[(g8 + 8) * 8 + 2 * t4] = acc[2];
+                P[(g8 + 8) * 8 + 2 * t4 + 1] = acc[3];
                 __syncwarp();
                 float acc2[4] = {0.f, 0.f, 0.f, 0.f};
                 mm16x8_tf32(acc2, Tm + (16 * i) * LDF + 16 * i, LDF, P, 8, lane);
@@ -650,8 +646,64 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
                 Tij[g8 * LDF + 2 * t4 + 1] = -acc2[1];
                 Tij[(g8 + 8) * LDF + 2 * t4] = -acc2[2];
                 Tij[(g8 + 8) * LDF + 2 * t4 + 1] = -acc2[3];
-                __syncwarp();
             }
+            bar_named(5, 128);
+            // Y = L_BA T_AA: warp pw takes row block rb = pw >> 1 of Y and the 8-column tiles
+            // ct0 = 2 (pw & 1) and ct0 + 1; T_AA has D_0, T_10 in columns 0-15 and D_1 in 16-31
+            {
+                const int rb = pw >> 1, ct0 = 2 * (pw & 1);
+                const float *Lr = L + (32 + 16 * rb) * LDF;
+                float acc[2][4];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+                    const int col = 8 * (ct0 + q);
+                    if (col < 16) mm16x8_tf32(acc[q], Lr, LDF, Tm + col, LDF, lane);  // L_B0 [D_0; T_10]
+                    mm16x8_tf32(acc[q], Lr + 16, LDF, Tm + 16 * LDF + col, LDF, lane);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float *Yt = Y + (16 * rb) * LDF + 8 * (ct0 + q);
+                    Yt[g8 * LDF + 2 * t4] = acc[q][0];
+                    Yt[g8 * LDF + 2 * t4 + 1] = acc[q][1];
+                    Yt[(g8 + 8) * LDF + 2 * t4] = acc[q][2];
+                    Yt[(g8 + 8) * LDF + 2 * t4 + 1] = acc[q][3];
+                }
+            }
+            bar_named(5, 128);
+            // T_BA = -T_BB Y: row block rb of T_BA is -D_2 Y_0 (rb = 0) or -(T_32 Y_0 + D_3 Y_1)
+            {
+                const int rb = pw >> 1, ct0 = 2 * (pw & 1);
+                const float *Tb = Tm + (32 + 16 * rb) * LDF + 32;  // [T_32 | D_3] or [D_2 | 0]
+                float acc[2][4];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+                    const int col = 8 * (ct0 + q);
+                    if (rb == 0) {
+                        mm16x8_tf32(acc[q], Tb, LDF, Y + col, LDF, lane);
+                    } else {
+                        mm16x8_tf32(acc[q], Tb, LDF, Y + col, LDF, lane);
+                        mm16x8_tf32(acc[q], Tb + 16, LDF, Y + 16 * LDF + col, LDF, lane);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float *Tt = Tm + (32 + 16 * rb) * LDF + 8 * (ct0 + q);
+                    Tt[g8 * LDF + 2 * t4] = -acc[q][0];
+                    Tt[g8 * LDF + 2 * t4 + 1] = -acc[q][1];
+                    Tt[(g8 + 8) * LDF + 2 * t4] = -acc[q][2];
+                    Tt[(g8 + 8) * LDF + 2 * t4 + 1] = -acc[q][3];
+                }
+            }
+        } else if (pw == 7 && defer) {
+            failed = !publish(prev_u, prev_c, jo - 1);
+        }
+        bar_named(2, 256);
+        // T_beta = T diag(beta), lower triangle, bf16 [tok][tok'] (K-major B): warp pw writes
+        // the 8 columns col0 .. col0 + 7, col0 = 8 pw
+        {
+            const int col0 = 8 * pw, jb = pw >> 1;
             const float4 b0 = *reinterpret_cast<const float4 *>(Bs + col0);
             const float4 b1 = *reinterpret_cast<const float4 *>(Bs + col0 + 4);
             const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
@@ -659,7 +711,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
             for (int hh = 0; hh < 2; ++hh) {
                 const int r = lane + 32 * hh;
                 float v[8];
-                if (r < 16 * j) {
+                if (r < 16 * jb) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v[e] = 0.f;
                 } else {
@@ -701,12 +753,14 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         }
         failed = !wait_bar(&bars[B_WMMA], (uint32_t)(jo & 1), x.flag, a, pc);
         if (bar_or(2, 256, failed)) { failed = true; break; }
-        if (ptid == 0) mbar_arrive(&bars[B_HEMPTY0 + b]);  // Kp^T of slot b is consumed
+        // V is consumed: the next job's tile is requested before this job's stores, which
+        // would otherwise hold it up in the SM's bulk-copy queue
+        if (have_next) stage_v(nx, jo + 1);
         fence_after_sync();
         {
             // row d of W^T and of U^T; each warp half takes 32 of the 64 tokens. W^T goes to
-            // the (now free) T buffer as the swizzled [d][tok] image, U^T to the V buffer as
-            // bf16 token pairs.
+            // the (now free) T buffer as the swizzled [d][tok] image, U^T to the job's Kp^T
+            // buffer (consumed by the W MMA) as bf16 token pairs.
             const int d = 32 * (warp & 3) + lane;
             float v[32];
             tmem_ld32(x.tmem + lane_off + tW + half, v);
@@ -718,7 +772,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
                 *reinterpret_cast<uint4 *>(sm + Prod::oT + sw128(d, (int)(half >> 3) + c8)) = pack8(y);
             }
             tmem_ld32(x.tmem + lane_off + tU + half, v);
-            uint32_t *U2 = reinterpret_cast<uint32_t *>(sm + Prod::oRV);
+            uint32_t *U2 = reinterpret_cast<uint32_t *>(sm + oKP);
 #pragma unroll
             for (int e = 0; e < 16; ++e) U2[((int)(half >> 1) + e) * 128 + d] = pack_bf16(v[2 * e], v[2 * e + 1]);
         }
@@ -727,12 +781,12 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         bar_named(2, 256);
         if (ptid == kPublisher) {
             bulk_store(slot + Slot::oWT, sm + Prod::oT, 16384);
-            bulk_store(slot + Slot::oU, sm + Prod::oRV, 16384);
+            bulk_store(slot + Slot::oU, sm + oKP, 16384);
             bulk_commit();
             bulk_wait_read();
+            mbar_arrive(&bars[B_HEMPTY0 + b]);  // the Kp^T buffer of slot b is free again
         }
-        bar_named(2, 256);  // the T and V buffers are free again
-        if (have_next) stage_v(nx, jo + 1);
+        bar_named(2, 256);  // the T buffer is free again
         prev_u = u;
         prev_c = c;
         it = nx;
