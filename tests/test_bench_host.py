@@ -1,0 +1,83 @@
+"""Host logic of bench.py without a GPU: the multi-rank path (world_size 2 on gloo, CPU),
+the reference arm's rank behaviour, and the workload accounting."""
+
+from __future__ import annotations
+
+import argparse
+import contextlib
+import io
+import json
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    w, r, local, pg = bench.dist_setup()
+    try:
+        assert (w, r, local) == (world, rank, rank) and pg is not None
+        assert pg.get_backend() == "gloo"
+        bench.barrier(pg)
+        # the slowest rank's time is the job's time
+        mx = bench.max_over_ranks(pg, 1.0 + rank * 2.5)
+        args = argparse.Namespace(workload="kda_b1_t256_h1_d64_f32", steps=1, warmup=1, gpus=world,
+                                  impl="reference")
+        buf = io.StringIO()
+        with contextlib.redirect_stdout(buf):
+            bench.run_reference(args, w, r, pg)
+        bench.barrier(pg)
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"max": mx, "out": buf.getvalue()}, f)
+    finally:
+        pg.destroy_process_group()
+
+
+def test_two_ranks_on_gloo(tmp_path):
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+
+    world, port = 2, _free_port()
+    mp.start_processes(_rank_main, args=(world, port, str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    assert all(r["max"] == 3.5 for r in res)
+    # rank 0 alone runs and prints the reference line; the other rank prints nothing
+    assert res[1]["out"] == ""
+    line = json.loads(res[0]["out"].strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    del torch
+
+
+def test_single_rank_needs_no_process_group(monkeypatch):
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_setup() == (1, 0, 0, None)
+    assert bench.max_over_ranks(None, 2.0) == 2.0
+
+
+def test_workload_accounting_and_dispatch():
+    from types import SimpleNamespace
+
+    from inputs import workload_inputs
+
+    # the benchmark workload's shape (its arrays are not needed for the accounting)
+    x = SimpleNamespace(dtype="bf16", T_total=16384, N=2, H_k=32, H_v=32, d_k=128, d_v=128,
+                        gate="channel", h0=True)
+    # 1,540 B per (token, head) at d = 128 bf16, plus h0 and ht: 815.8 MB per launch
+    assert bench.algorithmic_bytes(x) == 16384 * 32 * 1540 + 2 * 32 * 2 * 4 * 128 * 128
+    assert bench.forward_kernel(x, 152) == "kda_fwd_pc_kernel"  # 64 units on 152 SMs
+    assert bench.forward_kernel(x, 120) == "kda_fwd_tc_kernel"  # more than half the SMs
+    y = workload_inputs("kda_b1_t256_h1_d64_f32")
+    assert bench.forward_kernel(y, 152) == "kda_fwd_f32_kernel"
