@@ -41,7 +41,7 @@ using namespace tc5;
 using namespace tcu;
 
 constexpr int kMaxUnits = 76;       // units served by one launch (at most half the SMs)
-constexpr int kRing = 8;            // ring slots per unit
+constexpr int kRing = 8;            // ring slots per unit (a launch argument)
 constexpr int kThreads = 512;
 
 // Slot image (global ring and consumer shared memory). [d][tok] tiles hold one row per
@@ -133,11 +133,12 @@ struct UnitInfo {
 
 // Ring and flags in global memory; ready/done/abort start at zero for every launch.
 struct PcArgs {
-    unsigned char *ring;   // [U][kRing] slots of Slot::kStride bytes
-    int *ready;            // [U][kRing]: c + 1 once chunk c is in slot c % kRing
+    unsigned char *ring;   // [U][R] slots of Slot::kStride bytes
+    int *ready;            // [U][R]: c + 1 once chunk c is in slot c % R
     int *done;             // [U]: chunks whose slot image has been copied out
     int *abort;            // set by any CTA that gave up
     int U, P;              // units (= consumer CTAs), producer CTAs
+    int R;                 // ring slots per unit
 };
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -267,7 +268,7 @@ __device__ __forceinline__ bool next_job(JobIt &it, const Ctx &x, const PcArgs &
 }
 
 __device__ __forceinline__ unsigned char *slot_ptr(const PcArgs &pc, int u, int c) {
-    return pc.ring + ((int64_t)u * kRing + c % kRing) * Slot::kStride;
+    return pc.ring + ((int64_t)u * pc.R + c % pc.R) * Slot::kStride;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -393,6 +394,9 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             Tot[qr * 128 + c0] = acc0;
             Tot[qr * 128 + c1] = acc1;
         }
+        // G (and the per-head gates) are consumed: request the next job's right away
+        bar_named(1, 256);
+        if (have_next) stage_g(nx, jo + 1);
         failed = !wait_bar(&bars[B_LQK], (uint32_t)(jo & 1), x.flag, a, pc);
         if (!failed && ptid == kIssImg && jo > 0) {
             // the previous image is written (long since): the image buffer is free, and the
@@ -400,14 +404,13 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             bulk_wait_done();
             *x.stored = jo;
         }
-        // the ring slot holds chunk c - kRing until the consumer has copied it out
-        if (!failed && ptid == 0 && c >= kRing) failed = !wait_geq(&pc.done[u], c - kRing + 1, x.flag, a, pc);
+        // the ring slot holds chunk c - R until the consumer has copied it out
+        if (!failed && ptid == 0 && c >= pc.R) failed = !wait_geq(&pc.done[u], c - pc.R + 1, x.flag, a, pc);
         // hand-off slot b (Kp^T) is free once the back stage has multiplied job jo - 2
         if (!failed && jo >= 2)
             failed = !wait_bar(&bars[B_HEMPTY0 + b], (uint32_t)(((jo >> 1) - 1) & 1), x.flag, a, pc);
         if (bar_or(1, 256, failed)) { failed = true; break; }
         pend &= ~1u;
-        if (have_next) stage_g(nx, jo + 1);  // G and the per-head gates are consumed
         if (nz > 0) {
             for (int i = ptid; i < nz * 16; i += 256) {
                 const int r = nvalid + (i >> 4), c16 = i & 15;
@@ -571,7 +574,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         bulk_wait_done();
         if (!wait_count(x.stored, pjo + 1, x.flag, a, pc)) return false;
         fence_proxy_async_global();
-        st_release(&pc.ready[pu * kRing + pcn % kRing], pcn + 1);
+        st_release(&pc.ready[pu * pc.R + pcn % pc.R], pcn + 1);
         return true;
     };
 
@@ -814,7 +817,7 @@ __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &p
         if (lt == 0 && !failed) {
             // buffer b held chunk c - 2 until the serial step released it
             if (c >= 2) failed = !wait_bar(&bars[B_EMPTY0 + b], (uint32_t)(((c >> 1) - 1) & 1), x.flag, a, pc);
-            if (!failed) failed = !wait_geq(&pc.ready[u * kRing + c % kRing], c + 1, x.flag, a, pc);
+            if (!failed) failed = !wait_geq(&pc.ready[u * pc.R + c % pc.R], c + 1, x.flag, a, pc);
             if (!failed) mbar_arrive_expect_tx(&bars[B_FULL0 + b], Slot::kBytes);
         }
         if (bar_or(2, 128, failed)) {
@@ -1189,6 +1192,7 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     pc.abort = pc.done + U;
     pc.U = (int)U;
     pc.P = sms - (int)U;
+    pc.R = kRing;
     e = cudaMemsetAsync(pc.ready, 0, flag_bytes, stream);
     if (e == cudaSuccess) {
         void *args[] = {const_cast<FwdArgs *>(&a), &maps, &pc};
