@@ -8,6 +8,7 @@ from .kda import (  # noqa: F401
     kda_chunk_fwd,
     kda_chunk_fwd_ex,
     kda_chunk_fwd_f32,
+    kda_chunk_fwd_noalloc,
     kda_fwd_params,
     kda_get_device_error,
     lib,

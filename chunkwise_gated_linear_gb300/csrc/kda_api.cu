@@ -12,6 +12,8 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched);
+cudaError_t launch_fwd_pc_static(const FwdArgs &a, cudaStream_t stream);
+int pc_static_max_units();
 }  // namespace kda
 
 namespace {
@@ -44,7 +46,9 @@ cudaError_t device_error_ptr(unsigned int **out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int run(const kda_fwd_params &p, cudaStream_t stream) {
+// Checks the arguments and resolves them into `a` (and its device error word); returns a
+// status other than KDA_OK, with nothing launched, when the call is rejected.
+int prepare(const kda_fwd_params &p, kda::FwdArgs &a) {
     // With no tokens there is nothing to read or write but the states, so the token
     // tensors may be empty (NULL).
     if (p.T != 0 && (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr ||
@@ -64,7 +68,7 @@ int run(const kda_fwd_params &p, cudaStream_t stream) {
     const int64_t total_tokens = p.cu_seqlens ? (int64_t)p.T : N * p.T;
     if (total_tokens > INT32_MAX || N > 65535 || p.H_v > 65535) return KDA_ERR_UNSUPPORTED;
 
-    kda::FwdArgs a{};
+    a = kda::FwdArgs{};
     a.q = p.q;
     a.k = p.k;
     a.v = p.v;
@@ -83,7 +87,13 @@ int run(const kda_fwd_params &p, cudaStream_t stream) {
     a.group = p.H_v / p.H_k;
     a.scale = p.scale;
     a.gate_per_head = p.gate_mode == KDA_GATE_PER_HEAD ? 1 : 0;
+    return KDA_OK;
+}
 
+int run(const kda_fwd_params &p, cudaStream_t stream) {
+    kda::FwdArgs a;
+    const int st = prepare(p, a);
+    if (st != KDA_OK) return st;
     cudaError_t e = device_error_ptr(&a.err);
     if (e == cudaSuccess) {
         if (p.dtype == KDA_DTYPE_F32) {
@@ -122,6 +132,30 @@ int kda_chunk_fwd_f32(const float *q, const float *k, const float *v, const floa
     kda_fwd_params p{q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
                      KDA_DTYPE_F32, KDA_GATE_PER_CHANNEL, 0};
     return run(p, stream);
+}
+
+int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                          const float *h0, void *o, float *ht, int B, int T, int H_k, int H_v, int d_k,
+                          int d_v, int C, float scale, const int32_t *cu_seqlens, cudaStream_t stream) {
+    kda_fwd_params p{q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
+                     KDA_DTYPE_BF16, KDA_GATE_PER_CHANNEL, 0};
+    kda::FwdArgs a;
+    const int st = prepare(p, a);
+    if (st != KDA_OK) return st;
+    // only the persistent kernel's shapes, within the static scratch (checked on the host
+    // before any CUDA call)
+    if (d_k != 128 || d_v != 128 || (int64_t)a.N * a.H_v > kda::pc_static_max_units()) return KDA_ERR_UNSUPPORTED;
+    cudaError_t e = device_error_ptr(&a.err);
+    if (e == cudaSuccess) e = kda::launch_fwd_pc_static(a, stream);
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        return KDA_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) {
+        t_last_cuda_error = e;
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
 }
 
 int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) {

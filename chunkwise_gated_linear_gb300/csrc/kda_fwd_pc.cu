@@ -1204,6 +1204,73 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     return e != cudaSuccess ? e : ef;
 }
 
+// ---- the variant without allocation: scratch in a file-scope device array ----------------
+// Room for kStaticUnits units with kRing slots each, and their flags. Calls that use it must
+// not overlap (on any stream or thread): they share this one array.
+constexpr int kStaticUnits = 16;
+constexpr size_t kStaticRingBytes = (size_t)kStaticUnits * kRing * Slot::kStride;      // 9,568,256 B
+constexpr size_t kStaticFlagBytes = 1024;  // >= (kStaticUnits * (kRing + 1) + 1) ints
+static_assert((kStaticUnits * (kRing + 1) + 1) * sizeof(int) <= kStaticFlagBytes, "flag room");
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticRingBytes + kStaticFlagBytes];
+
+std::mutex g_static_mu;
+unsigned char *g_static_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device, looked up once per device.
+cudaError_t static_scratch(int dev, unsigned char **out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_static_ptr[dev] = static_cast<unsigned char *>(p);
+    }
+    *out = g_static_ptr[dev];
+    return cudaSuccess;
+}
+
+template <bool GATE_HEAD>
+cudaError_t launch_pc_static(const FwdArgs &a, cudaStream_t stream) {
+    const int64_t U = (int64_t)a.N * a.H_v;
+    if (U < 1 || U > kStaticUnits) return cudaErrorNotSupported;
+    int dev = 0, sms = 0, coop = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (e != cudaSuccess) return e;
+    if (!coop || 2 * U > sms) return cudaErrorNotSupported;
+    auto kern = kda_fwd_pc_kernel<GATE_HEAD>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Common::kBytes);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Common::kBytes);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+
+    TcMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode_tile_maps(&maps, a, GATE_HEAD)) return cudaErrorInvalidValue;
+
+    unsigned char *base = nullptr;
+    e = static_scratch(dev, &base);
+    if (e != cudaSuccess) return e;
+    PcArgs pc;
+    pc.ring = base;
+    pc.ready = reinterpret_cast<int *>(base + kStaticRingBytes);
+    pc.done = pc.ready + (size_t)U * kRing;
+    pc.abort = pc.done + U;
+    pc.U = (int)U;
+    pc.P = sms - (int)U;
+    pc.R = kRing;
+    // the flags start at zero for every call; the slots need no clearing
+    e = cudaMemsetAsync(pc.ready, 0, kStaticFlagBytes, stream);
+    if (e != cudaSuccess) return e;
+    void *args[] = {const_cast<FwdArgs *>(&a), &maps, &pc};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(sms), dim3(kThreads), args,
+                                       Common::kBytes, stream);
+}
+
 }  // namespace
 
 // The persistent kernel when the call has at most half as many units as the device has
@@ -1211,5 +1278,14 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
 cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     return a.gate_per_head ? launch_pc<true>(a, stream, launched) : launch_pc<false>(a, stream, launched);
 }
+
+// The same kernel with its scratch in g_static_scratch (nothing allocated). Returns
+// cudaErrorNotSupported, with nothing launched, when the call has more than kStaticUnits
+// units, more units than half the SMs, or the device cannot launch it cooperatively.
+cudaError_t launch_fwd_pc_static(const FwdArgs &a, cudaStream_t stream) {
+    return a.gate_per_head ? launch_pc_static<true>(a, stream) : launch_pc_static<false>(a, stream);
+}
+
+int pc_static_max_units() { return kStaticUnits; }
 
 }  // namespace kda

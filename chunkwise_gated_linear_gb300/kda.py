@@ -29,7 +29,7 @@ KDA_DEVICE_ERR_SEQLENS = 1
 KDA_DEVICE_ERR_TIMEOUT = 2
 
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_ex", "kda_status_string",
-            "kda_get_device_error")
+            "kda_get_device_error", "kda_chunk_fwd_noalloc")
 
 
 class KdaError(RuntimeError):
@@ -67,7 +67,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(path)
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         sig = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]
-        for name in ("kda_chunk_fwd", "kda_chunk_fwd_f32"):
+        for name in ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_noalloc"):
             fn = getattr(L, name)
             fn.argtypes = sig
             fn.restype = I
@@ -97,6 +97,12 @@ def kda_chunk_fwd_f32(q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, 
                       stream) -> int:
     return lib().kda_chunk_fwd_f32(q, k, v, g, beta, h0 or None, o, ht or None, B, T, H_k, H_v,
                                    d_k, d_v, C, scale, cu_seqlens or None, stream or None)
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale,
+                          cu_seqlens, stream) -> int:
+    return lib().kda_chunk_fwd_noalloc(q, k, v, g, beta, h0 or None, o, ht or None, B, T, H_k, H_v,
+                                       d_k, d_v, C, scale, cu_seqlens or None, stream or None)
 
 
 def kda_chunk_fwd_ex(params: kda_fwd_params, stream) -> int:

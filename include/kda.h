@@ -138,6 +138,29 @@ typedef struct kda_fwd_params {
  */
 int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream);
 
+/*
+ * kda_chunk_fwd_noalloc — the arguments and result of kda_chunk_fwd, computed by the
+ * persistent kernel with its scratch (the ring of chunk slots and its flags) in one
+ * fixed array of device memory inside the library: 9,568,256 + 1,024 bytes, room for 16
+ * (sequence, value head) units. The pages have no counterpart: it exists for callers
+ * that must not allocate (nothing is allocated, on the device or the host).
+ *
+ * Supported: bf16, d_k = d_v = 128, C = 64, at most 16 units (B * H_v, or N * H_v with
+ * cu_seqlens) and at most half as many units as the device has SMs; anything else returns
+ * KDA_ERR_UNSUPPORTED with nothing launched (the unit and size checks are made on the host
+ * before any CUDA call). Each call first zeroes the flag words of the array with
+ * cudaMemsetAsync on `stream`; the slots need no clearing.
+ *
+ * The array is shared by every call of this entry point on a device: calls that overlap
+ * in time (on any stream, from any thread) race on it and give wrong results. The caller
+ * must order them (same stream, or events). Other entry points do not use the array.
+ * Errors and the device error word are as for kda_chunk_fwd.
+ */
+int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *h0, void *o, float *ht, int B,
+                          int T, int H_k, int H_v, int d_k, int d_v, int C, float scale,
+                          const int32_t *cu_seqlens, cudaStream_t stream);
+
 /* A static, human-readable description of a status (and of the last CUDA error for
  * KDA_ERR_CUDA on this thread). */
 const char *kda_status_string(int status);

@@ -84,3 +84,16 @@ def test_ex_rejects_unknown_modes_and_flags():
     p.gate_mode = 5
     assert kda.kda_chunk_fwd_ex(p, 0) == kda.KDA_ERR_UNSUPPORTED
     assert kda.lib().kda_chunk_fwd_ex(None, None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_what_its_scratch_cannot_hold():
+    # checked on the host before any CUDA call: more than 16 units, or d != 128
+    args = dict(q=A, k=A, v=A, g=A, beta=A, h0=0, o=A, ht=0, B=1, T=64, H_k=1, H_v=17, d_k=128,
+                d_v=128, C=64, scale=1.0, cu_seqlens=0, stream=0)
+    assert kda.kda_chunk_fwd_noalloc(**args) == kda.KDA_ERR_UNSUPPORTED
+    args.update(B=2, H_v=16)  # 32 units
+    assert kda.kda_chunk_fwd_noalloc(**args) == kda.KDA_ERR_UNSUPPORTED
+    args.update(B=1, H_v=4, d_k=64)
+    assert kda.kda_chunk_fwd_noalloc(**args) == kda.KDA_ERR_UNSUPPORTED
+    args.update(d_k=128, q=0)
+    assert kda.kda_chunk_fwd_noalloc(**args) == kda.KDA_ERR_INVALID_ARG
