@@ -53,12 +53,12 @@ def kernel_source_hash() -> str:
 
 
 def algorithmic_bytes(x) -> int:
-    """HBM bytes the method must move: q, k once per key head; v, o, g, beta per value
-    head; h0 and ht once per (sequence, value head)."""
+    """HBM bytes the method must move: q, k once per key head; v, o, g, beta (if any) per
+    value head; h0 and ht once per (sequence, value head)."""
     e = 2 if x.dtype == "bf16" else 4
     T = x.T_total
     gate = 4 * x.d_k if x.gate == "channel" else 4
-    per_tok = x.H_k * 2 * x.d_k * e + x.H_v * (2 * x.d_v * e + gate + 4)
+    per_tok = x.H_k * 2 * x.d_k * e + x.H_v * (2 * x.d_v * e + gate + (4 if x.beta is not None else 0))
     state = x.N * x.H_v * 4 * x.d_k * x.d_v * ((x.h0 is not None) + 1)
     return T * per_tok + state
 
@@ -253,9 +253,11 @@ def run_ours(args, world, rank, local, pg):
     H = {
         "q": host(x.q, dt_io, (B, T, x.H_k, x.d_k)), "k": host(x.k, dt_io, (B, T, x.H_k, x.d_k)),
         "v": host(x.v, dt_io, (B, T, x.H_v, x.d_v)), "g": host(x.g, torch.float32, (B, T, x.H_v, x.d_k)),
-        "beta": host(x.beta, torch.float32, (B, T, x.H_v)),
         "h0": host(x.h0, torch.float32, (B, x.H_v, x.d_k, x.d_v)),
     }
+    if x.beta is not None:  # no beta: the decay-only recurrence
+        H["beta"] = host(x.beta, torch.float32, (B, T, x.H_v))
+    inputs = [key for key in ("q", "k", "v", "g", "beta", "h0") if key in H]
     D = {key: t.to(dev) for key, t in H.items()}
     D["o"] = torch.empty((B, T, x.H_v, x.d_v), dtype=dt_io, device=dev)
     D["ht"] = torch.empty((B, x.H_v, x.d_k, x.d_v), dtype=torch.float32, device=dev)
@@ -267,14 +269,15 @@ def run_ours(args, world, rank, local, pg):
 
     def call():
         st = entry(D["q"].data_ptr(), D["k"].data_ptr(), D["v"].data_ptr(), D["g"].data_ptr(),
-                   D["beta"].data_ptr(), D["h0"].data_ptr(), D["o"].data_ptr(), D["ht"].data_ptr(),
+                   D["beta"].data_ptr() if "beta" in D else None, D["h0"].data_ptr(), D["o"].data_ptr(),
+                   D["ht"].data_ptr(),
                    B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale, None, sh)
         if st != 0:
             raise RuntimeError(kda.status_string(st))
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            for key in ("q", "k", "v", "g", "beta", "h0"):
+            for key in inputs:
                 D[key].copy_(H[key], non_blocking=True)
             call()
             H["o"].copy_(D["o"], non_blocking=True)
@@ -314,7 +317,7 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize(dev)
     barrier(pg)
     ms_e2e = max_over_ranks(pg, ev2.elapsed_time(ev3) / args.steps)
-    h2d = sum(H[key].numel() * H[key].element_size() for key in ("q", "k", "v", "g", "beta", "h0"))
+    h2d = sum(H[key].numel() * H[key].element_size() for key in inputs)
     d2h = H["o"].numel() * H["o"].element_size() + H["ht"].numel() * H["ht"].element_size()
 
     peak, peak_kind = load_peaks()

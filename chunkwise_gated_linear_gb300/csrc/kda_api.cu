@@ -51,8 +51,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int prepare(const kda_fwd_params &p, kda::FwdArgs &a) {
     // With no tokens there is nothing to read or write but the states, so the token
     // tensors may be empty (NULL).
-    if (p.T != 0 && (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr ||
-                     p.beta == nullptr || p.o == nullptr))
+    // (beta may be NULL: the decay-only recurrence)
+    if (p.T != 0 && (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr || p.o == nullptr))
         return KDA_ERR_INVALID_ARG;
     if (p.B < 1 || p.T < 0 || p.H_k < 1 || p.H_v < 1 || p.H_v % p.H_k != 0) return KDA_ERR_INVALID_ARG;
     if ((p.flags & ~KDA_FLAG_ONE_CTA_PER_UNIT) != 0) return KDA_ERR_INVALID_ARG;
@@ -87,6 +87,7 @@ int prepare(const kda_fwd_params &p, kda::FwdArgs &a) {
     a.group = p.H_v / p.H_k;
     a.scale = p.scale;
     a.gate_per_head = p.gate_mode == KDA_GATE_PER_HEAD ? 1 : 0;
+    a.decay_only = p.beta == nullptr ? 1 : 0;
     return KDA_OK;
 }
 

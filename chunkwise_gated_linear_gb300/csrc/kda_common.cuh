@@ -27,6 +27,7 @@ struct FwdArgs {
     int group;                  // H_v / H_k
     float scale;
     int gate_per_head;
+    int decay_only;             // beta == nullptr: S <- Diag(a_t) S + k_t v_t^T (no erase)
     unsigned int *err;          // device error word of the current device (KDA_DEVICE_ERR_*)
 };
 

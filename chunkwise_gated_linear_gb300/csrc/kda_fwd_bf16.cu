@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_bf16_kernel(const FwdArgs a) {
         cp_async_commit();
         if (tid < 64) {
             const bool ok = tid < nvalid;
-            Bs[tid] = ok ? a.beta[(bos + row0 + tid) * a.H_v + h] : 0.f;
+            Bs[tid] = ok ? (a.decay_only ? 1.f : a.beta[(bos + row0 + tid) * a.H_v + h]) : 0.f;
         } else if (GATE_HEAD) {
             const int r = tid - 64;
             const bool ok = r < nvalid;
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_bf16_kernel(const FwdArgs a) {
                     const float ep = exp2f(acc), em = exp2f(-acc);
                     const float kv = __bfloat162float(Kraw[r * LDK + ch]);
                     const float qv = __bfloat162float(Qraw[r * LDK + ch]);
-                    Kp[r * LDK + ch] = __float2bfloat16_rn(kv * ep);
+                    Kp[r * LDK + ch] = __float2bfloat16_rn(a.decay_only ? 0.f : kv * ep);
                     Km[r * LDK + ch] = __float2bfloat16_rn(kv * em);
                     Qp[r * LDK + ch] = __float2bfloat16_rn(a.scale * qv * ep);
                 }
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_bf16_kernel(const FwdArgs a) {
                 const int r = i / DK, ch = i % DK;
                 const float kv = __bfloat162float(Kraw[r * LDK + ch]);
                 const float qv = __bfloat162float(Qraw[r * LDK + ch]);
-                Kp[r * LDK + ch] = __float2bfloat16_rn(kv * ep[r]);
+                Kp[r * LDK + ch] = __float2bfloat16_rn(a.decay_only ? 0.f : kv * ep[r]);
                 Km[r * LDK + ch] = __float2bfloat16_rn(kv * em[r]);
                 Qp[r * LDK + ch] = __float2bfloat16_rn(a.scale * qv * ep[r]);
                 Kbar[r * LDK + ch] = __float2bfloat16_rn(kv * eb[r]);

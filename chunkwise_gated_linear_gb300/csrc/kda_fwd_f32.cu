@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
         }
         if (tid < 64) {
             const bool ok = tid < nvalid;
-            Bs[tid] = ok ? a.beta[(bos + row0 + tid) * a.H_v + h] : 0.f;
+            Bs[tid] = ok ? (a.decay_only ? 1.f : a.beta[(bos + row0 + tid) * a.H_v + h]) : 0.f;
             if (GATE_HEAD) Gh[tid] = ok ? a.g[(bos + row0 + tid) * sg + h] : 0.f;
         }
         __syncthreads();
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
                 const float ep = exp2f(acc), em = exp2f(-acc);
                 const float kv = K[r * DK + c];
                 Km[r * DK + c] = kv * em;
-                K[r * DK + c] = kv * ep;
+                K[r * DK + c] = a.decay_only ? 0.f : kv * ep;
                 Q[r * DK + c] = a.scale * Q[r * DK + c] * ep;
             }
             const float eg = exp2f(acc);

@@ -328,8 +328,12 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         float *Gh = reinterpret_cast<float *>(sm + ((jo & 1) ? Prod::oGh1 : Prod::oGh0));
         if (ptid < 64) {
             const bool ok = ptid < nvalid;
-            const int64_t ob = ok ? (bos + row0 + ptid) * a.H_v + h : 0;
-            cp_async_4(Bf + ptid, a.beta + ob, ok ? 4 : 0);
+            if (a.decay_only) {
+                Bf[ptid] = ok ? 1.f : 0.f;
+            } else {
+                const int64_t ob = ok ? (bos + row0 + ptid) * a.H_v + h : 0;
+                cp_async_4(Bf + ptid, a.beta + ob, ok ? 4 : 0);
+            }
         } else if (GATE_HEAD && ptid < 128) {
             const int r = ptid - 64;
             const bool ok = r < nvalid;
@@ -451,7 +455,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
                         const float ep = ex2(gm), em = ex2(-gm);
                         const float kv = __bfloat162float(RK[r * 128 + cc]);
                         const float qv = __bfloat162float(RQ[r * 128 + cc]);
-                        kp[e] = kv * ep;
+                        kp[e] = a.decay_only ? 0.f : kv * ep;
                         km[e] = kv * em;
                         qp[e] = a.scale * qv * ep;
                         kb[e] = km[e] * eg;

@@ -126,7 +126,8 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
 
     q, k [B, T, H_k, d_k] and v [B, T, H_v, d_v], all bf16 or all fp32; g fp32
     [B, T, H_v, d_k] (per-channel gate) or [B, T, H_v] (one gate per head); beta fp32
-    [B, T, H_v]; h0 fp32 [N, H_v, d_k, d_v] or None. With ``cu_seqlens`` (int32 [N + 1]
+    [B, T, H_v], or None for the decay-only recurrence S <- Diag(a_t) S + k_t v_t^T; h0 fp32
+    [N, H_v, d_k, d_v] or None. With ``cu_seqlens`` (int32 [N + 1]
     on the device) B must be 1 and the N sequences are packed along T. ``o`` and ``ht``
     may be given to write into existing buffers. ``ht`` is None in the result when
     ``output_final_state`` is False. ``one_cta_per_unit`` sets KDA_FLAG_ONE_CTA_PER_UNIT
@@ -148,7 +149,7 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
         raise TypeError("q, k, v must be bf16 or fp32")
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype")
-    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+    if g.dtype != torch.float32 or (beta is not None and beta.dtype != torch.float32):
         raise TypeError("g and beta must be fp32")
     if g.shape == (B, T, H_v, d_k):
         gate = KDA_GATE_PER_CHANNEL
@@ -156,8 +157,8 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
         gate = KDA_GATE_PER_HEAD
     else:
         raise ValueError("g must be [B, T, H_v, d_k] or [B, T, H_v]")
-    if beta.shape != (B, T, H_v):
-        raise ValueError("beta must be [B, T, H_v]")
+    if beta is not None and beta.shape != (B, T, H_v):
+        raise ValueError("beta must be [B, T, H_v] (or None: the decay-only recurrence)")
     for t in (q, k, v, g, beta, h0, cu_seqlens):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("every tensor must be a contiguous CUDA tensor")
@@ -183,7 +184,7 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
         scale = d_k ** -0.5
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    p = kda_fwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0) or None, _ptr(o),
+    p = kda_fwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta) or None, _ptr(h0) or None, _ptr(o),
                        _ptr(ht) or None, nb, nt, H_k, H_v, d_k, d_v, chunk_size, float(scale),
                        _ptr(cu_seqlens) or None, dtype, gate,
                        KDA_FLAG_ONE_CTA_PER_UNIT if one_cta_per_unit else 0)

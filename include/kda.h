@@ -40,7 +40,12 @@
  *   if cu_seqlens == NULL the batch holds B sequences of T tokens each (N = B).
  *
  * NULL conventions: h0 == NULL means a zero initial state; ht == NULL means the final
- *   state is not written. q, k, v, g, beta and o are required unless T == 0.
+ *   state is not written; beta == NULL selects the decay-only recurrence (gated linear
+ *   attention: no erase, unit write; "07 · linear 路线（二）：衰减机制的演进", §1, and the
+ *   KDA page, §3.4):
+ *       S <- Diag(exp(g_t)) S + k_t v_t^T,   o_t = scale * S^T q_t
+ *   (GLA with a per-channel gate; RetNet, Lightning or Mamba-2 SSD with one gate per
+ *   head). q, k, v, g and o are required unless T == 0.
  *
  * Sizes supported: d_k, d_v in {64, 128}; C == 64; B >= 1; T >= 0; H_k >= 1; H_v >= 1.
  *   T == 0 (or empty sequences) is valid: no o rows, ht = h0 (or 0).

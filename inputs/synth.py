@@ -48,6 +48,7 @@ class Workload:
     varlen: bool = False  # packed with cu_seqlens (physical batch 1)
     len_range: tuple | None = None  # (lo, hi) for drawn lengths; overrides lengths
     n_seqs: int | None = None
+    beta: bool = True  # False: no beta (the decay-only recurrence)
 
     @property
     def T(self) -> int:
@@ -71,8 +72,11 @@ WORKLOADS = {
 
 WORKLOAD_SEEDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
 
-# Smaller cases of the same kernels for profiler captures (inputs still larger than L2).
+# Smaller cases of the same kernels for profiler captures (inputs still larger than L2),
+# and the decay-only variant of the benchmark shape.
 PROFILE_WORKLOADS = {
+    "kda_decayonly_b2_t8192_h32_d128_bf16": Workload(
+        "kda_decayonly_b2_t8192_h32_d128_bf16", (8192,) * 2, 32, 32, 128, 128, h0=True, beta=False),
     "kda_b1_t8192_h32_d128_bf16": Workload(
         "kda_b1_t8192_h32_d128_bf16", (8192,), 32, 32, 128, 128, h0=True),
 }
@@ -199,7 +203,7 @@ def workload_inputs(name: str, seed: int | None = None) -> Inputs:
     w = WORKLOADS[name] if name in WORKLOADS else PROFILE_WORKLOADS[name]
     s = WORKLOAD_SEEDS.get(name, 99) if seed is None else seed
     x = make_inputs(w.lengths, w.H_k, w.H_v, w.d_k, w.d_v, dtype=w.dtype, gate=w.gate,
-                    a_lo=w.a_lo, h0=w.h0, varlen=w.varlen, seed=s,
+                    a_lo=w.a_lo, h0=w.h0, beta=w.beta, varlen=w.varlen, seed=s,
                     len_range=w.len_range, n_seqs=w.n_seqs)
     x.meta["workload"] = name
     return x

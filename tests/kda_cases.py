@@ -28,7 +28,7 @@ def to_device(x: Inputs, device="cuda"):
 
     d = {
         "q": tens(x.q, dt), "k": tens(x.k, dt), "v": tens(x.v, dt),
-        "g": tens(x.g, torch.float32), "beta": tens(x.beta, torch.float32),
+        "g": tens(x.g, torch.float32), "beta": None if x.beta is None else tens(x.beta, torch.float32),
         "h0": None if x.h0 is None else torch.from_numpy(x.h0).to(device).contiguous(),
         "cu_seqlens": torch.from_numpy(x.cu_seqlens.astype(np.int32)).to(device) if x.varlen else None,
     }

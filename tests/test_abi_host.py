@@ -53,7 +53,6 @@ def _call(**over):
     (dict(k=0), kda.KDA_ERR_INVALID_ARG),
     (dict(v=0), kda.KDA_ERR_INVALID_ARG),
     (dict(g=0), kda.KDA_ERR_INVALID_ARG),
-    (dict(beta=0), kda.KDA_ERR_INVALID_ARG),
     (dict(o=0), kda.KDA_ERR_INVALID_ARG),
     (dict(B=0), kda.KDA_ERR_INVALID_ARG),
     (dict(T=-1), kda.KDA_ERR_INVALID_ARG),

@@ -74,7 +74,7 @@ def test_workload_accounting_and_dispatch():
 
     # the benchmark workload's shape (its arrays are not needed for the accounting)
     x = SimpleNamespace(dtype="bf16", T_total=16384, N=2, H_k=32, H_v=32, d_k=128, d_v=128,
-                        gate="channel", h0=True)
+                        gate="channel", h0=True, beta=True)
     # 1,540 B per (token, head) at d = 128 bf16, plus h0 and ht: 815.8 MB per launch
     assert bench.algorithmic_bytes(x) == 16384 * 32 * 1540 + 2 * 32 * 2 * 4 * 128 * 128
     assert bench.forward_kernel(x, 152) == "kda_fwd_pc_kernel"  # 64 units on 152 SMs

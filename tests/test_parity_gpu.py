@@ -179,3 +179,36 @@ def test_bf16_d128_kernels_agree():
     # so the two differ by about the bf16 unit roundoff and are equally close to the oracle
     assert rel_l2(o1, o2) < 8e-3 and rel_l2(h1, h2) < 8e-3
     assert abs(e1 - e2) < 2e-3
+
+
+# beta = NULL: the decay-only recurrence S <- Diag(a_t) S + k_t v_t^T, against the
+# oracle's decay-only path, on every kernel and both gate modes
+@pytest.mark.parametrize("case", ["d128", "d128_one_cta", "d64", "f32", "head_gate_varlen"])
+def test_decay_only(case):
+    kw = {}
+    if case.startswith("d128"):
+        x = make_inputs((300, 300), 2, 4, 128, 128, seed=140, h0=True, beta=False)
+        kw = {"one_cta_per_unit": case.endswith("one_cta")}
+    elif case == "d64":
+        x = make_inputs((200,), 2, 2, 64, 64, seed=141, h0=True, beta=False)
+    elif case == "f32":
+        x = make_inputs((130, 70), 1, 2, 128, 128, seed=142, dtype="f32", varlen=True, beta=False)
+    else:
+        x = make_inputs((1, 64, 190), 2, 2, 128, 128, seed=143, gate="head", h0=True, varlen=True,
+                        beta=False)
+    assert x.beta is None
+    _check(x, f"decay-only {case}", **kw)
+
+
+def test_decay_only_benchmark_shape_sampled():
+    from inputs import workload_inputs
+
+    x = workload_inputs("kda_decayonly_b2_t8192_h32_d128_bf16")
+    o, ht = run_gpu(x)
+    units = [(0, 0), (1, 31), (0, 17)]
+    res = run_oracle(x, units=units)
+    for (n, h), (ou, hu) in zip(units, res):
+        s, e = x.cu_seqlens[n], x.cu_seqlens[n + 1]
+        eo, eh = rel_l2(o[s:e, h], ou), rel_l2(ht[n, h], hu)
+        print(f"decay-only 2x8192x32: unit ({n}, {h}) rel_l2 o={eo:.3e} ht={eh:.3e}")
+        assert eo <= TOL["bf16"] and eh <= TOL["bf16"]
