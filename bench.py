@@ -266,12 +266,17 @@ def run_ours(args, world, rank, local, pg):
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
     entry = lib.kda_chunk_fwd if x.dtype == "bf16" else lib.kda_chunk_fwd_f32
+    chunk_arg = (64,)
+    if args.entry == "recurrent":
+        if x.dtype != "bf16":
+            raise SystemExit("--entry recurrent takes a bf16 workload")
+        entry, chunk_arg = lib.kda_recurrent_fwd, ()
 
     def call():
         st = entry(D["q"].data_ptr(), D["k"].data_ptr(), D["v"].data_ptr(), D["g"].data_ptr(),
                    D["beta"].data_ptr() if "beta" in D else None, D["h0"].data_ptr(), D["o"].data_ptr(),
                    D["ht"].data_ptr(),
-                   B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale, None, sh)
+                   B, T, x.H_k, x.H_v, x.d_k, x.d_v, *chunk_arg, x.scale, None, sh)
         if st != 0:
             raise RuntimeError(kda.status_string(st))
 
@@ -344,15 +349,19 @@ def run_ours(args, world, rank, local, pg):
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": x.dtype, "data": "synthetic",
             "config": {"workload": args.workload, "B": B, "T": T, "H_k": x.H_k, "H_v": x.H_v, "d_k": x.d_k,
-                       "d_v": x.d_v, "C": 64, "gate": "per-channel", "h0": True, "ht": True,
+                       "d_v": x.d_v, "C": 64 if args.entry == "chunk" else None, "entry": args.entry,
+                       "gate": "per-channel" if x.gate == "channel" else "per-head",
+                       "beta": x.beta is not None, "h0": x.h0 is not None, "ht": True,
                        "global_batch": B * world, "seq_len": T, "parallelism": f"dp{world} (independent batches)",
-                       "l2": "inputs larger than L2 (816 MB per step), no flush"},
+                       "l2": f"inputs larger than L2 ({abytes / 1e6:.0f} MB per step), no flush"
+                       if abytes > 129e6 else f"{abytes / 1e6:.0f} MB per step (not flushed)"},
             "e2e": {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": abytes,
-                         "kernel": forward_kernel(x, torch.cuda.get_device_properties(dev).multi_processor_count),
+                         "kernel": "kda_recurrent_kernel" if args.entry == "recurrent" else
+                         forward_kernel(x, torch.cuda.get_device_properties(dev).multi_processor_count),
                          "tflops": flops / (ms / 1000.0) / 1e12},
             "cpu_baseline": cpu,
             "clocks": clocks,
@@ -369,6 +378,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--entry", choices=["chunk", "recurrent"], default="chunk",
+                    help="kda_chunk_fwd (default) or kda_recurrent_fwd (the token-by-token decode step)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # the timing rules ask for at least 3 warm-up steps
     world, rank, local, pg = dist_setup()

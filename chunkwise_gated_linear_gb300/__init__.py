@@ -11,6 +11,8 @@ from .kda import (  # noqa: F401
     kda_chunk_fwd_noalloc,
     kda_fwd_params,
     kda_get_device_error,
+    kda_recurrent_fwd,
+    kda_recurrent_fwd_ex,
     lib,
     status_string,
 )

@@ -14,6 +14,7 @@ cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched);
 cudaError_t launch_fwd_pc_static(const FwdArgs &a, cudaStream_t stream);
 int pc_static_max_units();
+cudaError_t launch_recurrent(const FwdArgs &a, bool f32, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -157,6 +158,30 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
         return KDA_ERR_CUDA;
     }
     return KDA_OK;
+}
+
+int kda_recurrent_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) {
+    if (p == nullptr) return KDA_ERR_INVALID_ARG;
+    kda_fwd_params r = *p;
+    r.C = kda::kChunk;  // no chunks: C is not used
+    kda::FwdArgs a;
+    const int st = prepare(r, a);
+    if (st != KDA_OK) return st;
+    cudaError_t e = device_error_ptr(&a.err);
+    if (e == cudaSuccess) e = kda::launch_recurrent(a, p->dtype == KDA_DTYPE_F32, stream);
+    if (e != cudaSuccess) {
+        t_last_cuda_error = e;
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+int kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                      const float *h0, void *o, float *ht, int B, int T, int H_k, int H_v, int d_k, int d_v,
+                      float scale, const int32_t *cu_seqlens, cudaStream_t stream) {
+    kda_fwd_params p{q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, kda::kChunk, scale, cu_seqlens,
+                     KDA_DTYPE_BF16, KDA_GATE_PER_CHANNEL, 0};
+    return kda_recurrent_fwd_ex(&p, stream);
 }
 
 int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) {

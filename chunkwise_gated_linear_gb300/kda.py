@@ -29,7 +29,8 @@ KDA_DEVICE_ERR_SEQLENS = 1
 KDA_DEVICE_ERR_TIMEOUT = 2
 
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_ex", "kda_status_string",
-            "kda_get_device_error", "kda_chunk_fwd_noalloc")
+            "kda_get_device_error", "kda_chunk_fwd_noalloc", "kda_recurrent_fwd",
+            "kda_recurrent_fwd_ex")
 
 
 class KdaError(RuntimeError):
@@ -73,6 +74,10 @@ def lib() -> ctypes.CDLL:
             fn.restype = I
         L.kda_chunk_fwd_ex.argtypes = [ctypes.POINTER(kda_fwd_params), P]
         L.kda_chunk_fwd_ex.restype = I
+        L.kda_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+        L.kda_recurrent_fwd.restype = I
+        L.kda_recurrent_fwd_ex.argtypes = [ctypes.POINTER(kda_fwd_params), P]
+        L.kda_recurrent_fwd_ex.restype = I
         L.kda_status_string.argtypes = [I]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_get_device_error.argtypes = [P]
@@ -109,6 +114,16 @@ def kda_chunk_fwd_ex(params: kda_fwd_params, stream) -> int:
     return lib().kda_chunk_fwd_ex(ctypes.byref(params), stream or None)
 
 
+def kda_recurrent_fwd(q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, scale, cu_seqlens,
+                      stream) -> int:
+    return lib().kda_recurrent_fwd(q, k, v, g, beta or None, h0 or None, o, ht or None, B, T, H_k,
+                                   H_v, d_k, d_v, scale, cu_seqlens or None, stream or None)
+
+
+def kda_recurrent_fwd_ex(params: kda_fwd_params, stream) -> int:
+    return lib().kda_recurrent_fwd_ex(ctypes.byref(params), stream or None)
+
+
 def kda_get_device_error(stream) -> int:
     return lib().kda_get_device_error(stream or None)
 
@@ -121,7 +136,7 @@ def _ptr(t):
 
 def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
                   output_final_state=True, chunk_size=64, o=None, ht=None, stream=None,
-                  one_cta_per_unit=False):
+                  one_cta_per_unit=False, recurrent=False):
     """Chunkwise KDA forward on torch CUDA tensors; returns ``(o, ht)``.
 
     q, k [B, T, H_k, d_k] and v [B, T, H_v, d_v], all bf16 or all fp32; g fp32
@@ -131,7 +146,8 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
     on the device) B must be 1 and the N sequences are packed along T. ``o`` and ``ht``
     may be given to write into existing buffers. ``ht`` is None in the result when
     ``output_final_state`` is False. ``one_cta_per_unit`` sets KDA_FLAG_ONE_CTA_PER_UNIT
-    (never the persistent kernel that occupies every SM).
+    (never the persistent kernel that occupies every SM). ``recurrent`` computes token by
+    token (kda_recurrent_fwd_ex: the decode step; ``ht`` may then be ``h0`` itself).
     """
     import torch
 
@@ -188,7 +204,11 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
                        _ptr(ht) or None, nb, nt, H_k, H_v, d_k, d_v, chunk_size, float(scale),
                        _ptr(cu_seqlens) or None, dtype, gate,
                        KDA_FLAG_ONE_CTA_PER_UNIT if one_cta_per_unit else 0)
-    st = kda_chunk_fwd_ex(p, stream)
+    if recurrent:
+        p.flags = 0
+        st = kda_recurrent_fwd_ex(p, stream)
+    else:
+        st = kda_chunk_fwd_ex(p, stream)
     if st != KDA_OK:
-        raise KdaError(st, "kda_chunk_fwd_ex")
+        raise KdaError(st, "kda_recurrent_fwd_ex" if recurrent else "kda_chunk_fwd_ex")
     return o, ht

@@ -166,6 +166,23 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
                           int T, int H_k, int H_v, int d_k, int d_v, int C, float scale,
                           const int32_t *cu_seqlens, cudaStream_t stream);
 
+/*
+ * kda_recurrent_fwd — the same operation computed token by token (the recurrent form:
+ * "TileLang 实战：KDA 从零到一–Kimi Delta Attention", §0, and the recurrent form of
+ * "Gated DeltaNet"), for decoding: typically a few tokens per sequence, continuing from a
+ * state h0 written by kda_chunk_fwd or by an earlier call. Arguments, layouts, NULL
+ * conventions (beta == NULL: decay-only) and errors as kda_chunk_fwd, without C.
+ * ht may equal h0: the state is then updated in place (each part of it is read before it
+ * is written by the same thread). bf16 q/k/v/o; d_k, d_v in {64, 128}.
+ */
+int kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, const float *h0, void *o, float *ht, int B, int T,
+                      int H_k, int H_v, int d_k, int d_v, float scale,
+                      const int32_t *cu_seqlens, cudaStream_t stream);
+
+/* kda_recurrent_fwd with the dtype and gate mode of the struct (its C is ignored). */
+int kda_recurrent_fwd_ex(const kda_fwd_params *p, cudaStream_t stream);
+
 /* A static, human-readable description of a status (and of the last CUDA error for
  * KDA_ERR_CUDA on this thread). */
 const char *kda_status_string(int status);

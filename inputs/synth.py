@@ -75,6 +75,8 @@ WORKLOAD_SEEDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
 # Smaller cases of the same kernels for profiler captures (inputs still larger than L2),
 # and the decay-only variant of the benchmark shape.
 PROFILE_WORKLOADS = {
+    "kda_decode_b256_t1_h32_d128_bf16": Workload(
+        "kda_decode_b256_t1_h32_d128_bf16", (1,) * 256, 32, 32, 128, 128, h0=True),
     "kda_decayonly_b2_t8192_h32_d128_bf16": Workload(
         "kda_decayonly_b2_t8192_h32_d128_bf16", (8192,) * 2, 32, 32, 128, 128, h0=True, beta=False),
     "kda_b1_t8192_h32_d128_bf16": Workload(
