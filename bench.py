@@ -17,6 +17,7 @@ step a bounded sample of (sequence, head) units of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import glob
 import hashlib
 import json
@@ -243,40 +244,51 @@ def run_ours(args, world, rank, local, pg):
     lib = kda.lib()
 
     x = workload_inputs(args.workload, seed=1000 + rank)
-    B = x.N
-    T = x.T_total // B
+    B = x.N                       # sequences
+    Bp = 1 if x.varlen else B     # physical batch (packed sequences: one row of T_total tokens)
+    T = x.T_total // Bp
     dt_io = torch.bfloat16 if x.dtype == "bf16" else torch.float32
 
     def host(a, dtype, shape):
         return torch.from_numpy(np.ascontiguousarray(a)).reshape(shape).to(dtype).pin_memory()
 
+    gshape = (Bp, T, x.H_v, x.d_k) if x.gate == "channel" else (Bp, T, x.H_v)
     H = {
-        "q": host(x.q, dt_io, (B, T, x.H_k, x.d_k)), "k": host(x.k, dt_io, (B, T, x.H_k, x.d_k)),
-        "v": host(x.v, dt_io, (B, T, x.H_v, x.d_v)), "g": host(x.g, torch.float32, (B, T, x.H_v, x.d_k)),
-        "h0": host(x.h0, torch.float32, (B, x.H_v, x.d_k, x.d_v)),
+        "q": host(x.q, dt_io, (Bp, T, x.H_k, x.d_k)), "k": host(x.k, dt_io, (Bp, T, x.H_k, x.d_k)),
+        "v": host(x.v, dt_io, (Bp, T, x.H_v, x.d_v)), "g": host(x.g, torch.float32, gshape),
     }
     if x.beta is not None:  # no beta: the decay-only recurrence
-        H["beta"] = host(x.beta, torch.float32, (B, T, x.H_v))
+        H["beta"] = host(x.beta, torch.float32, (Bp, T, x.H_v))
+    if x.h0 is not None:  # no h0: a zero initial state
+        H["h0"] = host(x.h0, torch.float32, (B, x.H_v, x.d_k, x.d_v))
     inputs = [key for key in ("q", "k", "v", "g", "beta", "h0") if key in H]
     D = {key: t.to(dev) for key, t in H.items()}
-    D["o"] = torch.empty((B, T, x.H_v, x.d_v), dtype=dt_io, device=dev)
+    D["o"] = torch.empty((Bp, T, x.H_v, x.d_v), dtype=dt_io, device=dev)
     D["ht"] = torch.empty((B, x.H_v, x.d_k, x.d_v), dtype=torch.float32, device=dev)
     H["o"] = torch.empty_like(D["o"], device="cpu").pin_memory()
     H["ht"] = torch.empty_like(D["ht"], device="cpu").pin_memory()
+    cu = torch.from_numpy(x.cu_seqlens.astype(np.int32)).to(dev) if x.varlen else None
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
-    entry = lib.kda_chunk_fwd if x.dtype == "bf16" else lib.kda_chunk_fwd_f32
-    chunk_arg = (64,)
-    if args.entry == "recurrent":
-        if x.dtype != "bf16":
-            raise SystemExit("--entry recurrent takes a bf16 workload")
-        entry, chunk_arg = lib.kda_recurrent_fwd, ()
+    ptr = lambda key: D[key].data_ptr() if key in D else None  # noqa: E731
+    params = kda.kda_fwd_params(
+        ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"), ptr("ht"), B, T, x.H_k,
+        x.H_v, x.d_k, x.d_v, 64, x.scale, None if cu is None else cu.data_ptr(),
+        kda.KDA_DTYPE_BF16 if x.dtype == "bf16" else kda.KDA_DTYPE_F32,
+        kda.KDA_GATE_PER_CHANNEL if x.gate == "channel" else kda.KDA_GATE_PER_HEAD, 0)
+    north_star = args.entry == "chunk" and x.dtype == "bf16" and x.gate == "channel"
 
     def call():
-        st = entry(D["q"].data_ptr(), D["k"].data_ptr(), D["v"].data_ptr(), D["g"].data_ptr(),
-                   D["beta"].data_ptr() if "beta" in D else None, D["h0"].data_ptr(), D["o"].data_ptr(),
-                   D["ht"].data_ptr(),
-                   B, T, x.H_k, x.H_v, x.d_k, x.d_v, *chunk_arg, x.scale, None, sh)
+        # kda_chunk_fwd (the spec symbol) when the workload fits its argument list,
+        # else the struct entry points of the same ABI
+        if north_star:
+            st = lib.kda_chunk_fwd(ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"),
+                                   ptr("ht"), B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale,
+                                   None if cu is None else cu.data_ptr(), sh)
+        elif args.entry == "recurrent":
+            st = lib.kda_recurrent_fwd_ex(ctypes.byref(params), sh)
+        else:
+            st = lib.kda_chunk_fwd_ex(ctypes.byref(params), sh)
         if st != 0:
             raise RuntimeError(kda.status_string(st))
 
@@ -306,7 +318,7 @@ def run_ours(args, world, rank, local, pg):
     ms = ev0.elapsed_time(ev1) / args.steps
     clocks = clk.summary()
     ms_max = max_over_ranks(pg, ms)
-    tokens = B * T
+    tokens = x.T_total
     value = tokens * world / (ms_max / 1000.0)
 
     # end to end through the C ABI with host buffers: H2D inputs, call, D2H results
@@ -348,11 +360,13 @@ def run_ours(args, world, rank, local, pg):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": x.dtype, "data": "synthetic",
-            "config": {"workload": args.workload, "B": B, "T": T, "H_k": x.H_k, "H_v": x.H_v, "d_k": x.d_k,
+            "config": {"workload": args.workload, "B": B, "T": T if not x.varlen else None,
+                       "T_total": x.T_total, "H_k": x.H_k, "H_v": x.H_v, "d_k": x.d_k,
                        "d_v": x.d_v, "C": 64 if args.entry == "chunk" else None, "entry": args.entry,
                        "gate": "per-channel" if x.gate == "channel" else "per-head",
                        "beta": x.beta is not None, "h0": x.h0 is not None, "ht": True,
-                       "global_batch": B * world, "seq_len": T, "parallelism": f"dp{world} (independent batches)",
+                       "global_batch": B * world, "seq_len": T if not x.varlen else x.T_total // B,
+                       "parallelism": f"dp{world} (independent batches)",
                        "l2": f"inputs larger than L2 ({abytes / 1e6:.0f} MB per step), no flush"
                        if abytes > 129e6 else f"{abytes / 1e6:.0f} MB per step (not flushed)"},
             "e2e": {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",

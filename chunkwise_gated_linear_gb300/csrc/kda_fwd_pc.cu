@@ -28,6 +28,7 @@
 // never waits on a later one. The launch is cooperative (every CTA resident). Every
 // wait is bounded (about one second) and watches a global abort word, so a failure
 // anywhere ends all CTAs with KDA_DEVICE_ERR_TIMEOUT.
+#include <algorithm>
 #include <cstring>
 
 #include "tc_util.cuh"
@@ -41,7 +42,7 @@ using namespace tc5;
 using namespace tcu;
 
 constexpr int kMaxUnits = 76;       // units served by one launch (at most half the SMs)
-constexpr int kRing = 8;            // ring slots per unit (a launch argument)
+constexpr int kRing = 8;            // ring slots per unit, at least (a launch argument)
 constexpr int kThreads = 512;
 
 // Slot image (global ring and consumer shared memory). [d][tok] tiles hold one row per
@@ -90,25 +91,27 @@ struct Prod {
 static_assert(Prod::oEG + 512 <= Prod::oKP0, "image overlaps");
 // Consumer shared memory.
 struct Cons {
-    static constexpr int oBuf0 = 0;        // slot images, buffers 0 / 1
-    static constexpr int oBuf1 = Slot::kStride;
-    static constexpr int oOS = 2 * Slot::kStride;  // O staging, 2 x [32 tok][128] bf16
+    static constexpr int kBufs = 3;        // slot images in flight: loads have up to two
+                                           // chunks of the serial step to land
+    static constexpr int kEnd = kBufs * Slot::kStride;
 };
 // Both roles.
 struct Common {
-    static constexpr int oBar = Prod::kEnd;  // mbarriers
+    static constexpr int oBar = Prod::kEnd > Cons::kEnd ? Prod::kEnd : Cons::kEnd;  // mbarriers
     static constexpr int oTmemAddr = oBar + 256;
     static constexpr int oFlag = oTmemAddr + 16;   // CTA abort flag
     static constexpr int oUnits = oFlag + 16;      // UnitInfo [kMaxUnits]
-    static constexpr int kEnd = oUnits + 16 * kMaxUnits;
+    static constexpr int oSeen = oUnits + 16 * kMaxUnits;  // producer: done[u] last observed
+    static constexpr int kEnd = oSeen + 4 * kMaxUnits;
     static constexpr int kBytes = kEnd + 1024;      // + slack to align the base
 };
-static_assert(Cons::oOS + 16384 <= Common::oBar, "consumer layout overlaps");
+
 static_assert(Common::kBytes <= 232448, "shared memory");
 
 // TMEM columns
 constexpr uint32_t tGram = 0, tW = 64, tU = 128, kTmemProd = 256;     // producer
-constexpr uint32_t tX = 0, tSA = 128, tV = 192, tS = 256, kTmemCons = 512;  // consumer
+// consumer: D_X / O^T in two buffers (by chunk parity), S^T bf16, Vt^T, S^T fp32
+constexpr uint32_t tX0 = 0, tSA = 128, tV = 192, tS = 256, tX1 = 384, kTmemCons = 512;
 
 enum {
     // producer
@@ -119,8 +122,8 @@ enum {
     B_LFREE,                 // back -> front: L and beta consumed by the solve
     B_PZ0, B_PZ1,            // drains after a failure (one per MMA-issuing thread)
     // consumer
-    B_FULL0, B_FULL1,        // slot image in buffer 0 / 1 landed
-    B_EMPTY0, B_EMPTY1,      // buffer 0 / 1 consumed by the serial step
+    B_FULL0, B_FULL1, B_FULL2,     // slot image in buffer 0 / 1 / 2 landed
+    B_EMPTY0, B_EMPTY1, B_EMPTY2,  // buffer 0 / 1 / 2 consumed by the serial step
     B_X, B_S2,               // serial products
     B_CZ,
     kNumBars
@@ -195,12 +198,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
     return true;
 }
-// Bounded wait until the global word *p reaches at least `target` (acquire).
+// Bounded wait until the global word *p reaches at least `target` (acquire); the value
+// read last goes to *seen.
 __device__ __forceinline__ bool wait_geq(const int *p, int target, volatile int *cta_flag, const FwdArgs &a,
-                                         const PcArgs &pc) {
-    if (ld_acquire(p) >= target) return true;
+                                         const PcArgs &pc, int *seen = nullptr) {
+    int v = ld_acquire(p);
+    if (seen) *seen = v;
+    if (v >= target) return true;
     const long long t0 = clock64();
-    while (ld_acquire(p) < target) {
+    while ((v = ld_acquire(p)) < target) {
         if (*cta_flag) return false;
         if (*(volatile int *)pc.abort) {
             *cta_flag = 1;
@@ -212,6 +218,7 @@ __device__ __forceinline__ bool wait_geq(const int *p, int target, volatile int 
         }
         __nanosleep(64);
     }
+    if (seen) *seen = v;
     return true;
 }
 
@@ -222,6 +229,7 @@ struct Ctx {
     uint64_t *bars;
     volatile int *flag;     // this CTA is aborting
     volatile int *stored;   // producer: jobs whose front image is written to the ring
+    int *seen;              // producer, thread 0: done[u] as last acquired, per unit
     const UnitInfo *units;  // [U]
     int maxc, uniform;      // over the units of this launch
     int p;                  // producer index (producer CTAs)
@@ -408,8 +416,11 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             bulk_wait_done();
             *x.stored = jo;
         }
-        // the ring slot holds chunk c - R until the consumer has copied it out
-        if (!failed && ptid == 0 && c >= pc.R) failed = !wait_geq(&pc.done[u], c - pc.R + 1, x.flag, a, pc);
+        // the ring slot holds chunk c - R until the consumer has copied it out; done[u] only
+        // grows, so a value this CTA has already acquired that is large enough saves the
+        // round trip to L2
+        if (!failed && ptid == 0 && c >= pc.R && x.seen[u] < c - pc.R + 1)
+            failed = !wait_geq(&pc.done[u], c - pc.R + 1, x.flag, a, pc, &x.seen[u]);
         // hand-off slot b (Kp^T) is free once the back stage has multiplied job jo - 2
         if (!failed && jo >= 2)
             failed = !wait_bar(&bars[B_HEMPTY0 + b], (uint32_t)(((jo >> 1) - 1) & 1), x.flag, a, pc);
@@ -805,9 +816,10 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
 }
 
 // ---------------------------------------------------------------------------------------
-// consumer, loader (warps 4-7): slot images of unit u into the two shared buffers, each as
-// four bulk copies from four warps (so that they overlap). Returns, for thread 128, 0 or
-// 1 + 2 * buffer + parity of copies that may still be in flight.
+// consumer, loader (warps 4-7): slot images of unit u into the three shared buffers, each
+// as four bulk copies from four warps (so that they overlap); up to three in flight. A
+// ring slot is released when its buffer comes round again. Returns, for thread 128, the
+// copies that may still be in flight: bit b for buffer b, bit 4 + b its phase parity.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &pc, const Ctx &x, int u, int nch) {
     uint64_t *bars = x.bars;
@@ -817,10 +829,14 @@ __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &p
     int pend = 0;
     bool failed = false;
     for (int c = 0; c < nch; ++c) {
-        const int b = c & 1;
+        const int b = c % Cons::kBufs, k = c / Cons::kBufs;  // buffer and its use count
         if (lt == 0 && !failed) {
-            // buffer b held chunk c - 2 until the serial step released it
-            if (c >= 2) failed = !wait_bar(&bars[B_EMPTY0 + b], (uint32_t)(((c >> 1) - 1) & 1), x.flag, a, pc);
+            // buffer b held chunk c - 3 until the serial step released it; that copy has
+            // long landed, so the ring slot of chunk c - 3 is free for the producers
+            if (c >= Cons::kBufs) {
+                failed = !wait_bar(&bars[B_EMPTY0 + b], (uint32_t)((k - 1) & 1), x.flag, a, pc);
+                if (!failed) st_release(&pc.done[u], c - Cons::kBufs + 1);
+            }
             if (!failed) failed = !wait_geq(&pc.ready[u * pc.R + c % pc.R], c + 1, x.flag, a, pc);
             if (!failed) mbar_arrive_expect_tx(&bars[B_FULL0 + b], Slot::kBytes);
         }
@@ -830,17 +846,9 @@ __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &p
         }
         if (lane == 0) {
             fence_proxy_async_global();  // the producers' generic writes, before the async-proxy read
-            bulk_load(x.sm + (b ? Cons::oBuf1 : Cons::oBuf0) + lw * kPart, slot_ptr(pc, u, c) + lw * kPart, kPart,
-                      &bars[B_FULL0 + b]);
+            bulk_load(x.sm + b * Slot::kStride + lw * kPart, slot_ptr(pc, u, c) + lw * kPart, kPart, &bars[B_FULL0 + b]);
         }
-        pend = 1 + 2 * b + ((c >> 1) & 1);
-        if (lt == 0) {
-            failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c >> 1) & 1), x.flag, a, pc);
-            if (!failed) {
-                st_release(&pc.done[u], c + 1);  // the ring slot may be overwritten
-                pend = 0;
-            }
-        }
+        pend = (pend & ~(0x11 << b)) | ((1 | ((k & 1) << 4)) << b);
     }
     return lt == 0 ? pend : 0;
 }
@@ -890,16 +898,31 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
     fence_before_sync();
     bar_named(1, 256);
 
+    // O^T of chunk cc, row dv, tokens 32 grp .. +31 -> o[token][dv] (valid tokens only;
+    // a warp writes 64 contiguous bytes per token). Runs while the next chunk's first MMA
+    // does.
+    auto write_o = [&](int cc) {
+        const int row0o = cc * kChunk;
+        const int nvalido = min(kChunk, len - row0o);
+        float v[32];
+        tmem_ld32(tmem + lane_off + ((cc & 1) ? tX1 : tX0) + 64 + 32 * grp, v);
+        bf16 *op = o + (bos + row0o + 32 * grp) * sv + (int64_t)h * 128 + dv;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            if (32 * grp + e < nvalido) op[(int64_t)e * sv] = __float2bfloat16_rn(v[e]);
+    };
+
     bool failed = false;
     for (int c = 0; c < nchunks; ++c) {
         const int row0 = c * kChunk;
         const int nvalid = min(kChunk, len - row0);
-        const int b = c & 1;
-        const uint32_t oB = b ? Cons::oBuf1 : Cons::oBuf0;
+        const int b = c % Cons::kBufs;  // slot buffer; the TMEM buffers go by c & 1
+        const uint32_t oB = b * Slot::kStride;
         const float *EG = reinterpret_cast<const float *>(sm + oB + Slot::oEG);
         const uint32_t *U2 = reinterpret_cast<const uint32_t *>(sm + oB + Slot::oU);
+        const uint32_t tX = (c & 1) ? tX1 : tX0;
 
-        failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c >> 1) & 1), x.flag, a, pc);
+        failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c / Cons::kBufs) & 1), x.flag, a, pc);
         if (bar_or(1, 256, failed)) { failed = true; break; }
         fence_after_sync();
 
@@ -912,7 +935,9 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
                        s > 0);
             commit(&bars[B_X]);
         }
-        // meanwhile S^T <- S^T Diag(e^gamma_n): column d of S^T scales by e^gamma_n[d]
+        // meanwhile the previous chunk's output leaves, and S^T <- S^T Diag(e^gamma_n)
+        // (column d of S^T scales by e^gamma_n[d])
+        if (c > 0) write_o(c - 1);
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
             float v[32];
@@ -977,32 +1002,15 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
             tmem_st16(tmem + lane_off + tSAc + 16 * pass, p16);
         }
         tmem_st_wait();
-        // O^T row dv, tokens 32 grp .. +31 -> o[token][dv] (valid tokens only) through a
-        // [32 tok][128 dv] staging tile per half so that global stores are 16 bytes wide
-        {
-            bf16 *OS = reinterpret_cast<bf16 *>(sm + Cons::oOS + grp * 8192);
-            float v[32];
-            tmem_ld32(tmem + lane_off + tX + 64 + 32 * grp, v);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) OS[e * 128 + dv] = __float2bfloat16_rn(v[e]);
-        }
-        bar_named(1, 256);
-        {
-            const int st = (grp << 7) + (threadIdx.x & 127);  // 0..255
-#pragma unroll
-            for (int i = st; i < 1024; i += 256) {
-                const int r = i >> 4, c16 = i & 15;  // r: token 0..63 of the chunk
-                if (r < nvalid)
-                    *reinterpret_cast<uint4 *>(o + (bos + row0 + r) * sv + (int64_t)h * 128 + c16 * 8) =
-                        *reinterpret_cast<const uint4 *>(sm + Cons::oOS + (r >> 5) * 8192 + (r & 31) * 256 + c16 * 16);
-            }
-        }
         fence_before_sync();
-        bar_named(1, 256);  // the staging tiles and tX are free for the next chunk
     }
     if (failed) {
         *x.flag = 1;
         return;
+    }
+    if (nchunks > 0) {
+        fence_after_sync();
+        write_o(nchunks - 1);
     }
     if (a.ht != nullptr) {
         float *ht = a.ht + ((int64_t)n * a.H_v + h) * 128 * 128 + dv;
@@ -1027,6 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *stats = reinterpret_cast<int *>(sm + Common::oFlag + 4);  // most chunks, uniform
     volatile int *stored = reinterpret_cast<volatile int *>(sm + Common::oFlag + 12);
     UnitInfo *units = reinterpret_cast<UnitInfo *>(sm + Common::oUnits);
+    int *seen = reinterpret_cast<int *>(sm + Common::oSeen);
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool consumer = (int)blockIdx.x < pc.U;
     const uint32_t ncols = consumer ? kTmemCons : kTmemProd;
@@ -1051,6 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
         *flag = 0;
         *stored = 0;
+        for (int i = 0; i < kMaxUnits; ++i) seen[i] = 0;
         mbar_fence_init();
     }
     if (warp == 0) {
@@ -1076,6 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.bars = bars;
     x.flag = flag;
     x.stored = stored;
+    x.seen = seen;
     x.units = units;
     x.maxc = stats[0];
     x.uniform = stats[1];
@@ -1109,8 +1120,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             commit(z);
             mbar_wait(z, 0, kWaitCycles);
         }
-        if (consumer && tid == 128 && pend_load > 0)
-            mbar_wait(&bars[B_FULL0 + ((pend_load - 1) >> 1)], (uint32_t)((pend_load - 1) & 1), kWaitCycles);
+        if (consumer && tid == 128) {
+#pragma unroll 1
+            for (int bb = 0; bb < Cons::kBufs; ++bb)
+                if ((pend_load >> bb) & 1) mbar_wait(&bars[B_FULL0 + bb], (uint32_t)((pend_load >> (4 + bb)) & 1), kWaitCycles);
+        }
         if (!consumer && tid == 0) {
             if (pend_front & 1u) mbar_wait(&bars[B_LQK], (pend_front >> 4) & 1u, kWaitCycles);
             if (pend_front & 2u) mbar_wait(&bars[B_LG], (pend_front >> 5) & 1u, kWaitCycles);
@@ -1180,8 +1194,11 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     std::memset(&maps, 0, sizeof(maps));
     if (!encode_tile_maps(&maps, a, GATE_HEAD)) return cudaErrorInvalidValue;
 
-    const size_t ring_bytes = (size_t)U * kRing * Slot::kStride;
-    const size_t flag_words = (size_t)U * kRing + (size_t)U + 1;
+    // ring depth: 8 slots per unit at least, deeper for fewer units (about 38 MB, well
+    // inside L2), so that producers taking jobs in order rarely wait for a slow consumer
+    const int R = (int)std::max<int64_t>(kRing, std::min<int64_t>(4 * kRing, 512 / U));
+    const size_t ring_bytes = (size_t)U * R * Slot::kStride;
+    const size_t flag_words = (size_t)U * R + (size_t)U + 1;
     const size_t flag_bytes = (flag_words * sizeof(int) + 255) & ~(size_t)255;
     cudaMemPool_t pool = nullptr;
     e = scratch_pool(dev, &pool);
@@ -1192,11 +1209,11 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     PcArgs pc;
     pc.ring = static_cast<unsigned char *>(buf);
     pc.ready = reinterpret_cast<int *>(pc.ring + ring_bytes);
-    pc.done = pc.ready + (size_t)U * kRing;
+    pc.done = pc.ready + (size_t)U * R;
     pc.abort = pc.done + U;
     pc.U = (int)U;
     pc.P = sms - (int)U;
-    pc.R = kRing;
+    pc.R = R;
     e = cudaMemsetAsync(pc.ready, 0, flag_bytes, stream);
     if (e == cudaSuccess) {
         void *args[] = {const_cast<FwdArgs *>(&a), &maps, &pc};
