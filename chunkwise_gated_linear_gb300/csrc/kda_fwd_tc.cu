@@ -673,6 +673,23 @@ __global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, con
     u.sbase = smem_u32(sm);
     u.h = blockIdx.y;
     u.n = blockIdx.z;
+    if (a.cu_seqlens != nullptr && a.N <= 64) {
+        // Packed sequences of different lengths: blocks start in index order, so block z
+        // takes the z-th longest sequence (ties by index) and no long unit starts in the
+        // last wave. The lengths are ranked in the (not yet used) solve scratch.
+        int *len_s = reinterpret_cast<int *>(sm + Lay::oPS);
+        if (tid < a.N) len_s[tid] = a.cu_seqlens[tid + 1] - a.cu_seqlens[tid];
+        __syncthreads();
+        if (tid < a.N) {
+            const int ls = len_s[tid];
+            int rank = 0;
+            for (int t = 0; t < a.N; ++t) rank += (len_s[t] > ls) || (len_s[t] == ls && t < tid);
+            if (rank == (int)blockIdx.z) len_s[64] = tid;
+        }
+        __syncthreads();
+        u.n = len_s[64];
+        __syncthreads();
+    }
     u.hk = u.h / a.group;
     if (!seq_bounds(a, u.n, u.bos, u.len)) return;
     u.nchunks = (u.len + kChunk - 1) / kChunk;
