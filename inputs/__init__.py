@@ -5,4 +5,5 @@ L2-normalises q and k per token (a data-preparation step), takes log of the samp
 gates, applies sigmoid to the beta logits and rounds to the storage dtype.
 """
 
-from .synth import WORKLOADS, Inputs, Workload, make_inputs, workload_inputs  # noqa: F401
+from .synth import (WORKLOADS, FrontendInputs, Inputs, Workload, make_frontend_inputs,  # noqa: F401
+                    make_inputs, workload_inputs)

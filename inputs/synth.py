@@ -81,6 +81,9 @@ PROFILE_WORKLOADS = {
         "kda_decayonly_b2_t8192_h32_d128_bf16", (8192,) * 2, 32, 32, 128, 128, h0=True, beta=False),
     "kda_b1_t8192_h32_d128_bf16": Workload(
         "kda_b1_t8192_h32_d128_bf16", (8192,), 32, 32, 128, 128, h0=True),
+    # the benchmark's 64 units (so the same ring depth and launch split) over half the tokens
+    "kda_b2_t4096_h32_d128_bf16": Workload(
+        "kda_b2_t4096_h32_d128_bf16", (4096,) * 2, 32, 32, 128, 128, h0=True),
 }
 
 
@@ -197,6 +200,85 @@ def make_inputs(lengths, H_k, H_v, d_k, d_v, *, dtype="bf16", gate="channel", a_
         g=g, beta=b, h0=hinit, cu_seqlens=cu, H_k=H_k, H_v=H_v, d_k=d_k, d_v=d_v,
         dtype=dtype, gate=gate, scale=float(d_k ** -0.5 if scale is None else scale),
         varlen=bool(varlen), meta={"seed": seed, "a_lo": a_lo},
+    )
+
+
+@dataclass
+class FrontendInputs(Inputs):
+    """Raw inputs of the fused front-end, as handed to the GPU.
+
+    Where the matching switch is on, ``q`` and ``k`` are not normalised, ``g`` holds the
+    gate pre-activation a (not the log gate) and ``beta`` holds the logits b (not beta);
+    ``A_log`` [H_v] and ``dt_bias`` ([H_v, d_k] per-channel, [H_v] per-head) are the
+    gate's per-head parameters (None when the gate is given directly)."""
+
+    A_log: np.ndarray | None = None
+    dt_bias: np.ndarray | None = None
+    qk_l2norm: bool = True
+    beta_sigmoid: bool = True
+
+
+def make_frontend_inputs(lengths, H_k, H_v, d_k, d_v, *, dtype="bf16", gate="channel", h0=False,
+                         beta=True, varlen=None, seed=0, scale=None, qk_l2norm=True,
+                         beta_sigmoid=True, gate_act=True, qk_std=1.0) -> FrontendInputs:
+    """Raw inputs for the fused front-end (one ``default_rng(seed)`` stream, in order):
+
+    1. sequence lengths as given;
+    2. q, k [T, H_k, d_k] ~ N(0, qk_std**2) fp32 (normalised per token and head as in
+       :func:`make_inputs` when ``qk_l2norm`` is off);
+    3. v [T, H_v, d_v] ~ N(0, 1);
+    4. A_log [H_v] = log(U[0.5, 1]); dt_bias ~ U[-5.6, -3.4], one per (value head,
+       channel) or per value head; a ~ U[-1.2, 1.2] per (token, value head, channel) or
+       (token, value head). Then a + dt_bias lies in [-6.8, -2.2], softplus of it in
+       [1.1e-3, 0.105], and the per-token decay exp(g) in [0.90, 0.9994]: the
+       lower-bounded range (at least 0.9) that the Kimi Delta Attention page requires of
+       the gate. With ``gate_act`` off, g = log(U[0.9, 0.999]) directly instead;
+    5. b [T, H_v] ~ N(0, 1) logits (beta = sigmoid(b) stored instead when
+       ``beta_sigmoid`` is off; nothing when ``beta`` is off);
+    6. h0 [N, H_v, d_k, d_v] ~ N(0, 0.1**2), or none.
+    """
+    rng = np.random.default_rng(seed)
+    lengths = tuple(int(x) for x in lengths)
+    if varlen is None:
+        varlen = len(set(lengths)) > 1
+    cu = np.zeros(len(lengths) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lengths)
+    T = int(cu[-1])
+
+    q = (qk_std * _normal_rows(rng, T, H_k * d_k)).astype(np.float32)
+    k = (qk_std * _normal_rows(rng, T, H_k * d_k)).astype(np.float32)
+    if qk_l2norm:
+        q, k = q.reshape(T, H_k, d_k), k.reshape(T, H_k, d_k)
+    else:
+        q, k = _l2_normalise(q, H_k, d_k), _l2_normalise(k, H_k, d_k)
+    v = _normal_rows(rng, T, H_v * d_v).reshape(T, H_v, d_v)
+
+    gshape = (T, H_v, d_k) if gate == "channel" else (T, H_v)
+    A_log = dt_bias = None
+    if gate_act:
+        A_log = np.log(rng.uniform(0.5, 1.0, size=H_v)).astype(np.float32)
+        dt_bias = rng.uniform(-5.6, -3.4, size=gshape[1:]).astype(np.float32)
+        g = rng.uniform(-1.2, 1.2, size=gshape).astype(np.float32)
+    else:
+        g = np.log(rng.uniform(0.9, 0.999, size=gshape)).astype(np.float32)
+
+    b = None
+    if beta:
+        b = _normal_rows(rng, T, H_v)
+        if not beta_sigmoid:
+            b = (1.0 / (1.0 + np.exp(-b.astype(np.float64)))).astype(np.float32)
+
+    hinit = None
+    if h0:
+        hinit = (0.1 * rng.standard_normal((len(lengths), H_v, d_k, d_v), dtype=np.float32)).astype(np.float32)
+
+    return FrontendInputs(
+        q=round_to_dtype(q, dtype), k=round_to_dtype(k, dtype), v=round_to_dtype(v, dtype),
+        g=g, beta=b, h0=hinit, cu_seqlens=cu, H_k=H_k, H_v=H_v, d_k=d_k, d_v=d_v,
+        dtype=dtype, gate=gate, scale=float(d_k ** -0.5 if scale is None else scale),
+        varlen=bool(varlen), meta={"seed": seed, "frontend": True},
+        A_log=A_log, dt_bias=dt_bias, qk_l2norm=bool(qk_l2norm),
+        beta_sigmoid=bool(beta_sigmoid and beta),
     )
 
 
