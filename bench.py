@@ -61,7 +61,11 @@ def algorithmic_bytes(x) -> int:
     gate = 4 * x.d_k if x.gate == "channel" else 4
     per_tok = x.H_k * 2 * x.d_k * e + x.H_v * (2 * x.d_v * e + gate + (4 if x.beta is not None else 0))
     state = x.N * x.H_v * 4 * x.d_k * x.d_v * ((x.h0 is not None) + 1)
-    return T * per_tok + state
+    # the front-end's per-head parameters (A_log, dt_bias), when present
+    params = 0
+    if getattr(x, "A_log", None) is not None:
+        params = 4 * x.A_log.size + (4 * x.dt_bias.size if x.dt_bias is not None else 0)
+    return T * per_tok + state + params
 
 
 def algorithmic_flops(x, C=64) -> int:
@@ -188,11 +192,16 @@ def max_over_ranks(pg, value: float) -> float:
 def oracle_sample(x, n_units, threads=0):
     """Time the fp64 oracle on the first n_units (sequence, head) units; returns
     (seconds, equivalent tokens, threads used)."""
-    from oracle import kda_recurrence, oracle_threads
+    from oracle import kda_fused_recurrence, kda_recurrence, oracle_threads
 
     units = [(n, h) for n in range(x.N) for h in range(x.H_v)][:n_units]
     t0 = time.perf_counter()
-    kda_recurrence(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, x.scale, units=units, threads=threads)
+    if getattr(x, "meta", {}).get("frontend"):
+        kda_fused_recurrence(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, x.scale,
+                             qk_l2norm=x.qk_l2norm, beta_sigmoid=x.beta_sigmoid, A_log=x.A_log,
+                             dt_bias=x.dt_bias, units=units, threads=threads)
+    else:
+        kda_recurrence(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, x.scale, units=units, threads=threads)
     dt = time.perf_counter() - t0
     lens = x.lengths()
     unit_tokens = sum(int(lens[n]) for n, _ in units)
@@ -235,7 +244,7 @@ def run_ours(args, world, rank, local, pg):
     import torch
 
     from chunkwise_gated_linear_gb300 import kda
-    from inputs import workload_inputs
+    from inputs import workload_frontend_inputs, workload_inputs
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
@@ -243,7 +252,11 @@ def run_ours(args, world, rank, local, pg):
     dev = torch.device("cuda", local)
     lib = kda.lib()
 
-    x = workload_inputs(args.workload, seed=1000 + rank)
+    fe_on = args.frontend != "none"
+    if fe_on:
+        x = workload_frontend_inputs(args.workload, seed=1000 + rank)
+    else:
+        x = workload_inputs(args.workload, seed=1000 + rank)
     B = x.N                       # sequences
     Bp = 1 if x.varlen else B     # physical batch (packed sequences: one row of T_total tokens)
     T = x.T_total // Bp
@@ -261,7 +274,10 @@ def run_ours(args, world, rank, local, pg):
         H["beta"] = host(x.beta, torch.float32, (Bp, T, x.H_v))
     if x.h0 is not None:  # no h0: a zero initial state
         H["h0"] = host(x.h0, torch.float32, (B, x.H_v, x.d_k, x.d_v))
-    inputs = [key for key in ("q", "k", "v", "g", "beta", "h0") if key in H]
+    if fe_on:  # the gate's per-head parameters
+        H["A_log"] = host(x.A_log, torch.float32, (x.H_v,))
+        H["dt_bias"] = host(x.dt_bias, torch.float32, x.dt_bias.shape)
+    inputs = [key for key in ("q", "k", "v", "g", "beta", "h0", "A_log", "dt_bias") if key in H]
     D = {key: t.to(dev) for key, t in H.items()}
     D["o"] = torch.empty((Bp, T, x.H_v, x.d_v), dtype=dt_io, device=dev)
     D["ht"] = torch.empty((B, x.H_v, x.d_k, x.d_v), dtype=torch.float32, device=dev)
@@ -275,13 +291,18 @@ def run_ours(args, world, rank, local, pg):
         ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"), ptr("ht"), B, T, x.H_k,
         x.H_v, x.d_k, x.d_v, 64, x.scale, None if cu is None else cu.data_ptr(),
         kda.KDA_DTYPE_BF16 if x.dtype == "bf16" else kda.KDA_DTYPE_F32,
-        kda.KDA_GATE_PER_CHANNEL if x.gate == "channel" else kda.KDA_GATE_PER_HEAD, 0)
-    north_star = args.entry == "chunk" and x.dtype == "bf16" and x.gate == "channel"
+        kda.KDA_GATE_PER_CHANNEL if x.gate == "channel" else kda.KDA_GATE_PER_HEAD,
+        kda.KDA_FLAG_UNFUSED_FRONTEND if args.frontend == "unfused" else 0)
+    fe = kda.kda_frontend(1, 1 if x.beta is not None else 0, ptr("A_log"), ptr("dt_bias")) if fe_on else None
+    north_star = args.entry == "chunk" and x.dtype == "bf16" and x.gate == "channel" and not fe_on
 
     def call():
         # kda_chunk_fwd (the spec symbol) when the workload fits its argument list,
         # else the struct entry points of the same ABI
-        if north_star:
+        if fe_on:
+            fn = lib.kda_recurrent_fwd_fused if args.entry == "recurrent" else lib.kda_chunk_fwd_fused
+            st = fn(ctypes.byref(params), ctypes.byref(fe), sh)
+        elif north_star:
             st = lib.kda_chunk_fwd(ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"),
                                    ptr("ht"), B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale,
                                    None if cu is None else cu.data_ptr(), sh)
@@ -339,9 +360,16 @@ def run_ours(args, world, rank, local, pg):
 
     peak, peak_kind = load_peaks()
     abytes = algorithmic_bytes(x)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kernel = "kda_recurrent_kernel" if args.entry == "recurrent" else forward_kernel(x, sms)
+    launches = 1
+    if fe_on and (args.frontend == "unfused" or (kernel != "kda_fwd_pc_kernel" and args.entry == "chunk")):
+        # the separate front-end pass: q and k norms, the gate, the beta sigmoid
+        launches += 3 + (1 if x.beta is not None else 0)
+        kernel = "front-end pass + " + kernel
     achieved = abytes / (ms / 1000.0) / 1e9
     src_hash = kernel_source_hash()
-    traffic = MEASURED_TRAFFIC.get((args.workload, src_hash))
+    traffic = MEASURED_TRAFFIC.get((args.workload, src_hash)) if args.frontend == "none" else None
     flops = algorithmic_flops(x)
 
     cpu = None
@@ -365,6 +393,7 @@ def run_ours(args, world, rank, local, pg):
                        "d_v": x.d_v, "C": 64 if args.entry == "chunk" else None, "entry": args.entry,
                        "gate": "per-channel" if x.gate == "channel" else "per-head",
                        "beta": x.beta is not None, "h0": x.h0 is not None, "ht": True,
+                       "frontend": args.frontend,
                        "global_batch": B * world, "seq_len": T if not x.varlen else x.T_total // B,
                        "parallelism": f"dp{world} (independent batches)",
                        "l2": f"inputs larger than L2 ({abytes / 1e6:.0f} MB per step), no flush"
@@ -374,12 +403,10 @@ def run_ours(args, world, rank, local, pg):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": abytes,
-                         "kernel": "kda_recurrent_kernel" if args.entry == "recurrent" else
-                         forward_kernel(x, torch.cuda.get_device_properties(dev).multi_processor_count),
-                         "tflops": flops / (ms / 1000.0) / 1e12},
+                         "kernel": kernel, "tflops": flops / (ms / 1000.0) / 1e12},
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches,
         }
         print(json.dumps(line), flush=True)
 
@@ -394,6 +421,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--entry", choices=["chunk", "recurrent"], default="chunk",
                     help="kda_chunk_fwd (default) or kda_recurrent_fwd (the token-by-token decode step)")
+    ap.add_argument("--frontend", choices=["none", "fused", "unfused"], default="none",
+                    help="raw q, k, gate pre-activations and beta logits through the front-end "
+                         "(q/k L2 norm, gated gate, beta sigmoid): applied inside the forward kernel "
+                         "where it can (fused) or as a separate pass (unfused)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # the timing rules ask for at least 3 warm-up steps
     world, rank, local, pg = dist_setup()

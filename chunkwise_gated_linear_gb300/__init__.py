@@ -8,11 +8,14 @@ from .kda import (  # noqa: F401
     kda_chunk_fwd,
     kda_chunk_fwd_ex,
     kda_chunk_fwd_f32,
+    kda_chunk_fwd_fused,
     kda_chunk_fwd_noalloc,
+    kda_frontend,
     kda_fwd_params,
     kda_get_device_error,
     kda_recurrent_fwd,
     kda_recurrent_fwd_ex,
+    kda_recurrent_fwd_fused,
     lib,
     status_string,
 )

@@ -15,6 +15,7 @@ cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched)
 cudaError_t launch_fwd_pc_static(const FwdArgs &a, cudaStream_t stream);
 int pc_static_max_units();
 cudaError_t launch_recurrent(const FwdArgs &a, bool f32, cudaStream_t stream);
+cudaError_t launch_frontend(const FwdArgs &a, bool f32, FwdArgs *out, void **scratch, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -56,7 +57,7 @@ int prepare(const kda_fwd_params &p, kda::FwdArgs &a) {
     if (p.T != 0 && (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr || p.o == nullptr))
         return KDA_ERR_INVALID_ARG;
     if (p.B < 1 || p.T < 0 || p.H_k < 1 || p.H_v < 1 || p.H_v % p.H_k != 0) return KDA_ERR_INVALID_ARG;
-    if ((p.flags & ~KDA_FLAG_ONE_CTA_PER_UNIT) != 0) return KDA_ERR_INVALID_ARG;
+    if ((p.flags & ~(KDA_FLAG_ONE_CTA_PER_UNIT | KDA_FLAG_UNFUSED_FRONTEND)) != 0) return KDA_ERR_INVALID_ARG;
     if (p.dtype != KDA_DTYPE_BF16 && p.dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (p.gate_mode != KDA_GATE_PER_CHANNEL && p.gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_UNSUPPORTED;
     if ((p.d_k != 64 && p.d_k != 128) || (p.d_v != 64 && p.d_v != 128) || p.C != kda::kChunk)
@@ -92,28 +93,91 @@ int prepare(const kda_fwd_params &p, kda::FwdArgs &a) {
     return KDA_OK;
 }
 
-int run(const kda_fwd_params &p, cudaStream_t stream) {
-    kda::FwdArgs a;
-    const int st = prepare(p, a);
-    if (st != KDA_OK) return st;
-    cudaError_t e = device_error_ptr(&a.err);
-    if (e == cudaSuccess) {
-        if (p.dtype == KDA_DTYPE_F32) {
-            e = kda::launch_fwd_f32(a, stream);
-        } else if (p.d_k == 128 && p.d_v == 128) {
-            // few units: the persistent producer/consumer kernel, else one CTA per unit
-            bool launched = false;
-            if (!(p.flags & KDA_FLAG_ONE_CTA_PER_UNIT)) e = kda::launch_fwd_pc(a, stream, &launched);
-            if (e == cudaSuccess && !launched) e = kda::launch_fwd_tc(a, stream);
-        } else {
-            e = kda::launch_fwd_bf16(a, stream);
-        }
+// Adds the front-end `fe` to resolved arguments; a status other than KDA_OK rejects the
+// call with nothing launched.
+int prepare_frontend(const kda_frontend *fe, kda::FwdArgs &a) {
+    if (fe == nullptr) return KDA_OK;
+    if (fe->dt_bias != nullptr && fe->A_log == nullptr) return KDA_ERR_INVALID_ARG;
+    if (fe->beta_sigmoid && a.beta == nullptr) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(fe->A_log) || !aligned16(fe->dt_bias)) return KDA_ERR_ALIGNMENT;
+    a.fe_qk_l2norm = fe->qk_l2norm ? 1 : 0;
+    a.fe_beta_sigmoid = fe->beta_sigmoid ? 1 : 0;
+    a.fe_A_log = fe->A_log;
+    a.fe_dt_bias = fe->dt_bias;
+    return KDA_OK;
+}
+
+// The forward kernels without a front-end (none of them reads the fe_* fields but the
+// persistent kernel, which applies them).
+cudaError_t dispatch(const kda_fwd_params &p, const kda::FwdArgs &a, cudaStream_t stream) {
+    if (p.dtype == KDA_DTYPE_F32) return kda::launch_fwd_f32(a, stream);
+    if (p.d_k == 128 && p.d_v == 128) {
+        // few units: the persistent producer/consumer kernel, else one CTA per unit
+        bool launched = false;
+        cudaError_t e = cudaSuccess;
+        if (!(p.flags & KDA_FLAG_ONE_CTA_PER_UNIT)) e = kda::launch_fwd_pc(a, stream, &launched);
+        if (e == cudaSuccess && !launched) e = kda::launch_fwd_tc(a, stream);
+        return e;
     }
+    return kda::launch_fwd_bf16(a, stream);
+}
+
+int status_of(cudaError_t e) {
     if (e != cudaSuccess) {
         t_last_cuda_error = e;
         return KDA_ERR_CUDA;
     }
     return KDA_OK;
+}
+
+int run(const kda_fwd_params &p, const kda_frontend *fe, cudaStream_t stream) {
+    kda::FwdArgs a;
+    int st = prepare(p, a);
+    if (st == KDA_OK) st = prepare_frontend(fe, a);
+    if (st != KDA_OK) return st;
+    cudaError_t e = device_error_ptr(&a.err);
+    if (e != cudaSuccess) return status_of(e);
+    if (!kda::fe_any(a)) return status_of(dispatch(p, a, stream));
+    // the persistent kernel applies the front-end itself when it takes the call
+    if (!(p.flags & (KDA_FLAG_UNFUSED_FRONTEND | KDA_FLAG_ONE_CTA_PER_UNIT)) && p.dtype == KDA_DTYPE_BF16 &&
+        p.d_k == 128 && p.d_v == 128) {
+        bool launched = false;
+        e = kda::launch_fwd_pc(a, stream, &launched);
+        if (e != cudaSuccess || launched) return status_of(e);
+    }
+    // otherwise a separate pass prepares the inputs in scratch
+    kda::FwdArgs b;
+    void *scratch = nullptr;
+    e = kda::launch_frontend(a, p.dtype == KDA_DTYPE_F32, &b, &scratch, stream);
+    if (e == cudaSuccess) e = dispatch(p, b, stream);
+    if (scratch != nullptr) {
+        const cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e == cudaSuccess) e = ef;
+    }
+    return status_of(e);
+}
+
+int run_recurrent(const kda_fwd_params *p, const kda_frontend *fe, cudaStream_t stream) {
+    if (p == nullptr) return KDA_ERR_INVALID_ARG;
+    kda_fwd_params r = *p;
+    r.C = kda::kChunk;  // no chunks: C is not used
+    kda::FwdArgs a;
+    int st = prepare(r, a);
+    if (st == KDA_OK) st = prepare_frontend(fe, a);
+    if (st != KDA_OK) return st;
+    cudaError_t e = device_error_ptr(&a.err);
+    if (e != cudaSuccess) return status_of(e);
+    const bool f32 = p->dtype == KDA_DTYPE_F32;
+    if (!kda::fe_any(a) || !(p->flags & KDA_FLAG_UNFUSED_FRONTEND)) return status_of(kda::launch_recurrent(a, f32, stream));
+    kda::FwdArgs b;
+    void *scratch = nullptr;
+    e = kda::launch_frontend(a, f32, &b, &scratch, stream);
+    if (e == cudaSuccess) e = kda::launch_recurrent(b, f32, stream);
+    if (scratch != nullptr) {
+        const cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e == cudaSuccess) e = ef;
+    }
+    return status_of(e);
 }
 
 }  // namespace
@@ -125,7 +189,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g, c
                   int C, float scale, const int32_t *cu_seqlens, cudaStream_t stream) {
     kda_fwd_params p{q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
                      KDA_DTYPE_BF16, KDA_GATE_PER_CHANNEL, 0};
-    return run(p, stream);
+    return run(p, nullptr, stream);
 }
 
 int kda_chunk_fwd_f32(const float *q, const float *k, const float *v, const float *g, const float *beta,
@@ -133,7 +197,7 @@ int kda_chunk_fwd_f32(const float *q, const float *k, const float *v, const floa
                       int d_v, int C, float scale, const int32_t *cu_seqlens, cudaStream_t stream) {
     kda_fwd_params p{q, k, v, g, beta, h0, o, ht, B, T, H_k, H_v, d_k, d_v, C, scale, cu_seqlens,
                      KDA_DTYPE_F32, KDA_GATE_PER_CHANNEL, 0};
-    return run(p, stream);
+    return run(p, nullptr, stream);
 }
 
 int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -160,20 +224,10 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
     return KDA_OK;
 }
 
-int kda_recurrent_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) {
-    if (p == nullptr) return KDA_ERR_INVALID_ARG;
-    kda_fwd_params r = *p;
-    r.C = kda::kChunk;  // no chunks: C is not used
-    kda::FwdArgs a;
-    const int st = prepare(r, a);
-    if (st != KDA_OK) return st;
-    cudaError_t e = device_error_ptr(&a.err);
-    if (e == cudaSuccess) e = kda::launch_recurrent(a, p->dtype == KDA_DTYPE_F32, stream);
-    if (e != cudaSuccess) {
-        t_last_cuda_error = e;
-        return KDA_ERR_CUDA;
-    }
-    return KDA_OK;
+int kda_recurrent_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) { return run_recurrent(p, nullptr, stream); }
+
+int kda_recurrent_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cudaStream_t stream) {
+    return run_recurrent(p, fe, stream);
 }
 
 int kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -186,7 +240,12 @@ int kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *
 
 int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) {
     if (p == nullptr) return KDA_ERR_INVALID_ARG;
-    return run(*p, stream);
+    return run(*p, nullptr, stream);
+}
+
+int kda_chunk_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cudaStream_t stream) {
+    if (p == nullptr) return KDA_ERR_INVALID_ARG;
+    return run(*p, fe, stream);
 }
 
 const char *kda_status_string(int status) {

@@ -29,7 +29,18 @@ struct FwdArgs {
     int gate_per_head;
     int decay_only;             // beta == nullptr: S <- Diag(a_t) S + k_t v_t^T (no erase)
     unsigned int *err;          // device error word of the current device (KDA_DEVICE_ERR_*)
+    // Fused front-end, read only by the kernels that apply it in their staging:
+    int fe_qk_l2norm;           // q, k divided per (token, key head) by sqrt(sum of squares + 1e-6)
+    int fe_beta_sigmoid;        // beta holds logits b: sigmoid(b) is used
+    const float *fe_A_log;      // non-null: g holds the pre-activation a, and
+                                //   g = -exp(A_log[h]) * softplus(a + dt_bias) is used
+    const float *fe_dt_bias;    // [H_v] (per-head gate) or [H_v][d_k] (per-channel), or null
 };
+
+// True when any part of the front-end is switched on.
+__host__ __device__ __forceinline__ bool fe_any(const FwdArgs &a) {
+    return a.fe_qk_l2norm || a.fe_beta_sigmoid || a.fe_A_log != nullptr;
+}
 
 // Sequence bounds of sequence n; returns false (and raises the error bit) when the
 // offsets are malformed.
@@ -94,5 +105,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- front-end arithmetic ("Gated DeltaNet": the model's gate and write strength, and the
+// recurrent kernel's in-kernel q/k normalisation), from CUDA's own expf / log1pf -----------
+constexpr float kL2NormEps = 1e-6f;  // added to the sum of squares, inside the square root
+
+// log(1 + e^x); above 20 the correction e^-x is below half an ulp of x
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+// 1 / (1 + e^-b)
+__device__ __forceinline__ float sigmoid_f(float b) { return 1.f / (1.f + expf(-b)); }
+// natural-log gate from the pre-activation: -exp(A_log) * softplus(a + dt_bias), with
+// negA = -exp(A_log) taken once per head
+__device__ __forceinline__ float gate_f(float negA, float a, float bias) { return negA * softplus_f(a + bias); }
+
+// Stream-ordered scratch: the library's memory pool of device `dev` (kept between calls).
+cudaError_t scratch_pool(int dev, cudaMemPool_t *out);
 
 }  // namespace kda

@@ -86,7 +86,8 @@ struct Prod {
     static constexpr int oGh1 = 217088;
     static constexpr int oTot = 217344;    // [4][128] fp32 partial gate sums
     static constexpr int oPS = 219392;     // solve scratch, 8 warps x 16x8 fp32
-    static constexpr int kEnd = oPS + 4096;
+    static constexpr int oRN = oPS + 4096; // front-end: scale / |q_t| [64], 1 / |k_t| [64]
+    static constexpr int kEnd = oRN + 512;
 };
 static_assert(Prod::oEG + 512 <= Prod::oKP0, "image overlaps");
 // Consumer shared memory.
@@ -275,16 +276,83 @@ __device__ __forceinline__ bool next_job(JobIt &it, const Ctx &x, const PcArgs &
     }
 }
 
+// ---- front-end arithmetic: one special-function op per value, the rest on the FMA pipe ----
+// log(1 + t) for t in [0, 1] as t P(t), P a degree-7 least-squares fit of log(1 + t) / t on
+// Chebyshev nodes of [0, 1] (fit_log1p.py beside this file; worst relative error 2.2e-7).
+__device__ __forceinline__ float log1p_01(float t) {
+    float p = -8.574675769e-03f;
+    p = fmaf(p, t, 4.421419278e-02f);
+    p = fmaf(p, t, -1.078536808e-01f);
+    p = fmaf(p, t, 1.775702387e-01f);
+    p = fmaf(p, t, -2.449961156e-01f);
+    p = fmaf(p, t, 3.327617645e-01f);
+    p = fmaf(p, t, -4.999744892e-01f);
+    p = fmaf(p, t, 9.999998212e-01f);
+    return p * t;
+}
+// softplus(x) = max(x, 0) + log(1 + e^-|x|), the exponential on the special-function unit
+__device__ __forceinline__ float softplus_fast(float x) { return fmaxf(x, 0.f) + log1p_01(ex2(-fabsf(x) * kLog2e)); }
+// 1 / (1 + e^-b)
+__device__ __forceinline__ float sigmoid_fast(float b) { return __fdividef(1.f, 1.f + ex2(-b * kLog2e)); }
+
 __device__ __forceinline__ unsigned char *slot_ptr(const PcArgs &pc, int u, int c) {
     return pc.ring + ((int64_t)u * pc.R + c % pc.R) * Slot::kStride;
+}
+
+// Front-end norms of the chunk's raw Q and K rows (64 each, row-major bf16, 256 B per row):
+// RN[t] = scale / sqrt(|q_t|^2 + 1e-6), RN[64 + t] = 1 / sqrt(|k_t|^2 + 1e-6). Warp w of the
+// 8 front warps sums rows 16 w .. 16 w + 15 of [Q; K]: in step i lane l reads the 16-byte
+// chunk l & 15 of row 2 i + (l >> 4) (a quarter-warp reads 128 contiguous bytes), then the
+// eight partial sums of each half-warp are reduced across its 16 lanes by halving, so that
+// lane l ends with the sum of row 2 (l >> 1 & 7) + (l >> 4).
+__device__ __forceinline__ void qk_row_norms(unsigned char *sm, int pw, int lane, float scale) {
+    const unsigned char *base = sm + (pw < 4 ? Prod::oRQ + pw * 4096 : Prod::oRK + (pw - 4) * 4096);
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(base + (2 * i + (lane >> 4)) * 256 + (lane & 15) * 16);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(ws[j] << 16), hi = __uint_as_float(ws[j] & 0xffff0000u);
+            acc = fmaf(lo, lo, acc);
+            acc = fmaf(hi, hi, acc);
+        }
+        v[i] = acc;
+    }
+    // halving: after the step across lane bit 3, v[k] is row index 4 b3 + k; bit 2: 4 b3 + 2 b2 + k;
+    // bit 1: 4 b3 + 2 b2 + b1; bit 0: both lanes of a pair hold the full sum
+    const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float send = b3 ? v[k] : v[k + 4], keep = b3 ? v[k + 4] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float send = b2 ? v[k] : v[k + 2], keep = b2 ? v[k + 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+        const float send = b1 ? v[0] : v[1], keep = b1 ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    if ((lane & 1) == 0) {
+        const int row = 16 * pw + 2 * ((lane >> 1) & 7) + (lane >> 4);  // 0..127 over [Q; K]
+        reinterpret_cast<float *>(sm + Prod::oRN)[row] = (pw < 4 ? scale : 1.f) * rsqrtf(v[0] + kL2NormEps);
+    }
 }
 
 // ---------------------------------------------------------------------------------------
 // producer, front stage (warps 0-7): tiles, gate pass, Gram; the front image of the slot
 // goes to the ring by one bulk store. Returns the TMA loads that may still be in flight
-// (abort path): bit 0 Q/K, bit 1 G; bits 4 and 5 their parities.
+// (abort path): bit 0 Q/K, bit 1 G; bits 4 and 5 their parities. With FE the front-end is
+// applied on the way: beta and the per-head gates as they land, the per-channel gates
+// before the cumulative sum, and the q / k norms as factors of the image rows.
 // ---------------------------------------------------------------------------------------
-template <bool GATE_HEAD>
+template <bool GATE_HEAD, bool FE>
 __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMaps &maps, const PcArgs &pc,
                                                    const Ctx &x) {
     unsigned char *sm = x.sm;
@@ -367,10 +435,35 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         JobIt nx = it;
         const bool have_next = next_job(nx, x, pc);
         const uint32_t oKP = b ? Prod::oKP1 : Prod::oKP0;
-        const float *Bf = reinterpret_cast<const float *>(sm + (b ? Prod::oBF1 : Prod::oBF0));
-        const float *Gh = reinterpret_cast<const float *>(sm + (b ? Prod::oGh1 : Prod::oGh0));
+        float *Bf = reinterpret_cast<float *>(sm + (b ? Prod::oBF1 : Prod::oBF0));
+        float *Gh = reinterpret_cast<float *>(sm + (b ? Prod::oGh1 : Prod::oGh0));
+        const int h = u % a.H_v;
+        // front-end: -exp(A_log[h]) and this thread's two channel biases
+        float negA = 0.f, bias0 = 0.f, bias1 = 0.f;
+        if constexpr (FE) {
+            if (a.fe_A_log != nullptr) {
+                negA = -expf(a.fe_A_log[h]);
+                if (a.fe_dt_bias != nullptr) {
+                    if constexpr (GATE_HEAD) {
+                        bias0 = a.fe_dt_bias[h];
+                    } else {
+                        const int cb = 64 * (pw & 1) + lane;
+                        bias0 = a.fe_dt_bias[h * 128 + cb];
+                        bias1 = a.fe_dt_bias[h * 128 + cb + 32];
+                    }
+                }
+            }
+        }
 
-        cp_async_wait_all();
+        cp_async_wait_all();  // this job's beta and per-head gates (own copies)
+        if constexpr (FE) {
+            // each thread transforms the values it loaded itself (rows past the end stay 0)
+            if (ptid < 64) {
+                if (a.fe_beta_sigmoid && !a.decay_only && ptid < nvalid) Bf[ptid] = sigmoid_fast(Bf[ptid]);
+            } else if (GATE_HEAD && ptid < 128 && a.fe_A_log != nullptr && ptid - 64 < nvalid) {
+                Gh[ptid - 64] = negA * softplus_fast(Gh[ptid - 64] + bias0);
+            }
+        }
         if constexpr (!GATE_HEAD) failed = !wait_bar(&bars[B_LG], (uint32_t)(jo & 1), x.flag, a, pc);
         if (bar_or(1, 256, failed)) { failed = true; break; }
         pend &= ~2u;
@@ -387,7 +480,30 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         const int qr = pw >> 1;
         const int c0 = 64 * (pw & 1) + lane, c1 = c0 + 32;
         float gl0[16], gl1[16];
-        {
+        bool gate_done = false;
+        if constexpr (!GATE_HEAD && FE) {
+            if (a.fe_A_log != nullptr) {
+                // every gate of the thread first (independent), then the running sums
+                const float nAl = negA * kLog2e;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = 16 * qr + e;
+                    const float v0 = nAl * softplus_fast(G[r * 128 + c0] + bias0);
+                    const float v1 = nAl * softplus_fast(G[r * 128 + c1] + bias1);
+                    gl0[e] = r < nvalid ? v0 : 0.f;
+                    gl1[e] = r < nvalid ? v1 : 0.f;
+                }
+#pragma unroll
+                for (int e = 1; e < 16; ++e) {
+                    gl0[e] += gl0[e - 1];
+                    gl1[e] += gl1[e - 1];
+                }
+                Tot[qr * 128 + c0] = gl0[15];
+                Tot[qr * 128 + c1] = gl1[15];
+                gate_done = true;
+            }
+        }
+        if (!gate_done) {
             float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -434,6 +550,12 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             }
             bar_named(1, 256);
         }
+        if constexpr (FE) {
+            if (a.fe_qk_l2norm) {
+                qk_row_norms(sm, pw, lane, a.scale);
+                bar_named(1, 256);
+            }
+        }
         {
             float off0 = 0.f, off1 = 0.f, gn0 = 0.f, gn1 = 0.f;
 #pragma unroll
@@ -454,6 +576,20 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int tc = 2 * qr + j;  // 16-byte chunk (8 tokens) of a 64-token row
+                // front-end: the factors of these 8 rows (q: scale / |q|, k: 1 / |k|)
+                float fq[8], fk[8];
+                if constexpr (FE) {
+                    const bool nrm = a.fe_qk_l2norm != 0;
+                    const float4 *RN4 = reinterpret_cast<const float4 *>(sm + Prod::oRN) + 4 * qr + 2 * j;
+                    const float4 q0 = nrm ? RN4[0] : make_float4(a.scale, a.scale, a.scale, a.scale);
+                    const float4 q1 = nrm ? RN4[1] : q0;
+                    const float4 k0 = nrm ? RN4[16] : make_float4(1.f, 1.f, 1.f, 1.f);
+                    const float4 k1 = nrm ? RN4[17] : k0;
+                    fq[0] = q0.x; fq[1] = q0.y; fq[2] = q0.z; fq[3] = q0.w;
+                    fq[4] = q1.x; fq[5] = q1.y; fq[6] = q1.z; fq[7] = q1.w;
+                    fk[0] = k0.x; fk[1] = k0.y; fk[2] = k0.z; fk[3] = k0.w;
+                    fk[4] = k1.x; fk[5] = k1.y; fk[6] = k1.z; fk[7] = k1.w;
+                }
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     const int cc = ch ? c1 : c0;
@@ -464,11 +600,16 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
                         const int r = 16 * qr + 8 * j + e;
                         const float gm = off + (ch ? gl1[8 * j + e] : gl0[8 * j + e]);
                         const float ep = ex2(gm), em = ex2(-gm);
-                        const float kv = __bfloat162float(RK[r * 128 + cc]);
+                        float kv = __bfloat162float(RK[r * 128 + cc]);
                         const float qv = __bfloat162float(RQ[r * 128 + cc]);
+                        float qs = a.scale;
+                        if constexpr (FE) {
+                            qs = fq[e];
+                            kv *= fk[e];
+                        }
                         kp[e] = a.decay_only ? 0.f : kv * ep;
                         km[e] = kv * em;
-                        qp[e] = a.scale * qv * ep;
+                        qp[e] = qs * qv * ep;
                         kb[e] = km[e] * eg;
                     }
                     const uint32_t sw = sw128(cc, tc);
@@ -545,6 +686,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         it = nx;
         have = have_next;
     }
+    cp_async_wait_all();  // no copy into shared memory outlives the loop
     if (failed) {
         *x.flag = 1;
     } else if (ptid == kIssImg && jo > 0) {
@@ -1024,7 +1166,7 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
     }
 }
 
-template <bool GATE_HEAD>
+template <bool GATE_HEAD, bool FE>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_fwd_pc_kernel(const FwdArgs a, const __grid_constant__ TcMaps maps, const PcArgs pc) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1104,7 +1246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend_load = consumer_loader(a, pc, x, u, units[u].nch);
         }
     } else if (tid < 256) {
-        pend_front = producer_front<GATE_HEAD>(a, maps, pc, x);
+        pend_front = producer_front<GATE_HEAD, FE>(a, maps, pc, x);
     } else {
         pend_back = producer_back(a, maps, pc, x);
     }
@@ -1141,11 +1283,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Stream-ordered scratch (ring and flags) from a pool owned by the library, one per
-// device, that keeps its memory between calls.
+}  // namespace
+
+// Stream-ordered scratch (the ring and flags here, the front-end's prepared tensors) from a
+// pool owned by the library, one per device, that keeps its memory between calls.
+namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_pool_mu;
 cudaMemPool_t g_pool[kMaxDevices] = {};
+}  // namespace
 
 cudaError_t scratch_pool(int dev, cudaMemPool_t *out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -1171,7 +1317,9 @@ cudaError_t scratch_pool(int dev, cudaMemPool_t *out) {
     return cudaSuccess;
 }
 
-template <bool GATE_HEAD>
+namespace {
+
+template <bool GATE_HEAD, bool FE>
 cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     *launched = false;
     int dev = 0, sms = 0, coop = 0;
@@ -1182,7 +1330,7 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     const int64_t U = (int64_t)a.N * a.H_v;
     // worth it only when the units leave at least as many SMs idle as they occupy
     if (!coop || U < 1 || U > kMaxUnits || 2 * U > sms) return cudaSuccess;
-    auto kern = kda_fwd_pc_kernel<GATE_HEAD>;
+    auto kern = kda_fwd_pc_kernel<GATE_HEAD, FE>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Common::kBytes);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -1261,7 +1409,7 @@ cudaError_t launch_pc_static(const FwdArgs &a, cudaStream_t stream) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     if (e != cudaSuccess) return e;
     if (!coop || 2 * U > sms) return cudaErrorNotSupported;
-    auto kern = kda_fwd_pc_kernel<GATE_HEAD>;
+    auto kern = kda_fwd_pc_kernel<GATE_HEAD, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Common::kBytes);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -1295,9 +1443,12 @@ cudaError_t launch_pc_static(const FwdArgs &a, cudaStream_t stream) {
 }  // namespace
 
 // The persistent kernel when the call has at most half as many units as the device has
-// SMs; *launched tells whether it ran (otherwise nothing was launched).
+// SMs; *launched tells whether it ran (otherwise nothing was launched). The front-end
+// parts that `a` switches on are applied inside the kernel.
 cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
-    return a.gate_per_head ? launch_pc<true>(a, stream, launched) : launch_pc<false>(a, stream, launched);
+    if (fe_any(a))
+        return a.gate_per_head ? launch_pc<true, true>(a, stream, launched) : launch_pc<false, true>(a, stream, launched);
+    return a.gate_per_head ? launch_pc<true, false>(a, stream, launched) : launch_pc<false, false>(a, stream, launched);
 }
 
 // The same kernel with its scratch in g_static_scratch (nothing allocated). Returns

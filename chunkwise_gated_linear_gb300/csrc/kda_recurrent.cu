@@ -12,6 +12,11 @@
 // so each reduction over d is a sum over the thread's rows and two shuffles. The next
 // token's q, k, exp(g), v and beta are staged in shared memory (double-buffered) while
 // the current one is computed.
+//
+// The front-end ("Gated DeltaNet", "Recurrent 算法代码解析") is applied while staging when
+// switched on: q and k enter as x / sqrt(sum x^2 + 1e-6) — kept as the raw values and two
+// per-token factors, from per-warp partial sums of squares reduced after the staging
+// barrier — beta as sigmoid(b), and g as -exp(A_log) * softplus(a + dt_bias).
 #include "kda_common.cuh"
 
 namespace kda {
@@ -44,7 +49,9 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
 template <int DK, typename T, bool GATE_HEAD>
 __global__ void __launch_bounds__(128) kda_recurrent_kernel(const FwdArgs a) {
     constexpr int R = DK / 4;  // rows of S per thread
+    constexpr int NW = DK / 32;  // warps that stage q and k
     __shared__ float sq[2][DK], sk[2][DK], sa[2][DK], sv[2][kSlice], sb[2];
+    __shared__ float sn[2][NW][2];  // per-warp sums of squares of q and k (front-end norm)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j = 8 * warp + (lane >> 2), qd = lane & 3;  // column of the slice, row phase
@@ -60,19 +67,44 @@ __global__ void __launch_bounds__(128) kda_recurrent_kernel(const FwdArgs a) {
     T *o = static_cast<T *>(a.o);
     const int64_t sqk = (int64_t)a.H_k * DK, sv_ = (int64_t)a.H_v * a.d_v;
     const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * DK;
+    // front-end constants of this head: -exp(A_log[h]) and this thread's dt_bias
+    const bool fe_norm = a.fe_qk_l2norm != 0, fe_gate = a.fe_A_log != nullptr;
+    const float negA = fe_gate ? -expf(a.fe_A_log[h]) : 0.f;
+    const float bias = (fe_gate && a.fe_dt_bias != nullptr)
+                           ? a.fe_dt_bias[GATE_HEAD ? (int64_t)h : (int64_t)h * DK + (tid < DK ? tid : 0)]
+                           : 0.f;
 
     // stage token t into buffer t & 1
     auto stage = [&](int t) {
         const int bsel = t & 1;
         const int64_t row = bos + t;
-        if (tid < DK) {
-            sq[bsel][tid] = to_f32<T>(q[row * sqk + (int64_t)hk * DK + tid]);
-            sk[bsel][tid] = to_f32<T>(k[row * sqk + (int64_t)hk * DK + tid]);
-            const float gv = GATE_HEAD ? a.g[row * sg + h] : a.g[row * sg + (int64_t)h * DK + tid];
+        if (tid < DK) {  // whole warps (DK is a multiple of 32)
+            const float qv = to_f32<T>(q[row * sqk + (int64_t)hk * DK + tid]);
+            const float kv = to_f32<T>(k[row * sqk + (int64_t)hk * DK + tid]);
+            sq[bsel][tid] = qv;
+            sk[bsel][tid] = kv;
+            float gv = GATE_HEAD ? a.g[row * sg + h] : a.g[row * sg + (int64_t)h * DK + tid];
+            if (fe_gate) gv = gate_f(negA, gv, bias);
             sa[bsel][tid] = exp2f(gv * kLog2e);
+            if (fe_norm) {
+                float ssq = qv * qv, ssk = kv * kv;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+                    ssk += __shfl_xor_sync(0xffffffffu, ssk, o);
+                }
+                if (lane == 0) {
+                    sn[bsel][warp][0] = ssq;
+                    sn[bsel][warp][1] = ssk;
+                }
+            }
         }
         if (tid < kSlice) sv[bsel][tid] = to_f32<T>(v[row * sv_ + (int64_t)h * a.d_v + dv0 + tid]);
-        if (tid == 0) sb[bsel] = a.decay_only ? 1.f : a.beta[row * a.H_v + h];
+        if (tid == 0) {
+            float bv = a.decay_only ? 1.f : a.beta[row * a.H_v + h];
+            if (a.fe_beta_sigmoid && !a.decay_only) bv = sigmoid_f(bv);
+            sb[bsel] = bv;
+        }
     };
 
     // S[:, j] rows qd, qd + 4, ... (from h0, or zero)
@@ -87,6 +119,18 @@ __global__ void __launch_bounds__(128) kda_recurrent_kernel(const FwdArgs a) {
         const int bsel = t & 1;
         if (t + 1 < len) stage(t + 1);  // the other buffer, read by no thread now
         const float *cq = sq[bsel], *ck = sk[bsel], *ca = sa[bsel];
+        // the normalised q and k are the staged ones times rq and rk
+        float rq = 1.f, rk = 1.f;
+        if (fe_norm) {
+            float nq = 0.f, nk = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                nq += sn[bsel][w][0];
+                nk += sn[bsel][w][1];
+            }
+            rq = rsqrtf(nq + kL2NormEps);
+            rk = rsqrtf(nk + kL2NormEps);
+        }
         // decay, then the erase read S^T k
         float dot = 0.f;
 #pragma unroll
@@ -97,7 +141,8 @@ __global__ void __launch_bounds__(128) kda_recurrent_kernel(const FwdArgs a) {
         }
         dot += __shfl_xor_sync(0xffffffffu, dot, 1);
         dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-        const float u = a.decay_only ? sv[bsel][j] : sb[bsel] * (sv[bsel][j] - dot);
+        // u scaled by rk once more: the write is k u^T with k = rk * (staged k)
+        const float u = rk * (a.decay_only ? sv[bsel][j] : sb[bsel] * (sv[bsel][j] - rk * dot));
         // write, then the output read S^T q
         float oq = 0.f;
 #pragma unroll
@@ -108,7 +153,7 @@ __global__ void __launch_bounds__(128) kda_recurrent_kernel(const FwdArgs a) {
         }
         oq += __shfl_xor_sync(0xffffffffu, oq, 1);
         oq += __shfl_xor_sync(0xffffffffu, oq, 2);
-        if (qd == 0) o[(bos + t) * sv_ + (int64_t)h * a.d_v + dv0 + j] = from_f32<T>(a.scale * oq);
+        if (qd == 0) o[(bos + t) * sv_ + (int64_t)h * a.d_v + dv0 + j] = from_f32<T>(a.scale * rq * oq);
         __syncthreads();  // buffer t & 1 is free; token t + 1 is staged
     }
     if (a.ht != nullptr) {

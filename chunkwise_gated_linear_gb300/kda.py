@@ -25,12 +25,13 @@ KDA_DTYPE_F32 = 1
 KDA_GATE_PER_CHANNEL = 0
 KDA_GATE_PER_HEAD = 1
 KDA_FLAG_ONE_CTA_PER_UNIT = 1
+KDA_FLAG_UNFUSED_FRONTEND = 2
 KDA_DEVICE_ERR_SEQLENS = 1
 KDA_DEVICE_ERR_TIMEOUT = 2
 
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_ex", "kda_status_string",
             "kda_get_device_error", "kda_chunk_fwd_noalloc", "kda_recurrent_fwd",
-            "kda_recurrent_fwd_ex")
+            "kda_recurrent_fwd_ex", "kda_chunk_fwd_fused", "kda_recurrent_fwd_fused")
 
 
 class KdaError(RuntimeError):
@@ -48,6 +49,13 @@ class kda_fwd_params(ctypes.Structure):
         ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("C", ctypes.c_int),
         ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p),
         ("dtype", ctypes.c_int), ("gate_mode", ctypes.c_int), ("flags", ctypes.c_int),
+    ]
+
+
+class kda_frontend(ctypes.Structure):
+    _fields_ = [
+        ("qk_l2norm", ctypes.c_int), ("beta_sigmoid", ctypes.c_int),
+        ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
     ]
 
 
@@ -78,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.kda_recurrent_fwd.restype = I
         L.kda_recurrent_fwd_ex.argtypes = [ctypes.POINTER(kda_fwd_params), P]
         L.kda_recurrent_fwd_ex.restype = I
+        for name in ("kda_chunk_fwd_fused", "kda_recurrent_fwd_fused"):
+            fn = getattr(L, name)
+            fn.argtypes = [ctypes.POINTER(kda_fwd_params), ctypes.POINTER(kda_frontend), P]
+            fn.restype = I
         L.kda_status_string.argtypes = [I]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_get_device_error.argtypes = [P]
@@ -124,6 +136,16 @@ def kda_recurrent_fwd_ex(params: kda_fwd_params, stream) -> int:
     return lib().kda_recurrent_fwd_ex(ctypes.byref(params), stream or None)
 
 
+def kda_chunk_fwd_fused(params: kda_fwd_params, fe: kda_frontend | None, stream) -> int:
+    return lib().kda_chunk_fwd_fused(ctypes.byref(params), None if fe is None else ctypes.byref(fe),
+                                     stream or None)
+
+
+def kda_recurrent_fwd_fused(params: kda_fwd_params, fe: kda_frontend | None, stream) -> int:
+    return lib().kda_recurrent_fwd_fused(ctypes.byref(params), None if fe is None else ctypes.byref(fe),
+                                         stream or None)
+
+
 def kda_get_device_error(stream) -> int:
     return lib().kda_get_device_error(stream or None)
 
@@ -136,7 +158,8 @@ def _ptr(t):
 
 def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
                   output_final_state=True, chunk_size=64, o=None, ht=None, stream=None,
-                  one_cta_per_unit=False, recurrent=False):
+                  one_cta_per_unit=False, recurrent=False, qk_l2norm=False, beta_sigmoid=False,
+                  A_log=None, dt_bias=None, unfused_frontend=False):
     """Chunkwise KDA forward on torch CUDA tensors; returns ``(o, ht)``.
 
     q, k [B, T, H_k, d_k] and v [B, T, H_v, d_v], all bf16 or all fp32; g fp32
@@ -148,6 +171,13 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
     ``output_final_state`` is False. ``one_cta_per_unit`` sets KDA_FLAG_ONE_CTA_PER_UNIT
     (never the persistent kernel that occupies every SM). ``recurrent`` computes token by
     token (kda_recurrent_fwd_ex: the decode step; ``ht`` may then be ``h0`` itself).
+
+    Front-end (kda_chunk_fwd_fused / kda_recurrent_fwd_fused): ``qk_l2norm`` normalises q
+    and k per token and head in the kernel (eps 1e-6 inside the square root);
+    ``beta_sigmoid`` takes ``beta`` as logits; ``A_log`` (fp32 [H_v]) takes ``g`` as the
+    gate pre-activation a and uses g = -exp(A_log) * softplus(a + dt_bias), with
+    ``dt_bias`` fp32 [H_v] (per-head gate) or [H_v, d_k] (per-channel) or None.
+    ``unfused_frontend`` runs the front-end as a separate pass (for comparison).
     """
     import torch
 
@@ -175,7 +205,15 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
         raise ValueError("g must be [B, T, H_v, d_k] or [B, T, H_v]")
     if beta is not None and beta.shape != (B, T, H_v):
         raise ValueError("beta must be [B, T, H_v] (or None: the decay-only recurrence)")
-    for t in (q, k, v, g, beta, h0, cu_seqlens):
+    if dt_bias is not None and A_log is None:
+        raise ValueError("dt_bias needs A_log")
+    if A_log is not None:
+        if A_log.dtype != torch.float32 or tuple(A_log.shape) != (H_v,):
+            raise ValueError("A_log must be fp32 [H_v]")
+        want = (H_v, d_k) if gate == KDA_GATE_PER_CHANNEL else (H_v,)
+        if dt_bias is not None and (dt_bias.dtype != torch.float32 or tuple(dt_bias.shape) != want):
+            raise ValueError(f"dt_bias must be fp32 {list(want)}")
+    for t in (q, k, v, g, beta, h0, cu_seqlens, A_log, dt_bias):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("every tensor must be a contiguous CUDA tensor")
     if cu_seqlens is not None:
@@ -203,12 +241,19 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
     p = kda_fwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta) or None, _ptr(h0) or None, _ptr(o),
                        _ptr(ht) or None, nb, nt, H_k, H_v, d_k, d_v, chunk_size, float(scale),
                        _ptr(cu_seqlens) or None, dtype, gate,
-                       KDA_FLAG_ONE_CTA_PER_UNIT if one_cta_per_unit else 0)
+                       (KDA_FLAG_ONE_CTA_PER_UNIT if one_cta_per_unit else 0)
+                       | (KDA_FLAG_UNFUSED_FRONTEND if unfused_frontend else 0))
+    fused = qk_l2norm or beta_sigmoid or A_log is not None
     if recurrent:
-        p.flags = 0
-        st = kda_recurrent_fwd_ex(p, stream)
+        p.flags &= ~KDA_FLAG_ONE_CTA_PER_UNIT
+    if fused:
+        fe = kda_frontend(1 if qk_l2norm else 0, 1 if beta_sigmoid else 0, _ptr(A_log) or None,
+                          _ptr(dt_bias) or None)
+        name = "kda_recurrent_fwd_fused" if recurrent else "kda_chunk_fwd_fused"
+        st = (kda_recurrent_fwd_fused if recurrent else kda_chunk_fwd_fused)(p, fe, stream)
     else:
-        st = kda_chunk_fwd_ex(p, stream)
+        name = "kda_recurrent_fwd_ex" if recurrent else "kda_chunk_fwd_ex"
+        st = (kda_recurrent_fwd_ex if recurrent else kda_chunk_fwd_ex)(p, stream)
     if st != KDA_OK:
-        raise KdaError(st, "kda_recurrent_fwd_ex" if recurrent else "kda_chunk_fwd_ex")
+        raise KdaError(st, name)
     return o, ht

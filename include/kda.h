@@ -121,7 +121,7 @@ typedef struct kda_fwd_params {
     const int32_t *cu_seqlens;
     int dtype;     /* KDA_DTYPE_BF16 or KDA_DTYPE_F32 */
     int gate_mode; /* KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD */
-    int flags;     /* 0 or KDA_FLAG_ONE_CTA_PER_UNIT */
+    int flags;     /* 0, or KDA_FLAG_ONE_CTA_PER_UNIT and / or KDA_FLAG_UNFUSED_FRONTEND */
 } kda_fwd_params;
 
 /*
@@ -135,6 +135,10 @@ typedef struct kda_fwd_params {
  * the other SMs free for concurrent work. Both give the same result up to rounding.
  */
 #define KDA_FLAG_ONE_CTA_PER_UNIT 1
+/* With a front-end (kda_chunk_fwd_fused, kda_recurrent_fwd_fused): run it as a separate
+ * pass into scratch even where the selected kernel can apply it itself (for comparison;
+ * the result agrees up to rounding). Ignored by the other entry points. */
+#define KDA_FLAG_UNFUSED_FRONTEND 2
 
 /*
  * kda_chunk_fwd_ex — the general entry point: dtype and gate mode chosen by the struct.
@@ -182,6 +186,49 @@ int kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *
 
 /* kda_recurrent_fwd with the dtype and gate mode of the struct (its C is ignored). */
 int kda_recurrent_fwd_ex(const kda_fwd_params *p, cudaStream_t stream);
+
+/*
+ * The fused front-end: the per-token preparation that the Gated DeltaNet model applies to
+ * its projections before the recurrence ("Gated DeltaNet", section "模型调用方式：Qwen3.5
+ * GatedDeltaNet", and the recurrent kernel's in-kernel variants in "Recurrent 算法代码解析").
+ * Each part is independent; a zeroed struct switches everything off.
+ *
+ *   qk_l2norm     nonzero: q and k are divided, per (token, key head), by
+ *                 sqrt(sum over d_k of x^2 + 1e-6) before use; the scale then multiplies
+ *                 the normalised q.
+ *   beta_sigmoid  nonzero: the beta tensor holds logits b and beta = 1 / (1 + exp(-b)) is
+ *                 used. Requires beta != NULL.
+ *   A_log         non-NULL: the g tensor holds the gate pre-activation a (same layout as g)
+ *                 and the log gate g = -exp(A_log[h]) * softplus(a + dt_bias) is used.
+ *                 A_log: [H_v] fp32, device, 16-byte aligned.
+ *   dt_bias       with A_log: [H_v] fp32 (per-head gate) or [H_v, d_k] fp32 (per-channel
+ *                 gate: one bias per value head and channel), device, 16-byte aligned; NULL
+ *                 means no bias. Must be NULL when A_log is NULL.
+ *
+ * The input tensors are only read; nothing is written back to them.
+ */
+typedef struct kda_frontend {
+    int qk_l2norm;
+    int beta_sigmoid;
+    const float *A_log;
+    const float *dt_bias;
+} kda_frontend;
+
+/*
+ * kda_chunk_fwd_fused — kda_chunk_fwd_ex with the front-end `fe` applied to its inputs
+ * (fe == NULL: exactly kda_chunk_fwd_ex). The persistent kernel (bf16, d_k = d_v = 128, few
+ * units) applies it while staging each chunk, so q, k, g and beta are read once; the other
+ * kernels get it as a separate pass that writes the prepared q and k (in the input dtype),
+ * g and beta (fp32) to stream-ordered scratch from the library's pool (freed on the same
+ * stream), about 2 * T * H_k * d_k * elem + T * H_v * (d_k or 1) * 4 + T * H_v * 4 bytes.
+ * Errors as kda_chunk_fwd_ex, and KDA_ERR_INVALID_ARG for beta_sigmoid with beta == NULL or
+ * dt_bias without A_log, KDA_ERR_ALIGNMENT for A_log or dt_bias not 16-byte aligned.
+ */
+int kda_chunk_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cudaStream_t stream);
+
+/* kda_recurrent_fwd_ex with the front-end `fe` (applied inside the recurrent kernel, or as a
+ * separate pass with KDA_FLAG_UNFUSED_FRONTEND). */
+int kda_recurrent_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cudaStream_t stream);
 
 /* A static, human-readable description of a status (and of the last CUDA error for
  * KDA_ERR_CUDA on this thread). */

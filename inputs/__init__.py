@@ -6,4 +6,4 @@ gates, applies sigmoid to the beta logits and rounds to the storage dtype.
 """
 
 from .synth import (WORKLOADS, FrontendInputs, Inputs, Workload, make_frontend_inputs,  # noqa: F401
-                    make_inputs, workload_inputs)
+                    make_inputs, workload_frontend_inputs, workload_inputs)

@@ -291,3 +291,19 @@ def workload_inputs(name: str, seed: int | None = None) -> Inputs:
                     len_range=w.len_range, n_seqs=w.n_seqs)
     x.meta["workload"] = name
     return x
+
+
+def workload_frontend_inputs(name: str, seed: int | None = None) -> FrontendInputs:
+    """Raw front-end inputs with the shape of one named workload (its gate mode, beta and
+    h0 choices): every front-end part switched on."""
+    w = WORKLOADS[name] if name in WORKLOADS else PROFILE_WORKLOADS[name]
+    if w.len_range is not None:
+        lengths = tuple(int(v) for v in np.random.default_rng(WORKLOAD_SEEDS.get(name, 99))
+                        .integers(w.len_range[0], w.len_range[1] + 1, size=w.n_seqs))
+    else:
+        lengths = w.lengths
+    s = WORKLOAD_SEEDS.get(name, 99) if seed is None else seed
+    x = make_frontend_inputs(lengths, w.H_k, w.H_v, w.d_k, w.d_v, dtype=w.dtype, gate=w.gate, h0=w.h0,
+                             beta=w.beta, varlen=w.varlen, seed=s)
+    x.meta["workload"] = name
+    return x

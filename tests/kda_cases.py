@@ -55,3 +55,25 @@ def run_oracle(x: Inputs, units=None):
     from oracle import kda_recurrence
 
     return kda_recurrence(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, x.scale, units=units)
+
+
+def run_gpu_fe(x, d=None, **kw):
+    """run_gpu for front-end inputs (:class:`inputs.FrontendInputs`): the raw q, k, a and b
+    go in with the front-end switched on as the inputs say."""
+    import torch
+
+    if d is None:
+        d = to_device(x)
+    dev = d["q"].device
+    A_log = None if x.A_log is None else torch.from_numpy(x.A_log).to(dev).contiguous()
+    dt_bias = None if x.dt_bias is None else torch.from_numpy(x.dt_bias).to(dev).contiguous()
+    return run_gpu(x, d, qk_l2norm=x.qk_l2norm, beta_sigmoid=x.beta_sigmoid, A_log=A_log,
+                   dt_bias=dt_bias, **kw)
+
+
+def run_oracle_fe(x, units=None):
+    from oracle import kda_fused_recurrence
+
+    return kda_fused_recurrence(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, x.scale,
+                                qk_l2norm=x.qk_l2norm, beta_sigmoid=x.beta_sigmoid, A_log=x.A_log,
+                                dt_bias=x.dt_bias, units=units)

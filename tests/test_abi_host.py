@@ -72,9 +72,9 @@ def test_bad_arguments_are_rejected(over, want):
 
 def test_ex_rejects_unknown_modes_and_flags():
     p = kda.kda_fwd_params(A, A, A, A, A, None, A, None, 1, 64, 1, 1, 128, 128, 64, 1.0, None,
-                           kda.KDA_DTYPE_BF16, kda.KDA_GATE_PER_CHANNEL, 2)
+                           kda.KDA_DTYPE_BF16, kda.KDA_GATE_PER_CHANNEL, 8)
     assert kda.kda_chunk_fwd_ex(p, 0) == kda.KDA_ERR_INVALID_ARG
-    p.flags = kda.KDA_FLAG_ONE_CTA_PER_UNIT | 4
+    p.flags = kda.KDA_FLAG_ONE_CTA_PER_UNIT | kda.KDA_FLAG_UNFUSED_FRONTEND | 4
     assert kda.kda_chunk_fwd_ex(p, 0) == kda.KDA_ERR_INVALID_ARG
     p.flags = 0
     p.dtype = 7
@@ -96,3 +96,24 @@ def test_noalloc_rejects_what_its_scratch_cannot_hold():
     assert kda.kda_chunk_fwd_noalloc(**args) == kda.KDA_ERR_UNSUPPORTED
     args.update(d_k=128, q=0)
     assert kda.kda_chunk_fwd_noalloc(**args) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_fused_front_end_rejections():
+    # all checked on the host before any CUDA call
+    p = kda.kda_fwd_params(A, A, A, A, A, None, A, None, 1, 64, 1, 1, 128, 128, 64, 1.0, None,
+                           kda.KDA_DTYPE_BF16, kda.KDA_GATE_PER_CHANNEL, 0)
+    for fn in (kda.kda_chunk_fwd_fused, kda.kda_recurrent_fwd_fused):
+        # dt_bias without A_log
+        assert fn(p, kda.kda_frontend(0, 0, None, A), 0) == kda.KDA_ERR_INVALID_ARG
+        # misaligned gate parameters
+        assert fn(p, kda.kda_frontend(0, 0, A + 4, None), 0) == kda.KDA_ERR_ALIGNMENT
+        assert fn(p, kda.kda_frontend(0, 0, A, A + 8), 0) == kda.KDA_ERR_ALIGNMENT
+        # beta logits without beta
+        p.beta = None
+        assert fn(p, kda.kda_frontend(0, 1, None, None), 0) == kda.KDA_ERR_INVALID_ARG
+        p.beta = A
+        # the base checks still apply
+        p.d_k = 96
+        assert fn(p, kda.kda_frontend(1, 1, A, A), 0) == kda.KDA_ERR_UNSUPPORTED
+        p.d_k = 128
+    assert kda.lib().kda_chunk_fwd_fused(None, None, None) == kda.KDA_ERR_INVALID_ARG
