@@ -18,7 +18,6 @@ from __future__ import annotations
 
 import argparse
 import ctypes
-import glob
 import hashlib
 import json
 import os
@@ -35,20 +34,29 @@ WORKLOAD = "kda_b2_t8192_h32_d128_bf16"
 METRIC = "chunk KDA fwd tokens/s at T=8192,H=32,d=128 bf16; % of roofline"
 
 # DRAM traffic per launch of the forward kernel, from an ncu capture of this workload
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of the kernel sources
-# it was taken on; any change to the sources makes the figure stale (reported as null).
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of the sources of the
+# kernel it was taken on; any change to them makes the figure stale (reported as null).
 MEASURED_TRAFFIC = {
-    # profiles/kda_fwd_pc_b2_t8192_h32_d128.md: 394.20 MB on the half-size case (32 units),
-    # scaled by 2 to the 64 units of this workload
-    ("kda_b2_t8192_h32_d128_bf16", "68bfe8f3e5ec43cb"): 788_400_000,
+    # profiles/kda_fwd_pc_b2_t8192_h32_d128.md: 493.2 MB on the same 64 units over half the
+    # tokens (B=2, T=4096), scaled by 2 to this workload
+    ("kda_b2_t8192_h32_d128_bf16", "5d316c9d64e48314"): 986_400_000,
+}
+
+# The translation unit of each forward kernel and the headers it includes.
+KERNEL_SOURCES = {
+    "kda_fwd_pc_kernel": ("kda_fwd_pc.cu", "kda_common.cuh", "tc_util.cuh", "tc5.cuh"),
+    "kda_fwd_tc_kernel": ("kda_fwd_tc.cu", "kda_common.cuh", "tc_util.cuh", "tc5.cuh"),
+    "kda_fwd_bf16_kernel": ("kda_fwd_bf16.cu", "kda_common.cuh"),
+    "kda_fwd_f32_kernel": ("kda_fwd_f32.cu", "kda_common.cuh"),
+    "kda_recurrent_kernel": ("kda_recurrent.cu", "kda_common.cuh"),
 }
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "kda_fwd_pc_kernel") -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "chunkwise_gated_linear_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "chunkwise_gated_linear_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -368,8 +376,9 @@ def run_ours(args, world, rank, local, pg):
         launches += 3 + (1 if x.beta is not None else 0)
         kernel = "front-end pass + " + kernel
     achieved = abytes / (ms / 1000.0) / 1e9
-    src_hash = kernel_source_hash()
-    traffic = MEASURED_TRAFFIC.get((args.workload, src_hash)) if args.frontend == "none" else None
+    traffic = None
+    if args.frontend == "none" and kernel in KERNEL_SOURCES:
+        traffic = MEASURED_TRAFFIC.get((args.workload, kernel_source_hash(kernel)))
     flops = algorithmic_flops(x)
 
     cpu = None
