@@ -8,6 +8,8 @@ may import this package. It shares no code with the CUDA path and never imports 
 * :func:`kda_chunked` — the chunkwise restatement of the same result in fp64 numpy
   (``chunked.py``), following the per-chunk steps the pages give, used to pin the chunk
   algebra against the definition.
+* :func:`kda_recurrence_bwd` — the backward pass: reverse-mode differentiation of the
+  token recurrence in fp64 C (``kda_oracle_bwd.c``).
 * :func:`kda_fused_recurrence` — the front-end (q/k L2 norm, beta sigmoid, the Gated
   DeltaNet gate; ``frontend.py``) followed by the recurrence.
 """
@@ -15,3 +17,4 @@ may import this package. It shares no code with the CUDA path and never imports 
 from .recurrence import kda_recurrence, oracle_threads  # noqa: F401
 from .chunked import kda_chunked, separable_gram, naive_gram  # noqa: F401
 from .frontend import kda_fused_recurrence  # noqa: F401
+from .backward import kda_recurrence_bwd  # noqa: F401
