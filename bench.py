@@ -76,6 +76,33 @@ def algorithmic_bytes(x) -> int:
     return T * per_tok + state + params
 
 
+def backward_bytes(x) -> int:
+    """HBM bytes the backward must move: the forward inputs (q, k, v, g, beta, h0), dO and
+    dht in; dq, dk, dv, dg, dbeta and dh0 out."""
+    e = 2 if x.dtype == "bf16" else 4
+    gate = 4 * x.d_k if x.gate == "channel" else 4
+    bet = 8 if x.beta is not None else 0  # beta in, dbeta out
+    per_tok = x.H_k * 4 * x.d_k * e + x.H_v * (3 * x.d_v * e + 2 * gate + bet)
+    state = x.N * x.H_v * 4 * x.d_k * x.d_v * ((x.h0 is not None) + 2)  # h0, dht, dh0
+    return x.T_total * per_tok + state
+
+
+def backward_flops(x, C=64) -> int:
+    """fp32 FLOPs of the backward's contractions as this library runs them, per (chunk,
+    value head): the recomputed chunk factors (Gram, Aqk, U, W), the forward state scan
+    (W S, Kb^T Vt), the adjoint scan (A^T dO, Kb dS, Qp^T dO, W^T dVt) and the gradients
+    (dO S^T, dO Vt^T, dA Km, Vt dS^T, dVt S^T, dW Kp^T, dVt V^T, T^T dW, T^T dVt, dT T^T,
+    T^T X, dM Km, dM^T Kp, dA^T Qp), masks not exploited; a tail chunk counts in full."""
+    K, V = x.d_k, x.d_v
+    mac = (3 * C * C * K + C * C * V                      # prep: Gram, Aqk, W, U
+           + 2 * C * K * V                                # forward state scan
+           + C * C * V + 3 * C * K * V                    # adjoint scan
+           + 3 * C * K * V + 3 * C * C * V + 6 * C * C * K + 2 * C * C * C)  # gradients
+    lens = x.lengths()
+    chunks = int(sum((int(n) + C - 1) // C for n in lens))
+    return 2 * mac * chunks * x.H_v
+
+
 def algorithmic_flops(x, C=64) -> int:
     """Useful FLOPs of the chunk algorithm (causal halves counted once), per token and
     value head: Gram (strict lower) + Aqk (lower) + forward substitution on [Kp | V]
@@ -420,6 +447,144 @@ def run_ours(args, world, rank, local, pg):
         print(json.dumps(line), flush=True)
 
 
+# fp32 FMA peak of the GPU: SMs x 128 FMA lanes per clock x 2 FLOP x the maximum SM clock
+# (2070 MHz on the GB300s here); the backward's contractions run on these units.
+FP32_LANES_PER_SM = 128
+
+
+def fp32_peak_tflops(sms: int, mhz: float) -> float:
+    return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def run_backward(args, world, rank, local, pg):
+    """--entry backward: one kda_chunk_bwd call per step (the workload's forward inputs,
+    a seeded dO and dht; all six gradients written)."""
+    import numpy as np
+    import torch
+
+    from chunkwise_gated_linear_gb300 import kda
+    from inputs import workload_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = kda.lib()
+    x = workload_inputs(args.workload, seed=1000 + rank)
+    B = x.N
+    Bp = 1 if x.varlen else B
+    T = x.T_total // Bp
+    dt_io = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+    rng = np.random.default_rng(2000 + rank)
+
+    def host(a, dtype, shape):
+        return torch.from_numpy(np.ascontiguousarray(a)).reshape(shape).to(dtype).pin_memory()
+
+    gshape = (Bp, T, x.H_v, x.d_k) if x.gate == "channel" else (Bp, T, x.H_v)
+    H = {"q": host(x.q, dt_io, (Bp, T, x.H_k, x.d_k)), "k": host(x.k, dt_io, (Bp, T, x.H_k, x.d_k)),
+         "v": host(x.v, dt_io, (Bp, T, x.H_v, x.d_v)), "g": host(x.g, torch.float32, gshape),
+         "dO": host(rng.standard_normal(x.v.shape, dtype=np.float32), dt_io, (Bp, T, x.H_v, x.d_v)),
+         "dht": host(rng.standard_normal((B, x.H_v, x.d_k, x.d_v), dtype=np.float32), torch.float32,
+                     (B, x.H_v, x.d_k, x.d_v))}
+    if x.beta is not None:
+        H["beta"] = host(x.beta, torch.float32, (Bp, T, x.H_v))
+    if x.h0 is not None:
+        H["h0"] = host(x.h0, torch.float32, (B, x.H_v, x.d_k, x.d_v))
+    inputs = [key for key in ("q", "k", "v", "g", "beta", "h0", "dO", "dht") if key in H]
+    D = {key: t.to(dev) for key, t in H.items()}
+    outs = {"dq": D["q"], "dk": D["k"], "dv": D["v"], "dg": D["g"], "dbeta": D.get("beta"), "dh0": D["dht"]}
+    for key, like in outs.items():
+        if like is not None:
+            D[key] = torch.empty_like(like)
+            H[key] = torch.empty_like(like, device="cpu").pin_memory()
+    results = [key for key in outs if key in D]
+    cu = torch.from_numpy(x.cu_seqlens.astype(np.int32)).to(dev) if x.varlen else None
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    ptr = lambda key: D[key].data_ptr() if key in D else None  # noqa: E731
+    params = kda.kda_bwd_params(
+        ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("dO"), ptr("dht"), ptr("dq"), ptr("dk"),
+        ptr("dv"), ptr("dg"), ptr("dbeta"), ptr("dh0"), B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale,
+        None if cu is None else cu.data_ptr(), kda.KDA_DTYPE_BF16 if x.dtype == "bf16" else kda.KDA_DTYPE_F32,
+        kda.KDA_GATE_PER_CHANNEL if x.gate == "channel" else kda.KDA_GATE_PER_HEAD, 0)
+
+    def call():
+        st = lib.kda_chunk_bwd(ctypes.byref(params), sh)
+        if st != 0:
+            raise RuntimeError(kda.status_string(st))
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(pg)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            call()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(pg)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = clk.summary()
+    ms_max = max_over_ranks(pg, ms)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for key in inputs:
+                D[key].copy_(H[key], non_blocking=True)
+            call()
+            for key in results:
+                H[key].copy_(D[key], non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ev3.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    ms_e2e = max_over_ranks(pg, ev2.elapsed_time(ev3) / args.steps)
+    h2d = sum(H[key].numel() * H[key].element_size() for key in inputs)
+    d2h = sum(H[key].numel() * H[key].element_size() for key in results)
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_max_mhz") or 2070.0
+    flops = backward_flops(x)
+    tflops = flops / (ms / 1000.0) / 1e12
+    peak = fp32_peak_tflops(sms, mhz)
+    hbm_peak, peak_kind = load_peaks()
+    abytes = backward_bytes(x)
+    if rank == 0:
+        tokens = x.T_total
+        line = {
+            "metric": METRIC, "value": tokens * world / (ms_max / 1000.0), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "entry": "backward", "B": B, "T_total": x.T_total,
+                       "H_k": x.H_k, "H_v": x.H_v, "d_k": x.d_k, "d_v": x.d_v, "C": 64,
+                       "io_dtype": x.dtype, "gate": "per-channel" if x.gate == "channel" else "per-head",
+                       "beta": x.beta is not None, "h0": x.h0 is not None, "dht": True,
+                       "global_batch": B * world, "parallelism": f"dp{world} (independent batches)",
+                       "l2": f"inputs larger than L2 ({abytes / 1e6:.0f} MB per step), no flush"},
+            "e2e": {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None, "peak_kind": "derived: fp32 FMA lanes x clock",
+                         "algorithmic_flops_per_launch": flops, "kernel": "backward (prep, states, adjoint, grads, finish)",
+                         "hbm_bytes_per_launch": abytes, "hbm_frac": abytes / (ms / 1000.0) / 1e9 / hbm_peak},
+            "cpu_baseline": None,
+            "clocks": clocks,
+            "gpu_launches": args.steps * (6 if x.dtype == "bf16" else 4),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -428,8 +593,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--entry", choices=["chunk", "recurrent"], default="chunk",
-                    help="kda_chunk_fwd (default) or kda_recurrent_fwd (the token-by-token decode step)")
+    ap.add_argument("--entry", choices=["chunk", "recurrent", "backward"], default="chunk",
+                    help="kda_chunk_fwd (default), kda_recurrent_fwd (the token-by-token decode step) "
+                         "or kda_chunk_bwd (the backward pass)")
     ap.add_argument("--frontend", choices=["none", "fused", "unfused"], default="none",
                     help="raw q, k, gate pre-activations and beta logits through the front-end "
                          "(q/k L2 norm, gated gate, beta sigmoid): applied inside the forward kernel "
@@ -441,7 +607,7 @@ def main():
         if args.impl == "reference":
             run_reference(args, world, rank, pg)
         else:
-            run_ours(args, world, rank, local, pg)
+            (run_backward if args.entry == "backward" else run_ours)(args, world, rank, local, pg)
     finally:
         if pg is not None:
             pg.destroy_process_group()

@@ -4,7 +4,10 @@ Attention) for GB300 (sm_103a): a C-ABI CUDA library (``include/kda.h``,
 
 from .kda import (  # noqa: F401
     KdaError,
+    chunk_kda_bwd,
     chunk_kda_fwd,
+    kda_bwd_params,
+    kda_chunk_bwd,
     kda_chunk_fwd,
     kda_chunk_fwd_ex,
     kda_chunk_fwd_f32,

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "kda.h"
+#include "kda_bwd.h"
 #include "kda_common.cuh"
 
 namespace kda {
@@ -241,6 +242,50 @@ int kda_recurrent_fwd(const void *q, const void *k, const void *v, const float *
 int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream) {
     if (p == nullptr) return KDA_ERR_INVALID_ARG;
     return run(*p, nullptr, stream);
+}
+
+int kda_chunk_bwd(const kda_bwd_params *p, cudaStream_t stream) {
+    if (p == nullptr) return KDA_ERR_INVALID_ARG;
+    // the forward arguments through the forward's own checks (dq stands where o does)
+    kda_fwd_params f{p->q, p->k, p->v, p->g, p->beta, p->h0, p->dq, nullptr, p->B, p->T, p->H_k, p->H_v,
+                     p->d_k, p->d_v, p->C, p->scale, p->cu_seqlens, p->dtype, p->gate_mode, 0};
+    kda::FwdArgs a;
+    const int st = prepare(f, a);
+    if (st != KDA_OK) return st;
+    if (p->flags != 0) return KDA_ERR_INVALID_ARG;
+    if (p->T != 0 && (p->dO == nullptr || p->dk == nullptr || p->dv == nullptr || p->dg == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if ((p->beta == nullptr) != (p->dbeta == nullptr) && p->T != 0) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(p->dO) || !aligned16(p->dht) || !aligned16(p->dk) || !aligned16(p->dv) ||
+        !aligned16(p->dg) || !aligned16(p->dbeta) || !aligned16(p->dh0))
+        return KDA_ERR_ALIGNMENT;
+    kda::BwdArgs b{};
+    b.q = p->q;
+    b.k = p->k;
+    b.v = p->v;
+    b.g = p->g;
+    b.beta = p->beta;
+    b.h0 = p->h0;
+    b.dO = p->dO;
+    b.dht = p->dht;
+    b.dq = p->dq;
+    b.dk = p->dk;
+    b.dv = p->dv;
+    b.dg = p->dg;
+    b.dbeta = p->dbeta;
+    b.dh0 = p->dh0;
+    b.cu_seqlens = p->cu_seqlens;
+    b.N = a.N;
+    b.T = a.T;
+    b.H_k = a.H_k;
+    b.H_v = a.H_v;
+    b.d_k = a.d_k;
+    b.d_v = a.d_v;
+    b.group = a.group;
+    b.scale = a.scale;
+    b.gate_per_head = a.gate_per_head;
+    b.decay_only = a.decay_only;
+    return status_of(kda::launch_bwd(b, p->dtype == KDA_DTYPE_F32, stream));
 }
 
 int kda_chunk_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cudaStream_t stream) {

@@ -1,0 +1,577 @@
+// Chunkwise backward pass of the gated delta rule (fp32 arithmetic throughout).
+//
+// Gradients of sum(dO * O) + sum(dht * ht) with respect to q, k, v, g, beta and h0, in the
+// chunk form that "Gated DeltaNet" lays out in "反向传播：状态伴随与三角变换梯度": the chunk
+// factors are recomputed, the state adjoint runs backwards from dht through the chunks,
+// and the gradients of the WY factors are carried back through the triangular inverse.
+// With gamma the chunk-local cumulative log gate and Gn its value at the chunk's last
+// token, the forward chunk is (all per unit, 64 tokens):
+//   Qp = scale Q e^g, Kp = K e^g, Km = K e^-g, Kb = K e^(Gn - g), EG = e^Gn
+//   M = strict_lower(Kp Km^T), A = lower(Qp Km^T), T = (I + diag(beta) M)^-1
+//   W = T diag(beta) Kp, U = T diag(beta) V, Vt = U - W S, O = Qp S + A Vt,
+//   S' = diag(EG) S + Kb^T Vt
+// and, for the adjoint dS' of the chunk's exit state:
+//   dVt = A^T dO + Kb dS',  dS = diag(EG) dS' + Qp^T dO - W^T dVt
+//   dQp = dO S^T + dA Km (dA = lower(dO Vt^T)),  dKb = Vt dS'^T,  dW = -dVt S^T
+//   dT = (dW Kp^T + dVt V^T) diag(beta),  dL = -T^T dT T^T (strictly lower)
+//   dKp = diag(beta) T^T dW + diag(beta) dL Km,  dKm = (diag(beta) dL)^T Kp + dA^T Qp
+//   dV = diag(beta) T^T dVt,  dbeta = rows of (T^T dW . Kp) + (T^T dVt . V) + (dL . M)
+//   dQ = scale e^g dQp,  dK = e^g dKp + e^-g dKm + e^(Gn - g) dKb
+//   dgamma = dQp.Qp + dKp.Kp - dKm.Km - dKb.Kb,  dGn = sum_t dKb.Kb + dEG.EG,
+//   dg = reverse cumulative sum of dgamma over the chunk's tokens, plus dGn
+// (decay-only: Kp = 0, beta = 1, so T = I, W = 0, U = V and dV = dVt).
+//
+// Five kernels, all on stream-ordered scratch from the library's pool:
+//   prep     (chunk, unit) parallel: gamma, Qp, Kp, Km, Kb, EG, M, A, T, W, U, V, dO
+//   states   (unit, 64 columns of d_v): the forward state scan, storing S and Vt per chunk
+//   adjoint  (unit, 64 columns of d_v): the reverse scan of dS, storing dS' and dVt per
+//            chunk, and dh0
+//   grads    (chunk, unit) parallel: every gradient above; dq and dk added atomically into
+//            fp32 accumulators (value heads that share a key head add into the same rows)
+//   finish   the accumulators to the output dtype (bf16 outputs)
+// Every contraction goes through one CTA-wide fp32 GEMM (64 x 64 output tiles, 16-deep
+// k steps staged in shared memory, 4 x 4 outputs per thread).
+#include <algorithm>
+#include <cstdint>
+#include <type_traits>
+
+#include "kda_bwd.h"
+#include "kda_common.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kT = 256;  // threads of every backward kernel
+
+// Per-slot scratch layout (floats). A slot holds one chunk of one unit.
+struct Lay {
+    int64_t qp, kp, km, kb, wm, gm, u, vf, dof, vt, dvt, m, a, t, eg, bt, se, dsx, total;
+};
+__host__ __device__ inline Lay make_lay(int K, int V) {
+    Lay L;
+    int64_t o = 0;
+    auto take = [&](int64_t n) {
+        const int64_t at = o;
+        o += (n + 63) & ~(int64_t)63;
+        return at;
+    };
+    L.qp = take(64 * K); L.kp = take(64 * K); L.km = take(64 * K); L.kb = take(64 * K);
+    L.wm = take(64 * K); L.gm = take(64 * K);
+    L.u = take(64 * V); L.vf = take(64 * V); L.dof = take(64 * V); L.vt = take(64 * V); L.dvt = take(64 * V);
+    L.m = take(64 * 64); L.a = take(64 * 64); L.t = take(64 * 64);
+    L.eg = take(K); L.bt = take(64);
+    L.se = take((int64_t)K * V); L.dsx = take((int64_t)K * V);
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T *p);
+template <>
+__device__ __forceinline__ float ldf<float>(const float *p) {
+    return *p;
+}
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+}
+template <typename T>
+__device__ __forceinline__ void stf(T *p, float v);
+template <>
+__device__ __forceinline__ void stf<float>(float *p, float v) {
+    *p = v;
+}
+template <>
+__device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
+    *p = __float2bfloat16_rn(v);
+}
+
+// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), fp32, every matrix given by
+// a base pointer (global or shared) and element strides: A(m, k) = A[m * am + k * ak],
+// B(k, n) = B[k * bk + n * bn], C(m, n) = C[m * cm + n * cn]. M and N are multiples of 64,
+// K of 16; C must not overlap A or B. Called by all kT threads; ends with a barrier.
+constexpr int kStageFloats = 2 * 16 * 68;
+__device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int64_t am, int64_t ak,
+                           const float *B, int64_t bk, int64_t bn, float *C, int64_t cm, int64_t cn, bool acc,
+                           float *stage) {
+    float *As = stage, *Bs = stage + 16 * 68;
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    for (int m0 = 0; m0 < M; m0 += 64) {
+        for (int n0 = 0; n0 < N; n0 += 64) {
+            float c[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
+            for (int k0 = 0; k0 < K; k0 += 16) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int e = tid + kT * r;
+                    int m, k;
+                    if (ak == 1) { k = e & 15; m = e >> 4; } else { m = e & 63; k = e >> 6; }
+                    As[k * 68 + m] = A[(int64_t)(m0 + m) * am + (int64_t)(k0 + k) * ak];
+                    int kb, n;
+                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & 15; n = e >> 4; }
+                    Bs[kb * 68 + n] = B[(int64_t)(k0 + kb) * bk + (int64_t)(n0 + n) * bn];
+                }
+                __syncthreads();
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(As + kk * 68 + ty * 4);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(Bs + kk * 68 + tx * 4);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) c[i][j] = fmaf(av[i], bv[j], c[i][j]);
+                }
+                __syncthreads();
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float *p = C + (int64_t)(m0 + ty * 4 + i) * cm + (int64_t)(n0 + tx * 4 + j) * cn;
+                    *p = acc ? fmaf(alpha, c[i][j], *p) : alpha * c[i][j];
+                }
+        }
+    }
+    __syncthreads();
+}
+
+// Sequence bounds (fixed-length batches or packed sequences).
+__device__ __forceinline__ void bounds(const BwdArgs &a, int n, int64_t &bos, int &len) {
+    if (a.cu_seqlens == nullptr) {
+        bos = (int64_t)n * a.T;
+        len = a.T;
+    } else {
+        bos = a.cu_seqlens[n];
+        len = a.cu_seqlens[n + 1] - a.cu_seqlens[n];
+    }
+}
+// Slot of chunk c of sequence n (value head h): (bos / 64 + c + n) * H_v + h. Chunks of
+// different sequences never share a slot (there are at most T / 64 + N windows).
+__device__ __forceinline__ int64_t slot_of(const BwdArgs &a, int64_t bos, int n, int c, int h) {
+    return ((bos >> 6) + c + n) * a.H_v + h;
+}
+// The (sequence, chunk) that owns window s, or false when none does.
+__device__ bool window_owner(const BwdArgs &a, int64_t s, int &n, int &c, int64_t &bos, int &len) {
+    // the largest n with bos_n / 64 + n <= s (strictly increasing in n)
+    int lo = 0, hi = a.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        int64_t b;
+        int l;
+        bounds(a, mid, b, l);
+        if ((b >> 6) + mid <= s) lo = mid; else hi = mid - 1;
+    }
+    n = lo;
+    bounds(a, n, bos, len);
+    const int64_t cc = s - (bos >> 6) - n;
+    if (cc < 0 || cc * 64 >= len) return false;
+    c = (int)cc;
+    return true;
+}
+
+// ---- prep: the chunk factors -----------------------------------------------------------------
+template <typename T, bool GATE_HEAD>
+__global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
+    __shared__ __align__(16) float stage[kStageFloats];
+    __shared__ float Lsh[64 * 65];
+    int n, c, len;
+    int64_t bos;
+    if (!window_owner(a, blockIdx.y, n, c, bos, len)) return;
+    const int h = blockIdx.x, hk = h / a.group, K = a.d_k, V = a.d_v;
+    const Lay L = make_lay(K, V);
+    float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+    const int row0 = c * 64, nv = min(64, len - row0);
+    const int tid = threadIdx.x;
+    const T *q = static_cast<const T *>(a.q);
+    const T *k = static_cast<const T *>(a.k);
+    const T *v = static_cast<const T *>(a.v);
+    const T *dO = static_cast<const T *>(a.dO);
+    const int64_t sqk = (int64_t)a.H_k * K, sv = (int64_t)a.H_v * V;
+    const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * K;
+
+    // gamma (natural log), per channel, rows past the end hold the last valid value
+    for (int i = tid; i < K; i += kT) {
+        float acc = 0.f;
+        for (int t = 0; t < 64; ++t) {
+            if (t < nv) {
+                const int64_t r = bos + row0 + t;
+                acc += GATE_HEAD ? a.g[r * sg + h] : a.g[r * sg + (int64_t)h * K + i];
+            }
+            S[L.gm + t * K + i] = acc;
+        }
+        S[L.eg + i] = expf(acc);
+    }
+    for (int t = tid; t < 64; t += kT)
+        S[L.bt + t] = t < nv ? (a.decay_only ? 1.f : a.beta[(bos + row0 + t) * a.H_v + h]) : 0.f;
+    __syncthreads();
+    for (int e = tid; e < 64 * K; e += kT) {
+        const int t = e / K, i = e - t * K;
+        const int64_t r = bos + row0 + t;
+        const float kv = t < nv ? ldf<T>(k + r * sqk + (int64_t)hk * K + i) : 0.f;
+        const float qv = t < nv ? ldf<T>(q + r * sqk + (int64_t)hk * K + i) : 0.f;
+        const float gam = S[L.gm + e], gn = S[L.gm + 63 * K + i];
+        S[L.qp + e] = a.scale * qv * expf(gam);
+        S[L.kp + e] = a.decay_only ? 0.f : kv * expf(gam);
+        S[L.km + e] = kv * expf(-gam);
+        S[L.kb + e] = kv * expf(gn - gam);
+    }
+    for (int e = tid; e < 64 * V; e += kT) {
+        const int t = e / V, j = e - t * V;
+        const int64_t r = bos + row0 + t;
+        S[L.vf + e] = t < nv ? ldf<T>(v + r * sv + (int64_t)h * V + j) : 0.f;
+        S[L.dof + e] = t < nv ? ldf<T>(dO + r * sv + (int64_t)h * V + j) : 0.f;
+    }
+    __syncthreads();
+    // M = Kp Km^T (strictly lower), A = Qp Km^T (lower with the diagonal)
+    block_gemm(64, 64, K, 1.f, S + L.kp, K, 1, S + L.km, 1, K, S + L.m, 64, 1, false, stage);
+    block_gemm(64, 64, K, 1.f, S + L.qp, K, 1, S + L.km, 1, K, S + L.a, 64, 1, false, stage);
+    for (int e = tid; e < 64 * 64; e += kT) {
+        const int t = e >> 6, s = e & 63;
+        if (s >= t) S[L.m + e] = 0.f;
+        if (s > t) S[L.a + e] = 0.f;
+        Lsh[t * 65 + s] = s < t ? S[L.bt + t] * S[L.m + e] : 0.f;  // L = diag(beta) M
+    }
+    __syncthreads();
+    // T = (I + L)^-1 by forward substitution, row by row: T[i] = e_i - sum_{j<i} L[i][j] T[j]
+    float *Tm = S + L.t;
+    for (int i = 0; i < 64; ++i) {
+        if (tid < 64) {
+            float acc = tid == i ? 1.f : 0.f;
+            for (int j = 0; j < i; ++j) acc = fmaf(-Lsh[i * 65 + j], Tm[j * 64 + tid], acc);
+            Tm[i * 64 + tid] = acc;
+        }
+        __syncthreads();
+    }
+    // W = T diag(beta) Kp, U = T diag(beta) V: scale the rows first (beta of row s)
+    // (Kb as a temporary would be overwritten: use the dVt and Vt areas, free until the scans)
+    float *Kbeta = S + L.wm;  // W's own area: the product goes to Vt's area first
+    for (int e = tid; e < 64 * K; e += kT) Kbeta[e] = S[L.bt + e / K] * S[L.kp + e];
+    float *Vbeta = S + L.dvt;
+    for (int e = tid; e < 64 * V; e += kT) Vbeta[e] = S[L.bt + e / V] * S[L.vf + e];
+    __syncthreads();
+    block_gemm(64, V, 64, 1.f, Tm, 64, 1, Vbeta, V, 1, S + L.u, V, 1, false, stage);
+    // W: T (64 x 64) times Kbeta (64 x K) into the dS' area (free until the adjoint scan),
+    // then copied back over Kbeta
+    float *Wtmp = S + L.dsx;
+    block_gemm(64, K, 64, 1.f, Tm, 64, 1, Kbeta, K, 1, Wtmp, K, 1, false, stage);
+    for (int e = tid; e < 64 * K; e += kT) S[L.wm + e] = Wtmp[e];
+}
+
+// ---- states: the forward scan, S^T slice [K][64 columns] in shared memory -----------------
+__global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    float *St = sm;                      // S [K][64]
+    float *stage = sm + a.d_k * 64;
+    const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
+    const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
+    const Lay L = make_lay(K, V);
+    int64_t bos;
+    int len;
+    bounds(a, n, bos, len);
+    const int nch = (len + 63) / 64;
+    for (int e = tid; e < K * 64; e += kT) {
+        const int i = e >> 6, j = e & 63;
+        St[e] = a.h0 ? a.h0[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
+    }
+    __syncthreads();
+    for (int c = 0; c < nch; ++c) {
+        float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+        for (int e = tid; e < K * 64; e += kT) S[L.se + (int64_t)(e >> 6) * V + j0 + (e & 63)] = St[e];
+        // Vt = U - W S
+        float *Vt = S + L.vt + j0;
+        for (int e = tid; e < 64 * 64; e += kT) Vt[(e >> 6) * V + (e & 63)] = S[L.u + (e >> 6) * V + j0 + (e & 63)];
+        __syncthreads();
+        block_gemm(64, 64, K, -1.f, S + L.wm, K, 1, St, 64, 1, Vt, V, 1, true, stage);
+        // S <- diag(EG) S + Kb^T Vt
+        for (int e = tid; e < K * 64; e += kT) St[e] *= S[L.eg + (e >> 6)];
+        __syncthreads();
+        block_gemm(K, 64, 64, 1.f, S + L.kb, 1, K, Vt, V, 1, St, 64, 1, true, stage);
+    }
+}
+
+// ---- adjoint: the reverse scan, dS^T slice [K][64 columns] in shared memory ---------------
+__global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    float *dS = sm;  // [K][64]
+    float *stage = sm + a.d_k * 64;
+    const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
+    const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
+    const Lay L = make_lay(K, V);
+    int64_t bos;
+    int len;
+    bounds(a, n, bos, len);
+    const int nch = (len + 63) / 64;
+    for (int e = tid; e < K * 64; e += kT) {
+        const int i = e >> 6, j = e & 63;
+        dS[e] = a.dht ? a.dht[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
+    }
+    __syncthreads();
+    for (int c = nch - 1; c >= 0; --c) {
+        float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+        for (int e = tid; e < K * 64; e += kT) S[L.dsx + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dS[e];
+        float *dVt = S + L.dvt + j0;
+        // dVt = A^T dO + Kb dS'
+        block_gemm(64, 64, 64, 1.f, S + L.a, 1, 64, S + L.dof + j0, V, 1, dVt, V, 1, false, stage);
+        block_gemm(64, 64, K, 1.f, S + L.kb, K, 1, dS, 64, 1, dVt, V, 1, true, stage);
+        // dS <- diag(EG) dS' + Qp^T dO - W^T dVt
+        for (int e = tid; e < K * 64; e += kT) dS[e] *= S[L.eg + (e >> 6)];
+        __syncthreads();
+        block_gemm(K, 64, 64, 1.f, S + L.qp, 1, K, S + L.dof + j0, V, 1, dS, 64, 1, true, stage);
+        block_gemm(K, 64, 64, -1.f, S + L.wm, 1, K, dVt, V, 1, dS, 64, 1, true, stage);
+    }
+    if (a.dh0 != nullptr)
+        for (int e = tid; e < K * 64; e += kT)
+            a.dh0[(((int64_t)n * a.H_v + h) * K + (e >> 6)) * V + j0 + (e & 63)] = dS[e];
+}
+
+// ---- grads: every gradient of one chunk ---------------------------------------------------------
+// Shared memory: dQp, dKp, dKm, dKb, dW (then T^T dVt) [64][K or V], dA, dT (then dL), X
+// [64][64], small vectors and the GEMM stage.
+template <typename T, bool GATE_HEAD>
+__global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    int n, c, len;
+    int64_t bos;
+    if (!window_owner(a, blockIdx.y, n, c, bos, len)) return;
+    const int h = blockIdx.x, hk = h / a.group, K = a.d_k, V = a.d_v, tid = threadIdx.x;
+    const int KV = K > V ? K : V;
+    float *dQp = sm, *dKp = dQp + 64 * K, *dKm = dKp + 64 * K, *dKb = dKm + 64 * K;
+    float *dW = dKb + 64 * K;  // [64][KV]
+    float *dA = dW + 64 * KV, *dT = dA + 4096, *X = dT + 4096;
+    float *dEG = X + 4096, *dGn = dEG + 128, *dbeta = dGn + 128;
+    float *stage = dbeta + 64;
+    const Lay L = make_lay(K, V);
+    const float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+    const float *Qp = S + L.qp, *Kp = S + L.kp, *Km = S + L.km, *Kb = S + L.kb;
+    const float *Gm = S + L.gm, *Vf = S + L.vf, *dOf = S + L.dof, *Vt = S + L.vt, *dVt = S + L.dvt;
+    const float *Mm = S + L.m, *Tm = S + L.t, *EG = S + L.eg, *Bt = S + L.bt;
+    const float *Se = S + L.se, *dSx = S + L.dsx;
+    const int row0 = c * 64, nv = min(64, len - row0);
+
+    // dQp = dO S^T;  dA = lower(dO Vt^T);  dQp += dA Km
+    block_gemm(64, K, V, 1.f, dOf, V, 1, Se, 1, V, dQp, K, 1, false, stage);
+    block_gemm(64, 64, V, 1.f, dOf, V, 1, Vt, 1, V, dA, 64, 1, false, stage);
+    for (int e = tid; e < 4096; e += kT)
+        if ((e & 63) > (e >> 6)) dA[e] = 0.f;
+    __syncthreads();
+    block_gemm(64, K, 64, 1.f, dA, 64, 1, Km, K, 1, dQp, K, 1, true, stage);
+    // dKb = Vt dS'^T;  dW = -dVt S^T;  dEG = rows of dS' . S
+    block_gemm(64, K, V, 1.f, Vt, V, 1, dSx, 1, V, dKb, K, 1, false, stage);
+    block_gemm(64, K, V, -1.f, dVt, V, 1, Se, 1, V, dW, K, 1, false, stage);
+    for (int i = tid; i < K; i += kT) {
+        float s = 0.f;
+        for (int j = 0; j < V; ++j) s = fmaf(dSx[(int64_t)i * V + j], Se[(int64_t)i * V + j], s);
+        dEG[i] = s;
+    }
+    for (int t = tid; t < 64; t += kT) dbeta[t] = 0.f;
+    __syncthreads();
+    if (!a.decay_only) {
+        // dT = (dW Kp^T + dVt V^T) diag(beta)
+        block_gemm(64, 64, K, 1.f, dW, K, 1, Kp, 1, K, dT, 64, 1, false, stage);
+        block_gemm(64, 64, V, 1.f, dVt, V, 1, Vf, 1, V, dT, 64, 1, true, stage);
+        for (int e = tid; e < 4096; e += kT) dT[e] *= Bt[e & 63];
+        __syncthreads();
+        // T^T dW -> dKp (then scaled by beta), dbeta += rows of (T^T dW) . Kp
+        block_gemm(64, K, 64, 1.f, Tm, 1, 64, dW, K, 1, dKp, K, 1, false, stage);
+        // T^T dVt -> dW's area (dW is consumed)
+        float *TtdU = dW;
+        block_gemm(64, V, 64, 1.f, Tm, 1, 64, dVt, V, 1, TtdU, V, 1, false, stage);
+        for (int t = tid; t < 64; t += kT) {
+            float s = 0.f;
+            for (int i = 0; i < K; ++i) s = fmaf(dKp[t * K + i], Kp[t * K + i], s);
+            for (int j = 0; j < V; ++j) s = fmaf(TtdU[t * V + j], Vf[t * V + j], s);
+            dbeta[t] = s;
+        }
+        __syncthreads();
+        for (int e = tid; e < 64 * K; e += kT) dKp[e] *= Bt[e / K];
+        // dv = diag(beta) T^T dVt
+        T *dv = static_cast<T *>(a.dv);
+        for (int e = tid; e < 64 * V; e += kT) {
+            const int t = e / V, j = e - t * V;
+            if (t < nv) stf<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j, Bt[t] * TtdU[e]);
+        }
+        // dL = -T^T dT T^T (strictly lower): X = dT T^T, dL = -T^T X into dT's area
+        block_gemm(64, 64, 64, 1.f, dT, 64, 1, Tm, 1, 64, X, 64, 1, false, stage);
+        block_gemm(64, 64, 64, -1.f, Tm, 1, 64, X, 64, 1, dT, 64, 1, false, stage);
+        float *dL = dT;
+        for (int e = tid; e < 4096; e += kT)
+            if ((e & 63) >= (e >> 6)) dL[e] = 0.f;
+        __syncthreads();
+        // dbeta += rows of dL . M;  dM = diag(beta) dL (in place)
+        for (int t = tid; t < 64; t += kT) {
+            float s = 0.f;
+            for (int s2 = 0; s2 < t; ++s2) s = fmaf(dL[t * 64 + s2], Mm[t * 64 + s2], s);
+            dbeta[t] += s;
+        }
+        __syncthreads();
+        for (int e = tid; e < 4096; e += kT) dL[e] *= Bt[e >> 6];
+        __syncthreads();
+        // dKp += dM Km;  dKm = dM^T Kp
+        block_gemm(64, K, 64, 1.f, dL, 64, 1, Km, K, 1, dKp, K, 1, true, stage);
+        block_gemm(64, K, 64, 1.f, dL, 1, 64, Kp, K, 1, dKm, K, 1, false, stage);
+    } else {
+        // decay-only: U = V, W = 0: dv = dVt
+        T *dv = static_cast<T *>(a.dv);
+        for (int e = tid; e < 64 * V; e += kT) {
+            const int t = e / V, j = e - t * V;
+            if (t < nv) stf<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j, dVt[e]);
+        }
+        for (int e = tid; e < 64 * K; e += kT) {
+            dKp[e] = 0.f;
+            dKm[e] = 0.f;
+        }
+        __syncthreads();
+    }
+    // dKm += dA^T Qp
+    block_gemm(64, K, 64, 1.f, dA, 1, 64, Qp, K, 1, dKm, K, 1, true, stage);
+
+    // dq, dk (atomically: value heads of one key head share rows), dgamma in dQp's area
+    float *dqa = a.dq_acc, *dka = a.dk_acc;
+    for (int e = tid; e < 64 * K; e += kT) {
+        const int t = e / K, i = e - t * K;
+        const float gam = Gm[e], gn = Gm[63 * K + i];
+        const float ep = expf(gam), em = expf(-gam), eb = expf(gn - gam);
+        const float vq = dQp[e], vkp = dKp[e], vkm = dKm[e], vkb = dKb[e];
+        if (t < nv) {
+            const int64_t o = ((bos + row0 + t) * a.H_k + hk) * K + i;
+            atomicAdd(dqa + o, a.scale * ep * vq);
+            atomicAdd(dka + o, ep * vkp + em * vkm + eb * vkb);
+        }
+        dQp[e] = vq * Qp[e] + vkp * Kp[e] - vkm * Km[e] - vkb * Kb[e];  // dgamma
+        dKb[e] = vkb * Kb[e];                                             // for dGn
+    }
+    __syncthreads();
+    for (int i = tid; i < K; i += kT) {
+        float s = dEG[i] * EG[i];
+        for (int t = 0; t < 64; ++t) s += dKb[t * K + i];
+        dGn[i] = s;
+    }
+    __syncthreads();
+    // dg: reverse cumulative sum over the chunk's tokens, plus dGn
+    float *dgamma = dQp;
+    if (!GATE_HEAD) {
+        for (int i = tid; i < K; i += kT) {
+            float acc = dGn[i];
+            for (int t = 63; t >= 0; --t) {
+                acc += dgamma[t * K + i];
+                if (t < nv) a.dg[((bos + row0 + t) * a.H_v + h) * K + i] = acc;
+            }
+        }
+    } else {
+        // one gate per (token, head): the channels' sums
+        for (int i = tid; i < K; i += kT) {
+            float acc = dGn[i];
+            for (int t = 63; t >= 0; --t) {
+                acc += dgamma[t * K + i];
+                dgamma[t * K + i] = acc;
+            }
+        }
+        __syncthreads();
+        for (int t = tid; t < nv; t += kT) {
+            float s = 0.f;
+            for (int i = 0; i < K; ++i) s += dgamma[t * K + i];
+            a.dg[(bos + row0 + t) * a.H_v + h] = s;
+        }
+    }
+    if (!a.decay_only && a.dbeta != nullptr)
+        for (int t = tid; t < nv; t += kT) a.dbeta[(bos + row0 + t) * a.H_v + h] = dbeta[t];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kT) bwd_finish_kernel(const float *acc, T *out, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x; i < n; i += (int64_t)gridDim.x * kT)
+        stf<T>(out + i, acc[i]);
+}
+
+size_t grads_smem(int K, int V) {
+    const int KV = K > V ? K : V;
+    return sizeof(float) * ((size_t)4 * 64 * K + (size_t)64 * KV + 3 * 4096 + 128 + 128 + 64 + kStageFloats);
+}
+
+template <typename T, bool GATE_HEAD>
+cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
+    BwdArgs a = a0;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int K = a.d_k, V = a.d_v;
+    const int64_t Ttot = a.cu_seqlens ? (int64_t)a.T : (int64_t)a.N * a.T;
+    const int64_t windows = (Ttot + 63) / 64 + a.N;
+    const Lay L = make_lay(K, V);
+    const size_t slot_bytes = sizeof(float) * (size_t)L.total;
+    const size_t scratch_bytes = slot_bytes * (size_t)(windows * a.H_v);
+    const size_t acc_elems = (size_t)Ttot * a.H_k * K;
+    const bool own_acc = !std::is_same<T, float>::value;  // bf16 outputs: fp32 accumulators
+    const size_t acc_bytes = own_acc ? 2 * sizeof(float) * acc_elems : 0;
+    cudaMemPool_t pool = nullptr;
+    e = scratch_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    void *buf = nullptr;
+    e = cudaMallocFromPoolAsync(&buf, scratch_bytes + acc_bytes + 256, pool, stream);
+    if (e != cudaSuccess) return e;
+    a.scratch = static_cast<float *>(buf);
+    if (own_acc) {
+        a.dq_acc = reinterpret_cast<float *>(static_cast<unsigned char *>(buf) + scratch_bytes);
+        a.dk_acc = a.dq_acc + acc_elems;
+    } else {
+        a.dq_acc = static_cast<float *>(a.dq);
+        a.dk_acc = static_cast<float *>(a.dk);
+    }
+    if (acc_elems > 0) {
+        e = cudaMemsetAsync(a.dq_acc, 0, sizeof(float) * acc_elems, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a.dk_acc, 0, sizeof(float) * acc_elems, stream);
+    }
+    const size_t scan_smem = sizeof(float) * ((size_t)K * 64 + kStageFloats);
+    const size_t gsmem = grads_smem(K, V);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_grads_kernel<T, GATE_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)gsmem);
+    if (e == cudaSuccess && windows > 0 && Ttot > 0) {
+        const dim3 gw(a.H_v, (unsigned)windows);
+        bwd_prep_kernel<T, GATE_HEAD><<<gw, kT, 0, stream>>>(a);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) {
+            bwd_states_kernel<<<dim3(V / 64, a.H_v, a.N), kT, scan_smem, stream>>>(a);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            bwd_adjoint_kernel<<<dim3(V / 64, a.H_v, a.N), kT, scan_smem, stream>>>(a);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            bwd_grads_kernel<T, GATE_HEAD><<<gw, kT, gsmem, stream>>>(a);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess && own_acc && acc_elems > 0) {
+            const int grid = (int)std::min<int64_t>((int64_t)sms * 8, ((int64_t)acc_elems + kT - 1) / kT);
+            bwd_finish_kernel<T><<<grid, kT, 0, stream>>>(a.dq_acc, static_cast<T *>(a.dq), (int64_t)acc_elems);
+            bwd_finish_kernel<T><<<grid, kT, 0, stream>>>(a.dk_acc, static_cast<T *>(a.dk), (int64_t)acc_elems);
+            e = cudaGetLastError();
+        }
+    } else if (e == cudaSuccess) {
+        // no tokens: dh0 = dht (or zero)
+        const size_t sb = sizeof(float) * (size_t)a.N * a.H_v * K * V;
+        if (a.dh0 != nullptr)
+            e = a.dht ? cudaMemcpyAsync(a.dh0, a.dht, sb, cudaMemcpyDeviceToDevice, stream)
+                      : cudaMemsetAsync(a.dh0, 0, sb, stream);
+    }
+    const cudaError_t ef = cudaFreeAsync(buf, stream);
+    return e != cudaSuccess ? e : ef;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs &a, bool f32, cudaStream_t stream) {
+    if (f32)
+        return a.gate_per_head ? launch_typed<float, true>(a, stream) : launch_typed<float, false>(a, stream);
+    return a.gate_per_head ? launch_typed<__nv_bfloat16, true>(a, stream)
+                           : launch_typed<__nv_bfloat16, false>(a, stream);
+}
+
+}  // namespace kda

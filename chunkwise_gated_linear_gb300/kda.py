@@ -31,7 +31,8 @@ KDA_DEVICE_ERR_TIMEOUT = 2
 
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_ex", "kda_status_string",
             "kda_get_device_error", "kda_chunk_fwd_noalloc", "kda_recurrent_fwd",
-            "kda_recurrent_fwd_ex", "kda_chunk_fwd_fused", "kda_recurrent_fwd_fused")
+            "kda_recurrent_fwd_ex", "kda_chunk_fwd_fused", "kda_recurrent_fwd_fused",
+            "kda_chunk_bwd")
 
 
 class KdaError(RuntimeError):
@@ -45,6 +46,20 @@ class kda_fwd_params(ctypes.Structure):
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
         ("o", ctypes.c_void_p), ("ht", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("T", ctypes.c_int), ("H_k", ctypes.c_int), ("H_v", ctypes.c_int),
+        ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("C", ctypes.c_int),
+        ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p),
+        ("dtype", ctypes.c_int), ("gate_mode", ctypes.c_int), ("flags", ctypes.c_int),
+    ]
+
+
+class kda_bwd_params(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
+        ("dO", ctypes.c_void_p), ("dht", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p), ("dh0", ctypes.c_void_p),
         ("B", ctypes.c_int), ("T", ctypes.c_int), ("H_k", ctypes.c_int), ("H_v", ctypes.c_int),
         ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("C", ctypes.c_int),
         ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p),
@@ -86,6 +101,8 @@ def lib() -> ctypes.CDLL:
         L.kda_recurrent_fwd.restype = I
         L.kda_recurrent_fwd_ex.argtypes = [ctypes.POINTER(kda_fwd_params), P]
         L.kda_recurrent_fwd_ex.restype = I
+        L.kda_chunk_bwd.argtypes = [ctypes.POINTER(kda_bwd_params), P]
+        L.kda_chunk_bwd.restype = I
         for name in ("kda_chunk_fwd_fused", "kda_recurrent_fwd_fused"):
             fn = getattr(L, name)
             fn.argtypes = [ctypes.POINTER(kda_fwd_params), ctypes.POINTER(kda_frontend), P]
@@ -144,6 +161,10 @@ def kda_chunk_fwd_fused(params: kda_fwd_params, fe: kda_frontend | None, stream)
 def kda_recurrent_fwd_fused(params: kda_fwd_params, fe: kda_frontend | None, stream) -> int:
     return lib().kda_recurrent_fwd_fused(ctypes.byref(params), None if fe is None else ctypes.byref(fe),
                                          stream or None)
+
+
+def kda_chunk_bwd(params: kda_bwd_params, stream) -> int:
+    return lib().kda_chunk_bwd(ctypes.byref(params), stream or None)
 
 
 def kda_get_device_error(stream) -> int:
@@ -257,3 +278,57 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
     if st != KDA_OK:
         raise KdaError(st, name)
     return o, ht
+
+
+def chunk_kda_bwd(q, k, v, g, beta, do, *, h0=None, dht=None, scale=None, cu_seqlens=None,
+                  chunk_size=64, want_dh0=True, stream=None):
+    """Backward of :func:`chunk_kda_fwd` on torch CUDA tensors (kda_chunk_bwd).
+
+    Same inputs as the forward plus ``do`` (the gradient of o, like v) and ``dht`` (of ht,
+    fp32 [N, H_v, d_k, d_v], or None). Returns ``(dq, dk, dv, dg, dbeta, dh0)``: dq, dk, dv
+    in the dtype of q, dg like g, dbeta like beta (None without beta), dh0 fp32 (None when
+    ``want_dh0`` is False).
+    """
+    import torch
+
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or do.shape != v.shape:
+        raise ValueError("q, k must be [B, T, H_k, d_k]; v and do [B, T, H_v, d_v]")
+    B, T, H_k, d_k = q.shape
+    _, _, H_v, d_v = v.shape
+    if q.dtype == torch.bfloat16:
+        dtype = KDA_DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dtype = KDA_DTYPE_F32
+    else:
+        raise TypeError("q, k, v must be bf16 or fp32")
+    if k.dtype != q.dtype or v.dtype != q.dtype or do.dtype != q.dtype:
+        raise TypeError("q, k, v and do must share one dtype")
+    if g.shape == (B, T, H_v, d_k):
+        gate = KDA_GATE_PER_CHANNEL
+    elif g.shape == (B, T, H_v):
+        gate = KDA_GATE_PER_HEAD
+    else:
+        raise ValueError("g must be [B, T, H_v, d_k] or [B, T, H_v]")
+    for t in (q, k, v, g, beta, do, h0, dht, cu_seqlens):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("every tensor must be a contiguous CUDA tensor")
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    nb = N
+    if cu_seqlens is not None and B != 1:
+        raise ValueError("packed sequences need B == 1")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg = torch.empty_like(g)
+    dbeta = None if beta is None else torch.empty_like(beta)
+    dh0 = torch.empty((N, H_v, d_k, d_v), dtype=torch.float32, device=q.device) if want_dh0 else None
+    if scale is None:
+        scale = d_k ** -0.5
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    p = kda_bwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta) or None, _ptr(h0) or None,
+                       _ptr(do), _ptr(dht) or None, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                       _ptr(dbeta) or None, _ptr(dh0) or None, nb, T, H_k, H_v, d_k, d_v, chunk_size,
+                       float(scale), _ptr(cu_seqlens) or None, dtype, gate, 0)
+    st = kda_chunk_bwd(p, stream)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_bwd")
+    return dq, dk, dv, dg, dbeta, dh0

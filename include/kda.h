@@ -230,6 +230,46 @@ int kda_chunk_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cudaStr
  * separate pass with KDA_FLAG_UNFUSED_FRONTEND). */
 int kda_recurrent_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cudaStream_t stream);
 
+/*
+ * kda_chunk_bwd — the backward pass: gradients of L = sum(dO * o) + sum(dht * ht) with
+ * respect to q, k, v, g, beta and h0, for the forward pass that kda_chunk_fwd_ex computes
+ * with the same arguments ("Gated DeltaNet", "反向传播：状态伴随与三角变换梯度": the state
+ * adjoint runs backwards from dht through the chunks and the WY factors' gradients go back
+ * through the triangular inverse). The chunk factors and the chunk-entry states are
+ * recomputed from the inputs; all arithmetic is fp32.
+ *
+ * Forward arguments (q, k, v, g, beta, h0, sizes, scale, cu_seqlens, dtype, gate_mode) as
+ * in kda_fwd_params, and (all device pointers, contiguous, 16-byte aligned):
+ *   dO     [B, T, H_v, d_v], the dtype of q
+ *   dht    [N, H_v, d_k, d_v] fp32, or NULL (no gradient reaches the final state)
+ *   dq, dk [B, T, H_k, d_k], dv [B, T, H_v, d_v], the dtype of q (dq and dk sum the value
+ *          heads that share a key head)
+ *   dg     the shape of g (fp32): gradient of the natural-log gates
+ *   dbeta  [B, T, H_v] fp32; must be NULL when beta is NULL (decay-only)
+ *   dh0    [N, H_v, d_k, d_v] fp32, or NULL when not wanted (also when h0 is NULL: it is
+ *          then the gradient with respect to the zero initial state)
+ * Outputs are fully overwritten. Scratch: about 540 KB per (64-token chunk, value head)
+ * at d = 128 (the chunk factors, entry states and their adjoints), plus fp32 accumulators
+ * of dq and dk for bf16 outputs, all stream-ordered from the library's pool and freed on
+ * the same stream. Errors as kda_chunk_fwd_ex (flags must be 0).
+ */
+typedef struct kda_bwd_params {
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    const void *dO;
+    const float *dht;
+    void *dq, *dk, *dv;
+    float *dg, *dbeta, *dh0;
+    int B, T, H_k, H_v, d_k, d_v, C;
+    float scale;
+    const int32_t *cu_seqlens;
+    int dtype;     /* KDA_DTYPE_BF16 or KDA_DTYPE_F32 */
+    int gate_mode; /* KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD */
+    int flags;     /* 0 */
+} kda_bwd_params;
+
+int kda_chunk_bwd(const kda_bwd_params *p, cudaStream_t stream);
+
 /* A static, human-readable description of a status (and of the last CUDA error for
  * KDA_ERR_CUDA on this thread). */
 const char *kda_status_string(int status);

@@ -117,3 +117,24 @@ def test_fused_front_end_rejections():
         assert fn(p, kda.kda_frontend(1, 1, A, A), 0) == kda.KDA_ERR_UNSUPPORTED
         p.d_k = 128
     assert kda.lib().kda_chunk_fwd_fused(None, None, None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_backward_rejections():
+    # all checked on the host before any CUDA call
+    def params(**over):
+        p = kda.kda_bwd_params(A, A, A, A, A, None, A, None, A, A, A, A, A, None, 1, 64, 1, 1, 128, 128,
+                               64, 1.0, None, kda.KDA_DTYPE_BF16, kda.KDA_GATE_PER_CHANNEL, 0)
+        for key, val in over.items():
+            setattr(p, key, val)
+        return p
+
+    assert kda.kda_chunk_bwd(params(flags=1), 0) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_chunk_bwd(params(dO=None), 0) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_chunk_bwd(params(dq=None), 0) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_chunk_bwd(params(dbeta=None), 0) == kda.KDA_ERR_INVALID_ARG   # beta without dbeta
+    assert kda.kda_chunk_bwd(params(beta=None), 0) == kda.KDA_ERR_INVALID_ARG    # dbeta without beta
+    assert kda.kda_chunk_bwd(params(dO=A + 4), 0) == kda.KDA_ERR_ALIGNMENT
+    assert kda.kda_chunk_bwd(params(dh0=A + 8), 0) == kda.KDA_ERR_ALIGNMENT
+    assert kda.kda_chunk_bwd(params(d_k=96), 0) == kda.KDA_ERR_UNSUPPORTED
+    assert kda.kda_chunk_bwd(params(C=32), 0) == kda.KDA_ERR_UNSUPPORTED
+    assert kda.lib().kda_chunk_bwd(None, None) == kda.KDA_ERR_INVALID_ARG
