@@ -104,18 +104,34 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
+            // the next k step's tile is fetched into registers while this one is multiplied
+            float ra[4], rb[4];
+            auto fetch = [&](int k0) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int e = tid + kT * r;
+                    int m, k;
+                    if (ak == 1) { k = e & 15; m = e >> 4; } else { m = e & 63; k = e >> 6; }
+                    ra[r] = A[(int64_t)(m0 + m) * am + (int64_t)(k0 + k) * ak];
+                    int kb, n;
+                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & 15; n = e >> 4; }
+                    rb[r] = B[(int64_t)(k0 + kb) * bk + (int64_t)(n0 + n) * bn];
+                }
+            };
+            fetch(0);
             for (int k0 = 0; k0 < K; k0 += 16) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int e = tid + kT * r;
                     int m, k;
                     if (ak == 1) { k = e & 15; m = e >> 4; } else { m = e & 63; k = e >> 6; }
-                    As[k * 68 + m] = A[(int64_t)(m0 + m) * am + (int64_t)(k0 + k) * ak];
+                    As[k * 68 + m] = ra[r];
                     int kb, n;
                     if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & 15; n = e >> 4; }
-                    Bs[kb * 68 + n] = B[(int64_t)(k0 + kb) * bk + (int64_t)(n0 + n) * bn];
+                    Bs[kb * 68 + n] = rb[r];
                 }
                 __syncthreads();
+                if (k0 + 16 < K) fetch(k0 + 16);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
                     const float4 a4 = *reinterpret_cast<const float4 *>(As + kk * 68 + ty * 4);
@@ -138,6 +154,12 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
         }
     }
     __syncthreads();
+}
+
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
 }
 
 // Sequence bounds (fixed-length batches or packed sequences).
@@ -175,10 +197,14 @@ __device__ bool window_owner(const BwdArgs &a, int64_t s, int &n, int &c, int64_
 }
 
 // ---- prep: the chunk factors -----------------------------------------------------------------
+// Shared memory: GEMM stage, L and T [64][65], the row partial sums of T [4][64], gamma [64][K].
+size_t prep_smem(int K) { return sizeof(float) * ((size_t)kStageFloats + 2 * 64 * 65 + 4 * 64 + 64 * (size_t)K); }
+
 template <typename T, bool GATE_HEAD>
 __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
-    __shared__ __align__(16) float stage[kStageFloats];
-    __shared__ float Lsh[64 * 65];
+    extern __shared__ __align__(16) float psm[];
+    float *stage = psm, *Lsh = stage + kStageFloats, *Tsh = Lsh + 64 * 65, *red = Tsh + 64 * 65;
+    float *Gs = red + 4 * 64;
     int n, c, len;
     int64_t bos;
     if (!window_owner(a, blockIdx.y, n, c, bos, len)) return;
@@ -194,18 +220,24 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
     const int64_t sqk = (int64_t)a.H_k * K, sv = (int64_t)a.H_v * V;
     const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * K;
 
-    // gamma (natural log), per channel, rows past the end hold the last valid value
+    // gamma (natural log), per channel: the gate tile into shared memory (rows past the end
+    // zero, so that they keep the last valid value), then a running sum per channel
+    for (int e = tid; e < 64 * K; e += kT) {
+        const int t = e / K, i = e - t * K;
+        const int64_t r = bos + row0 + t;
+        Gs[e] = t < nv ? (GATE_HEAD ? a.g[r * sg + h] : a.g[r * sg + (int64_t)h * K + i]) : 0.f;
+    }
+    __syncthreads();
     for (int i = tid; i < K; i += kT) {
         float acc = 0.f;
         for (int t = 0; t < 64; ++t) {
-            if (t < nv) {
-                const int64_t r = bos + row0 + t;
-                acc += GATE_HEAD ? a.g[r * sg + h] : a.g[r * sg + (int64_t)h * K + i];
-            }
-            S[L.gm + t * K + i] = acc;
+            acc += Gs[t * K + i];
+            Gs[t * K + i] = acc;
         }
         S[L.eg + i] = expf(acc);
     }
+    __syncthreads();
+    for (int e = tid; e < 64 * K; e += kT) S[L.gm + e] = Gs[e];
     for (int t = tid; t < 64; t += kT)
         S[L.bt + t] = t < nv ? (a.decay_only ? 1.f : a.beta[(bos + row0 + t) * a.H_v + h]) : 0.f;
     __syncthreads();
@@ -214,7 +246,7 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
         const int64_t r = bos + row0 + t;
         const float kv = t < nv ? ldf<T>(k + r * sqk + (int64_t)hk * K + i) : 0.f;
         const float qv = t < nv ? ldf<T>(q + r * sqk + (int64_t)hk * K + i) : 0.f;
-        const float gam = S[L.gm + e], gn = S[L.gm + 63 * K + i];
+        const float gam = Gs[e], gn = Gs[63 * K + i];
         S[L.qp + e] = a.scale * qv * expf(gam);
         S[L.kp + e] = a.decay_only ? 0.f : kv * expf(gam);
         S[L.km + e] = kv * expf(-gam);
@@ -237,16 +269,22 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
         Lsh[t * 65 + s] = s < t ? S[L.bt + t] * S[L.m + e] : 0.f;  // L = diag(beta) M
     }
     __syncthreads();
-    // T = (I + L)^-1 by forward substitution, row by row: T[i] = e_i - sum_{j<i} L[i][j] T[j]
-    float *Tm = S + L.t;
-    for (int i = 0; i < 64; ++i) {
-        if (tid < 64) {
-            float acc = tid == i ? 1.f : 0.f;
-            for (int j = 0; j < i; ++j) acc = fmaf(-Lsh[i * 65 + j], Tm[j * 64 + tid], acc);
-            Tm[i * 64 + tid] = acc;
+    // T = (I + L)^-1 by forward substitution, row by row: T[i] = e_i - sum_{j<i} L[i][j] T[j];
+    // each row's sum is split over four groups of 64 threads (j = grp, grp + 4, ...)
+    {
+        const int col = tid & 63, grp = tid >> 6;
+        for (int i = 0; i < 64; ++i) {
+            float part = 0.f;
+            for (int j = grp; j < i; j += 4) part = fmaf(Lsh[i * 65 + j], Tsh[j * 65 + col], part);
+            red[grp * 64 + col] = part;
+            __syncthreads();
+            if (grp == 0)
+                Tsh[i * 65 + col] = (col == i ? 1.f : 0.f) - (red[col] + red[64 + col] + red[128 + col] + red[192 + col]);
+            __syncthreads();
         }
-        __syncthreads();
     }
+    float *Tm = S + L.t;
+    for (int e = tid; e < 4096; e += kT) Tm[e] = Tsh[(e >> 6) * 65 + (e & 63)];
     // W = T diag(beta) Kp, U = T diag(beta) V: scale the rows first (beta of row s)
     // (Kb as a temporary would be overwritten: use the dVt and Vt areas, free until the scans)
     float *Kbeta = S + L.wm;  // W's own area: the product goes to Vt's area first
@@ -254,11 +292,11 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
     float *Vbeta = S + L.dvt;
     for (int e = tid; e < 64 * V; e += kT) Vbeta[e] = S[L.bt + e / V] * S[L.vf + e];
     __syncthreads();
-    block_gemm(64, V, 64, 1.f, Tm, 64, 1, Vbeta, V, 1, S + L.u, V, 1, false, stage);
+    block_gemm(64, V, 64, 1.f, Tsh, 65, 1, Vbeta, V, 1, S + L.u, V, 1, false, stage);
     // W: T (64 x 64) times Kbeta (64 x K) into the dS' area (free until the adjoint scan),
     // then copied back over Kbeta
     float *Wtmp = S + L.dsx;
-    block_gemm(64, K, 64, 1.f, Tm, 64, 1, Kbeta, K, 1, Wtmp, K, 1, false, stage);
+    block_gemm(64, K, 64, 1.f, Tsh, 65, 1, Kbeta, K, 1, Wtmp, K, 1, false, stage);
     for (int e = tid; e < 64 * K; e += kT) S[L.wm + e] = Wtmp[e];
 }
 
@@ -363,10 +401,12 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
     // dKb = Vt dS'^T;  dW = -dVt S^T;  dEG = rows of dS' . S
     block_gemm(64, K, V, 1.f, Vt, V, 1, dSx, 1, V, dKb, K, 1, false, stage);
     block_gemm(64, K, V, -1.f, dVt, V, 1, Se, 1, V, dW, K, 1, false, stage);
-    for (int i = tid; i < K; i += kT) {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int i = warp; i < K; i += kT / 32) {  // a warp per row, lanes along it
         float s = 0.f;
-        for (int j = 0; j < V; ++j) s = fmaf(dSx[(int64_t)i * V + j], Se[(int64_t)i * V + j], s);
-        dEG[i] = s;
+        for (int j = lane; j < V; j += 32) s = fmaf(dSx[(int64_t)i * V + j], Se[(int64_t)i * V + j], s);
+        s = warp_sum(s);
+        if (lane == 0) dEG[i] = s;
     }
     for (int t = tid; t < 64; t += kT) dbeta[t] = 0.f;
     __syncthreads();
@@ -381,11 +421,12 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         // T^T dVt -> dW's area (dW is consumed)
         float *TtdU = dW;
         block_gemm(64, V, 64, 1.f, Tm, 1, 64, dVt, V, 1, TtdU, V, 1, false, stage);
-        for (int t = tid; t < 64; t += kT) {
+        for (int t = warp; t < 64; t += kT / 32) {
             float s = 0.f;
-            for (int i = 0; i < K; ++i) s = fmaf(dKp[t * K + i], Kp[t * K + i], s);
-            for (int j = 0; j < V; ++j) s = fmaf(TtdU[t * V + j], Vf[t * V + j], s);
-            dbeta[t] = s;
+            for (int i = lane; i < K; i += 32) s = fmaf(dKp[t * K + i], Kp[t * K + i], s);
+            for (int j = lane; j < V; j += 32) s = fmaf(TtdU[t * V + j], Vf[t * V + j], s);
+            s = warp_sum(s);
+            if (lane == 0) dbeta[t] = s;
         }
         __syncthreads();
         for (int e = tid; e < 64 * K; e += kT) dKp[e] *= Bt[e / K];
@@ -403,10 +444,11 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
             if ((e & 63) >= (e >> 6)) dL[e] = 0.f;
         __syncthreads();
         // dbeta += rows of dL . M;  dM = diag(beta) dL (in place)
-        for (int t = tid; t < 64; t += kT) {
+        for (int t = warp; t < 64; t += kT / 32) {
             float s = 0.f;
-            for (int s2 = 0; s2 < t; ++s2) s = fmaf(dL[t * 64 + s2], Mm[t * 64 + s2], s);
-            dbeta[t] += s;
+            for (int s2 = lane; s2 < t; s2 += 32) s = fmaf(dL[t * 64 + s2], Mm[t * 64 + s2], s);
+            s = warp_sum(s);
+            if (lane == 0) dbeta[t] += s;
         }
         __syncthreads();
         for (int e = tid; e < 4096; e += kT) dL[e] *= Bt[e >> 6];
@@ -472,10 +514,11 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
             }
         }
         __syncthreads();
-        for (int t = tid; t < nv; t += kT) {
+        for (int t = warp; t < nv; t += kT / 32) {
             float s = 0.f;
-            for (int i = 0; i < K; ++i) s += dgamma[t * K + i];
-            a.dg[(bos + row0 + t) * a.H_v + h] = s;
+            for (int i = lane; i < K; i += 32) s += dgamma[t * K + i];
+            s = warp_sum(s);
+            if (lane == 0) a.dg[(bos + row0 + t) * a.H_v + h] = s;
         }
     }
     if (!a.decay_only && a.dbeta != nullptr)
@@ -529,12 +572,16 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
     }
     const size_t scan_smem = sizeof(float) * ((size_t)K * 64 + kStageFloats);
     const size_t gsmem = grads_smem(K, V);
+    const size_t psmem = prep_smem(K);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_grads_kernel<T, GATE_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)gsmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_prep_kernel<T, GATE_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)psmem);
     if (e == cudaSuccess && windows > 0 && Ttot > 0) {
         const dim3 gw(a.H_v, (unsigned)windows);
-        bwd_prep_kernel<T, GATE_HEAD><<<gw, kT, 0, stream>>>(a);
+        bwd_prep_kernel<T, GATE_HEAD><<<gw, kT, psmem, stream>>>(a);
         e = cudaGetLastError();
         if (e == cudaSuccess) {
             bwd_states_kernel<<<dim3(V / 64, a.H_v, a.N), kT, scan_smem, stream>>>(a);
