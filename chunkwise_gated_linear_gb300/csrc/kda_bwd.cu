@@ -42,7 +42,9 @@ namespace kda {
 
 namespace {
 
-constexpr int kT = 256;  // threads of every backward kernel
+constexpr int kT = 512;            // threads of every backward kernel
+constexpr int kRows = kT / 16 == 32 ? 2 : 4;  // GEMM output rows per thread (16 column groups)
+constexpr int kLoads = 1024 / kT;  // staged elements of each operand tile per thread and k step
 
 // Per-slot scratch layout (floats). A slot holds one chunk of one unit.
 struct Lay {
@@ -90,7 +92,8 @@ __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
 // C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), fp32, every matrix given by
 // a base pointer (global or shared) and element strides: A(m, k) = A[m * am + k * ak],
 // B(k, n) = B[k * bk + n * bn], C(m, n) = C[m * cm + n * cn]. M and N are multiples of 64,
-// K of 16; C must not overlap A or B. Called by all kT threads; ends with a barrier.
+// K of 16; C must not overlap A or B. Called by all kT threads (each owns kRows x 4 outputs
+// of every 64 x 64 tile); ends with a barrier.
 constexpr int kStageFloats = 2 * 16 * 68;
 __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int64_t am, int64_t ak,
                            const float *B, int64_t bk, int64_t bn, float *C, int64_t cm, int64_t cn, bool acc,
@@ -99,16 +102,16 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     for (int m0 = 0; m0 < M; m0 += 64) {
         for (int n0 = 0; n0 < N; n0 += 64) {
-            float c[4][4];
+            float c[kRows][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < kRows; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
             // the next k step's tile is fetched into registers while this one is multiplied
-            float ra[4], rb[4];
+            float ra[kLoads], rb[kLoads];
             auto fetch = [&](int k0) {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
+                for (int r = 0; r < kLoads; ++r) {
                     const int e = tid + kT * r;
                     int m, k;
                     if (ak == 1) { k = e & 15; m = e >> 4; } else { m = e & 63; k = e >> 6; }
@@ -121,7 +124,7 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
             fetch(0);
             for (int k0 = 0; k0 < K; k0 += 16) {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
+                for (int r = 0; r < kLoads; ++r) {
                     const int e = tid + kT * r;
                     int m, k;
                     if (ak == 1) { k = e & 15; m = e >> 4; } else { m = e & 63; k = e >> 6; }
@@ -134,21 +137,28 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
                 if (k0 + 16 < K) fetch(k0 + 16);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(As + kk * 68 + ty * 4);
+                    float av[kRows];
+                    if constexpr (kRows == 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(As + kk * 68 + ty * 4);
+                        av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+                    } else {
+                        const float2 a2 = *reinterpret_cast<const float2 *>(As + kk * 68 + ty * 2);
+                        av[0] = a2.x; av[1] = a2.y;
+                    }
                     const float4 b4 = *reinterpret_cast<const float4 *>(Bs + kk * 68 + tx * 4);
-                    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+                    const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                    for (int i = 0; i < kRows; ++i)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) c[i][j] = fmaf(av[i], bv[j], c[i][j]);
                 }
                 __syncthreads();
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < kRows; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float *p = C + (int64_t)(m0 + ty * 4 + i) * cm + (int64_t)(n0 + tx * 4 + j) * cn;
+                    float *p = C + (int64_t)(m0 + ty * kRows + i) * cm + (int64_t)(n0 + tx * 4 + j) * cn;
                     *p = acc ? fmaf(alpha, c[i][j], *p) : alpha * c[i][j];
                 }
         }
@@ -197,14 +207,18 @@ __device__ bool window_owner(const BwdArgs &a, int64_t s, int &n, int &c, int64_
 }
 
 // ---- prep: the chunk factors -----------------------------------------------------------------
-// Shared memory: GEMM stage, L and T [64][65], the row partial sums of T [4][64], gamma [64][K].
-size_t prep_smem(int K) { return sizeof(float) * ((size_t)kStageFloats + 2 * 64 * 65 + 4 * 64 + 64 * (size_t)K); }
+// Shared memory: GEMM stage, L and T [64][65], the row partial sums of T [kT / 64][64],
+// gamma [64][K].
+constexpr int kGroups = kT / 64;
+size_t prep_smem(int K) {
+    return sizeof(float) * ((size_t)kStageFloats + 2 * 64 * 65 + kGroups * 64 + 64 * (size_t)K);
+}
 
 template <typename T, bool GATE_HEAD>
 __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float psm[];
     float *stage = psm, *Lsh = stage + kStageFloats, *Tsh = Lsh + 64 * 65, *red = Tsh + 64 * 65;
-    float *Gs = red + 4 * 64;
+    float *Gs = red + kGroups * 64;
     int n, c, len;
     int64_t bos;
     if (!window_owner(a, blockIdx.y, n, c, bos, len)) return;
@@ -270,16 +284,20 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
     }
     __syncthreads();
     // T = (I + L)^-1 by forward substitution, row by row: T[i] = e_i - sum_{j<i} L[i][j] T[j];
-    // each row's sum is split over four groups of 64 threads (j = grp, grp + 4, ...)
+    // each row's sum is split over kGroups groups of 64 threads (j = grp, grp + kGroups, ...)
     {
         const int col = tid & 63, grp = tid >> 6;
         for (int i = 0; i < 64; ++i) {
             float part = 0.f;
-            for (int j = grp; j < i; j += 4) part = fmaf(Lsh[i * 65 + j], Tsh[j * 65 + col], part);
+            for (int j = grp; j < i; j += kGroups) part = fmaf(Lsh[i * 65 + j], Tsh[j * 65 + col], part);
             red[grp * 64 + col] = part;
             __syncthreads();
-            if (grp == 0)
-                Tsh[i * 65 + col] = (col == i ? 1.f : 0.f) - (red[col] + red[64 + col] + red[128 + col] + red[192 + col]);
+            if (grp == 0) {
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < kGroups; ++q) sum += red[q * 64 + col];
+                Tsh[i * 65 + col] = (col == i ? 1.f : 0.f) - sum;
+            }
             __syncthreads();
         }
     }
@@ -300,13 +318,31 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
     for (int e = tid; e < 64 * K; e += kT) S[L.wm + e] = Wtmp[e];
 }
 
-// ---- states: the forward scan, S^T slice [K][64 columns] in shared memory -----------------
+// Copy n floats (a multiple of 4, both ends 16-byte aligned) global -> shared with cp.async,
+// all kT threads; `rows` rows of `cols` floats with the given global row stride.
+__device__ __forceinline__ void stage_rows(float *dst, const float *src, int rows, int cols, int64_t stride) {
+    const int per = cols / 4;
+    for (int e = threadIdx.x; e < rows * per; e += kT) {
+        const int r = e / per, c4 = e - r * per;
+        cp_async_16(dst + r * cols + 4 * c4, src + r * stride + 4 * c4, 16);
+    }
+}
+
+// ---- states: the forward scan, S slice [K][64 columns] in shared memory -----------------------
+// Per chunk the operands (W, Kb [64][K], U's 64 columns, e^Gn) are copied into shared memory
+// first, so that the products read no global memory.
+size_t states_smem(int K) { return sizeof(float) * ((size_t)K * 64 * 3 + 64 * 64 + K + kStageFloats); }
+
 __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
-    float *St = sm;                      // S [K][64]
-    float *stage = sm + a.d_k * 64;
-    const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
+    float *St = sm;              // S [K][64]
+    float *Ws = St + K * 64;     // W [64][K]
+    float *Kbs = Ws + 64 * K;    // Kb [64][K]
+    float *Us = Kbs + 64 * K;    // U, then Vt [64][64]
+    float *EGs = Us + 64 * 64;   // e^Gn [K]
+    float *stage = EGs + K;
+    const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const Lay L = make_lay(K, V);
     int64_t bos;
     int len;
@@ -319,26 +355,42 @@ __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     __syncthreads();
     for (int c = 0; c < nch; ++c) {
         float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+        stage_rows(Ws, S + L.wm, 64, K, K);
+        stage_rows(Kbs, S + L.kb, 64, K, K);
+        stage_rows(Us, S + L.u + j0, 64, 64, V);
+        stage_rows(EGs, S + L.eg, 1, K, K);
+        cp_async_commit();
         for (int e = tid; e < K * 64; e += kT) S[L.se + (int64_t)(e >> 6) * V + j0 + (e & 63)] = St[e];
-        // Vt = U - W S
-        float *Vt = S + L.vt + j0;
-        for (int e = tid; e < 64 * 64; e += kT) Vt[(e >> 6) * V + (e & 63)] = S[L.u + (e >> 6) * V + j0 + (e & 63)];
+        cp_async_wait_all();
         __syncthreads();
-        block_gemm(64, 64, K, -1.f, S + L.wm, K, 1, St, 64, 1, Vt, V, 1, true, stage);
+        // Vt = U - W S (in U's place), stored for the gradient kernel
+        block_gemm(64, 64, K, -1.f, Ws, K, 1, St, 64, 1, Us, 64, 1, true, stage);
+        for (int e = tid; e < 64 * 64; e += kT) S[L.vt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = Us[e];
         // S <- diag(EG) S + Kb^T Vt
-        for (int e = tid; e < K * 64; e += kT) St[e] *= S[L.eg + (e >> 6)];
+        for (int e = tid; e < K * 64; e += kT) St[e] *= EGs[e >> 6];
         __syncthreads();
-        block_gemm(K, 64, 64, 1.f, S + L.kb, 1, K, Vt, V, 1, St, 64, 1, true, stage);
+        block_gemm(K, 64, 64, 1.f, Kbs, 1, K, Us, 64, 1, St, 64, 1, true, stage);
     }
 }
 
-// ---- adjoint: the reverse scan, dS^T slice [K][64 columns] in shared memory ---------------
+// ---- adjoint: the reverse scan, dS slice [K][64 columns] in shared memory -------------------
+size_t adjoint_smem(int K) {
+    return sizeof(float) * ((size_t)K * 64 * 4 + 3 * 64 * 64 + K + kStageFloats);
+}
+
 __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
-    float *dS = sm;  // [K][64]
-    float *stage = sm + a.d_k * 64;
-    const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
+    float *dS = sm;               // dS [K][64]
+    float *Kbs = dS + K * 64;     // Kb [64][K]
+    float *Qps = Kbs + 64 * K;    // Qp [64][K]
+    float *Ws = Qps + 64 * K;     // W [64][K]
+    float *As = Ws + 64 * K;      // A [64][64]
+    float *dOs = As + 64 * 64;    // dO's 64 columns [64][64]
+    float *dVs = dOs + 64 * 64;   // dVt [64][64]
+    float *EGs = dVs + 64 * 64;   // e^Gn [K]
+    float *stage = EGs + K;
+    const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const Lay L = make_lay(K, V);
     int64_t bos;
     int len;
@@ -351,16 +403,25 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     __syncthreads();
     for (int c = nch - 1; c >= 0; --c) {
         float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+        stage_rows(Kbs, S + L.kb, 64, K, K);
+        stage_rows(Qps, S + L.qp, 64, K, K);
+        stage_rows(Ws, S + L.wm, 64, K, K);
+        stage_rows(As, S + L.a, 64, 64, 64);
+        stage_rows(dOs, S + L.dof + j0, 64, 64, V);
+        stage_rows(EGs, S + L.eg, 1, K, K);
+        cp_async_commit();
         for (int e = tid; e < K * 64; e += kT) S[L.dsx + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dS[e];
-        float *dVt = S + L.dvt + j0;
-        // dVt = A^T dO + Kb dS'
-        block_gemm(64, 64, 64, 1.f, S + L.a, 1, 64, S + L.dof + j0, V, 1, dVt, V, 1, false, stage);
-        block_gemm(64, 64, K, 1.f, S + L.kb, K, 1, dS, 64, 1, dVt, V, 1, true, stage);
-        // dS <- diag(EG) dS' + Qp^T dO - W^T dVt
-        for (int e = tid; e < K * 64; e += kT) dS[e] *= S[L.eg + (e >> 6)];
+        cp_async_wait_all();
         __syncthreads();
-        block_gemm(K, 64, 64, 1.f, S + L.qp, 1, K, S + L.dof + j0, V, 1, dS, 64, 1, true, stage);
-        block_gemm(K, 64, 64, -1.f, S + L.wm, 1, K, dVt, V, 1, dS, 64, 1, true, stage);
+        // dVt = A^T dO + Kb dS', stored for the gradient kernel
+        block_gemm(64, 64, 64, 1.f, As, 1, 64, dOs, 64, 1, dVs, 64, 1, false, stage);
+        block_gemm(64, 64, K, 1.f, Kbs, K, 1, dS, 64, 1, dVs, 64, 1, true, stage);
+        for (int e = tid; e < 64 * 64; e += kT) S[L.dvt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dVs[e];
+        // dS <- diag(EG) dS' + Qp^T dO - W^T dVt
+        for (int e = tid; e < K * 64; e += kT) dS[e] *= EGs[e >> 6];
+        __syncthreads();
+        block_gemm(K, 64, 64, 1.f, Qps, 1, K, dOs, 64, 1, dS, 64, 1, true, stage);
+        block_gemm(K, 64, 64, -1.f, Ws, 1, K, dVs, 64, 1, dS, 64, 1, true, stage);
     }
     if (a.dh0 != nullptr)
         for (int e = tid; e < K * 64; e += kT)
@@ -570,7 +631,7 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
         e = cudaMemsetAsync(a.dq_acc, 0, sizeof(float) * acc_elems, stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(a.dk_acc, 0, sizeof(float) * acc_elems, stream);
     }
-    const size_t scan_smem = sizeof(float) * ((size_t)K * 64 + kStageFloats);
+    const size_t ssmem = states_smem(K), asmem = adjoint_smem(K);
     const size_t gsmem = grads_smem(K, V);
     const size_t psmem = prep_smem(K);
     if (e == cudaSuccess)
@@ -579,16 +640,20 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_prep_kernel<T, GATE_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)psmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_adjoint_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)asmem);
     if (e == cudaSuccess && windows > 0 && Ttot > 0) {
         const dim3 gw(a.H_v, (unsigned)windows);
         bwd_prep_kernel<T, GATE_HEAD><<<gw, kT, psmem, stream>>>(a);
         e = cudaGetLastError();
         if (e == cudaSuccess) {
-            bwd_states_kernel<<<dim3(V / 64, a.H_v, a.N), kT, scan_smem, stream>>>(a);
+            bwd_states_kernel<<<dim3(V / 64, a.H_v, a.N), kT, ssmem, stream>>>(a);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) {
-            bwd_adjoint_kernel<<<dim3(V / 64, a.H_v, a.N), kT, scan_smem, stream>>>(a);
+            bwd_adjoint_kernel<<<dim3(V / 64, a.H_v, a.N), kT, asmem, stream>>>(a);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) {
