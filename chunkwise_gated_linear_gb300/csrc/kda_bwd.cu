@@ -44,7 +44,8 @@ namespace {
 
 constexpr int kT = 512;            // threads of every backward kernel
 constexpr int kRows = kT / 16 == 32 ? 2 : 4;  // GEMM output rows per thread (16 column groups)
-constexpr int kLoads = 1024 / kT;  // staged elements of each operand tile per thread and k step
+constexpr int kKS = 32;             // k step of the GEMM
+constexpr int kLoads = 64 * kKS / kT;  // staged elements of each operand tile per thread and k step
 
 // Per-slot scratch layout (floats). A slot holds one chunk of one unit.
 struct Lay {
@@ -92,13 +93,13 @@ __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
 // C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), fp32, every matrix given by
 // a base pointer (global or shared) and element strides: A(m, k) = A[m * am + k * ak],
 // B(k, n) = B[k * bk + n * bn], C(m, n) = C[m * cm + n * cn]. M and N are multiples of 64,
-// K of 16; C must not overlap A or B. Called by all kT threads (each owns kRows x 4 outputs
+// K of 32; C must not overlap A or B. Called by all kT threads (each owns kRows x 4 outputs
 // of every 64 x 64 tile); ends with a barrier.
-constexpr int kStageFloats = 2 * 16 * 68;
+constexpr int kStageFloats = 2 * kKS * 68;
 __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int64_t am, int64_t ak,
                            const float *B, int64_t bk, int64_t bn, float *C, int64_t cm, int64_t cn, bool acc,
                            float *stage) {
-    float *As = stage, *Bs = stage + 16 * 68;
+    float *As = stage, *Bs = stage + kKS * 68;
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     for (int m0 = 0; m0 < M; m0 += 64) {
         for (int n0 = 0; n0 < N; n0 += 64) {
@@ -114,29 +115,29 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
                 for (int r = 0; r < kLoads; ++r) {
                     const int e = tid + kT * r;
                     int m, k;
-                    if (ak == 1) { k = e & 15; m = e >> 4; } else { m = e & 63; k = e >> 6; }
+                    if (ak == 1) { k = e & (kKS - 1); m = e / kKS; } else { m = e & 63; k = e >> 6; }
                     ra[r] = A[(int64_t)(m0 + m) * am + (int64_t)(k0 + k) * ak];
                     int kb, n;
-                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & 15; n = e >> 4; }
+                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & (kKS - 1); n = e / kKS; }
                     rb[r] = B[(int64_t)(k0 + kb) * bk + (int64_t)(n0 + n) * bn];
                 }
             };
             fetch(0);
-            for (int k0 = 0; k0 < K; k0 += 16) {
+            for (int k0 = 0; k0 < K; k0 += kKS) {
 #pragma unroll
                 for (int r = 0; r < kLoads; ++r) {
                     const int e = tid + kT * r;
                     int m, k;
-                    if (ak == 1) { k = e & 15; m = e >> 4; } else { m = e & 63; k = e >> 6; }
+                    if (ak == 1) { k = e & (kKS - 1); m = e / kKS; } else { m = e & 63; k = e >> 6; }
                     As[k * 68 + m] = ra[r];
                     int kb, n;
-                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & 15; n = e >> 4; }
+                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & (kKS - 1); n = e / kKS; }
                     Bs[kb * 68 + n] = rb[r];
                 }
                 __syncthreads();
-                if (k0 + 16 < K) fetch(k0 + 16);
+                if (k0 + kKS < K) fetch(k0 + kKS);
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
+                for (int kk = 0; kk < kKS; ++kk) {
                     float av[kRows];
                     if constexpr (kRows == 4) {
                         const float4 a4 = *reinterpret_cast<const float4 *>(As + kk * 68 + ty * 4);
@@ -441,8 +442,8 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
     const int KV = K > V ? K : V;
     float *dQp = sm, *dKp = dQp + 64 * K, *dKm = dKp + 64 * K, *dKb = dKm + 64 * K;
     float *dW = dKb + 64 * K;  // [64][KV]
-    float *dA = dW + 64 * KV, *dT = dA + 4096, *X = dT + 4096;
-    float *dEG = X + 4096, *dGn = dEG + 128, *dbeta = dGn + 128;
+    float *dA = dW + 64 * KV, *dT = dA + 4096, *X = dA;  // X reuses dA once dA is consumed
+    float *dEG = dT + 4096, *dGn = dEG + 128, *dbeta = dGn + 128;
     float *stage = dbeta + 64;
     const Lay L = make_lay(K, V);
     const float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
@@ -459,6 +460,8 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         if ((e & 63) > (e >> 6)) dA[e] = 0.f;
     __syncthreads();
     block_gemm(64, K, 64, 1.f, dA, 64, 1, Km, K, 1, dQp, K, 1, true, stage);
+    // dKm = dA^T Qp (dA is not needed after this)
+    block_gemm(64, K, 64, 1.f, dA, 1, 64, Qp, K, 1, dKm, K, 1, false, stage);
     // dKb = Vt dS'^T;  dW = -dVt S^T;  dEG = rows of dS' . S
     block_gemm(64, K, V, 1.f, Vt, V, 1, dSx, 1, V, dKb, K, 1, false, stage);
     block_gemm(64, K, V, -1.f, dVt, V, 1, Se, 1, V, dW, K, 1, false, stage);
@@ -514,9 +517,9 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         __syncthreads();
         for (int e = tid; e < 4096; e += kT) dL[e] *= Bt[e >> 6];
         __syncthreads();
-        // dKp += dM Km;  dKm = dM^T Kp
+        // dKp += dM Km;  dKm += dM^T Kp
         block_gemm(64, K, 64, 1.f, dL, 64, 1, Km, K, 1, dKp, K, 1, true, stage);
-        block_gemm(64, K, 64, 1.f, dL, 1, 64, Kp, K, 1, dKm, K, 1, false, stage);
+        block_gemm(64, K, 64, 1.f, dL, 1, 64, Kp, K, 1, dKm, K, 1, true, stage);
     } else {
         // decay-only: U = V, W = 0: dv = dVt
         T *dv = static_cast<T *>(a.dv);
@@ -524,14 +527,9 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
             const int t = e / V, j = e - t * V;
             if (t < nv) stf<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j, dVt[e]);
         }
-        for (int e = tid; e < 64 * K; e += kT) {
-            dKp[e] = 0.f;
-            dKm[e] = 0.f;
-        }
+        for (int e = tid; e < 64 * K; e += kT) dKp[e] = 0.f;
         __syncthreads();
     }
-    // dKm += dA^T Qp
-    block_gemm(64, K, 64, 1.f, dA, 1, 64, Qp, K, 1, dKm, K, 1, true, stage);
 
     // dq, dk (atomically: value heads of one key head share rows), dgamma in dQp's area
     float *dqa = a.dq_acc, *dka = a.dk_acc;
@@ -594,7 +592,7 @@ __global__ void __launch_bounds__(kT) bwd_finish_kernel(const float *acc, T *out
 
 size_t grads_smem(int K, int V) {
     const int KV = K > V ? K : V;
-    return sizeof(float) * ((size_t)4 * 64 * K + (size_t)64 * KV + 3 * 4096 + 128 + 128 + 64 + kStageFloats);
+    return sizeof(float) * ((size_t)4 * 64 * K + (size_t)64 * KV + 2 * 4096 + 128 + 128 + 64 + kStageFloats);
 }
 
 template <typename T, bool GATE_HEAD>

@@ -370,8 +370,11 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
     uint32_t pend = 0;
 
     // Bulk copies issued by one thread are served one after another; the copies of a job
-    // are spread over the lane 0 of different warps so that they overlap.
-    constexpr int kIssQ = 0, kIssK = 32, kIssG = 64, kIssImg = 96;
+    // are spread over the lane 0 of different warps so that they overlap. The issuers are
+    // threads that load nothing with cp.async (beta and the per-head gates come from threads
+    // 0-127): a thread's cp.async wait was measured to also wait for its own bulk copies
+    // still in flight, which held the whole stage at the next barrier.
+    constexpr int kIssQ = 128, kIssK = 160, kIssG = 192, kIssImg = 224;
     auto stage_qk = [&](const JobIt &j, int jo) {
         if (ptid == kIssQ || ptid == kIssK) {
             const int hk = (j.u % a.H_v) / a.group;
@@ -455,7 +458,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             }
         }
 
-        cp_async_wait_all();  // this job's beta and per-head gates (own copies)
+        if (ptid < (GATE_HEAD ? 128 : 64)) cp_async_wait_all();  // this job's beta and per-head gates
         if constexpr (FE) {
             // each thread transforms the values it loaded itself (rows past the end stay 0)
             if (ptid < 64) {
