@@ -81,6 +81,9 @@ PROFILE_WORKLOADS = {
         "kda_decayonly_b2_t8192_h32_d128_bf16", (8192,) * 2, 32, 32, 128, 128, h0=True, beta=False),
     "kda_b1_t8192_h32_d128_bf16": Workload(
         "kda_b1_t8192_h32_d128_bf16", (8192,), 32, 32, 128, 128, h0=True),
+    # a short case of the backward for profiler captures (its scratch still exceeds L2)
+    "kda_b1_t2048_h32_d128_bf16": Workload(
+        "kda_b1_t2048_h32_d128_bf16", (2048,), 32, 32, 128, 128, h0=True),
     # the benchmark's 64 units (so the same ring depth and launch split) over half the tokens
     "kda_b2_t4096_h32_d128_bf16": Workload(
         "kda_b2_t4096_h32_d128_bf16", (4096,) * 2, 32, 32, 128, 128, h0=True),
