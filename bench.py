@@ -88,7 +88,7 @@ def backward_bytes(x) -> int:
 
 
 def backward_flops(x, C=64) -> int:
-    """fp32 FLOPs of the backward's contractions as this library runs them, per (chunk,
+    """Useful FLOPs of the backward's contractions as this library runs them, per (chunk,
     value head): the recomputed chunk factors (Gram, Aqk, U, W), the forward state scan
     (W S, Kb^T Vt), the adjoint scan (A^T dO, Kb dS, Qp^T dO, W^T dVt) and the gradients
     (dO S^T, dO Vt^T, dA Km, Vt dS^T, dVt S^T, dW Kp^T, dVt V^T, T^T dW, T^T dVt, dT T^T,
@@ -447,13 +447,19 @@ def run_ours(args, world, rank, local, pg):
         print(json.dumps(line), flush=True)
 
 
-# fp32 FMA peak of the GPU: SMs x 128 FMA lanes per clock x 2 FLOP x the maximum SM clock
-# (2070 MHz on the GB300s here); the backward's contractions run on these units.
-FP32_LANES_PER_SM = 128
+# The backward's contractions run on the tensor cores in tf32 (split operands, three
+# products each). Their peak is the measured bf16 dense rate times the nominal tf32 / bf16
+# ratio (1.1 / 2.25 PFLOP/s dense on GB300).
+TF32_OVER_BF16 = 1.1 / 2.25
 
 
-def fp32_peak_tflops(sms: int, mhz: float) -> float:
-    return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+def tf32_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]) * TF32_OVER_BF16, "measured bf16 x nominal tf32/bf16 ratio"
+    return 1900.0 * TF32_OVER_BF16, "fallback bf16 x nominal tf32/bf16 ratio"
 
 
 def run_backward(args, world, rank, local, pg):
@@ -553,11 +559,9 @@ def run_backward(args, world, rank, local, pg):
     h2d = sum(H[key].numel() * H[key].element_size() for key in inputs)
     d2h = sum(H[key].numel() * H[key].element_size() for key in results)
 
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    mhz = clocks.get("sm_max_mhz") or 2070.0
     flops = backward_flops(x)
     tflops = flops / (ms / 1000.0) / 1e12
-    peak = fp32_peak_tflops(sms, mhz)
+    peak, tc_kind = tf32_peak()
     hbm_peak, peak_kind = load_peaks()
     abytes = backward_bytes(x)
     if rank == 0:
@@ -574,8 +578,8 @@ def run_backward(args, world, rank, local, pg):
                        "l2": f"inputs larger than L2 ({abytes / 1e6:.0f} MB per step), no flush"},
             "e2e": {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tflops / peak, "traffic": None, "peak_kind": "derived: fp32 FMA lanes x clock",
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None, "peak_kind": tc_kind,
                          "algorithmic_flops_per_launch": flops, "kernel": "backward (prep, states, adjoint, grads, finish)",
                          "hbm_bytes_per_launch": abytes, "hbm_frac": abytes / (ms / 1000.0) / 1e9 / hbm_peak},
             "cpu_baseline": None,

@@ -43,7 +43,6 @@ namespace kda {
 namespace {
 
 constexpr int kT = 512;            // threads of every backward kernel
-constexpr int kRows = kT / 16 == 32 ? 2 : 4;  // GEMM output rows per thread (16 column groups)
 constexpr int kKS = 32;             // k step of the GEMM
 constexpr int kLoads = 64 * kKS / kT;  // staged elements of each operand tile per thread and k step
 
@@ -90,25 +89,47 @@ __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
     *p = __float2bfloat16_rn(v);
 }
 
+// tf32 tensor-core product on split operands: x = hi + lo with hi = tf32(x), lo = tf32(x -
+// hi); a b ~ hi_a hi_b + hi_a lo_b + lo_a hi_b ("3xTF32"), whose error is about that of an
+// fp32 product (the dropped lo_a lo_b term is below 2^-22 relative).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), fp32, every matrix given by
 // a base pointer (global or shared) and element strides: A(m, k) = A[m * am + k * ak],
 // B(k, n) = B[k * bk + n * bn], C(m, n) = C[m * cm + n * cn]. M and N are multiples of 64,
-// K of 32; C must not overlap A or B. Called by all kT threads (each owns kRows x 4 outputs
-// of every 64 x 64 tile); ends with a barrier.
-constexpr int kStageFloats = 2 * kKS * 68;
+// K of 32; C must not overlap A or B. Called by all kT threads; ends with a barrier.
+// Each 64 x 64 output tile is split over the 16 warps as 16 x 16 blocks (two m16n8
+// accumulators per warp) on tf32 mma.sync with split operands (3xTF32); the operand tiles
+// go through shared memory in 32-deep k steps, the next one fetched into registers while
+// the current one is multiplied.
+constexpr int kSP = 72;  // row stride of the staged tiles (conflict-free fragment reads)
+constexpr int kStageFloats = 2 * kKS * kSP;
 __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int64_t am, int64_t ak,
                            const float *B, int64_t bk, int64_t bn, float *C, int64_t cm, int64_t cn, bool acc,
                            float *stage) {
-    float *As = stage, *Bs = stage + kKS * 68;
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    static_assert(kT == 512, "16 warps: 4 x 4 blocks of 16 x 16 per 64 x 64 tile");
+    float *As = stage, *Bs = stage + kKS * kSP;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int mb = (warp & 3) * 16, nb = (warp >> 2) * 16;
     for (int m0 = 0; m0 < M; m0 += 64) {
         for (int n0 = 0; n0 < N; n0 += 64) {
-            float c[kRows][4];
-#pragma unroll
-            for (int i = 0; i < kRows; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
-            // the next k step's tile is fetched into registers while this one is multiplied
+            float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             float ra[kLoads], rb[kLoads];
             auto fetch = [&](int k0) {
 #pragma unroll
@@ -129,38 +150,41 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
                     const int e = tid + kT * r;
                     int m, k;
                     if (ak == 1) { k = e & (kKS - 1); m = e / kKS; } else { m = e & 63; k = e >> 6; }
-                    As[k * 68 + m] = ra[r];
+                    As[k * kSP + m] = ra[r];
                     int kb, n;
                     if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & (kKS - 1); n = e / kKS; }
-                    Bs[kb * 68 + n] = rb[r];
+                    Bs[kb * kSP + n] = rb[r];
                 }
                 __syncthreads();
                 if (k0 + kKS < K) fetch(k0 + kKS);
 #pragma unroll
-                for (int kk = 0; kk < kKS; ++kk) {
-                    float av[kRows];
-                    if constexpr (kRows == 4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(As + kk * 68 + ty * 4);
-                        av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
-                    } else {
-                        const float2 a2 = *reinterpret_cast<const float2 *>(As + kk * 68 + ty * 2);
-                        av[0] = a2.x; av[1] = a2.y;
+                for (int k8 = 0; k8 < kKS; k8 += 8) {
+                    // A (16 x 8): rows mb + g, mb + g + 8; columns k8 + t, k8 + t + 4
+                    uint32_t ah[4], al[4];
+                    split_tf32(As[(k8 + t) * kSP + mb + g], ah[0], al[0]);
+                    split_tf32(As[(k8 + t) * kSP + mb + g + 8], ah[1], al[1]);
+                    split_tf32(As[(k8 + t + 4) * kSP + mb + g], ah[2], al[2]);
+                    split_tf32(As[(k8 + t + 4) * kSP + mb + g + 8], ah[3], al[3]);
+#pragma unroll
+                    for (int f = 0; f < 2; ++f) {
+                        // B (8 x 8): rows k8 + t, k8 + t + 4; column nb + 8 f + g
+                        uint32_t bh0, bl0, bh1, bl1;
+                        split_tf32(Bs[(k8 + t) * kSP + nb + 8 * f + g], bh0, bl0);
+                        split_tf32(Bs[(k8 + t + 4) * kSP + nb + 8 * f + g], bh1, bl1);
+                        mma_m16n8k8_tf32(c[f], al, bh0, bh1);
+                        mma_m16n8k8_tf32(c[f], ah, bl0, bl1);
+                        mma_m16n8k8_tf32(c[f], ah, bh0, bh1);
                     }
-                    const float4 b4 = *reinterpret_cast<const float4 *>(Bs + kk * 68 + tx * 4);
-                    const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                    for (int i = 0; i < kRows; ++i)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) c[i][j] = fmaf(av[i], bv[j], c[i][j]);
                 }
                 __syncthreads();
             }
 #pragma unroll
-            for (int i = 0; i < kRows; ++i)
+            for (int f = 0; f < 2; ++f)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float *p = C + (int64_t)(m0 + ty * kRows + i) * cm + (int64_t)(n0 + tx * 4 + j) * cn;
-                    *p = acc ? fmaf(alpha, c[i][j], *p) : alpha * c[i][j];
+                for (int q = 0; q < 4; ++q) {
+                    const int m = m0 + mb + g + (q >= 2 ? 8 : 0), n = n0 + nb + 8 * f + 2 * t + (q & 1);
+                    float *p = C + (int64_t)m * cm + (int64_t)n * cn;
+                    *p = acc ? fmaf(alpha, c[f][q], *p) : alpha * c[f][q];
                 }
         }
     }
