@@ -114,11 +114,14 @@ __device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (
 // B(k, n) = B[k * bk + n * bn], C(m, n) = C[m * cm + n * cn]. M and N are multiples of 64,
 // K of 32; C must not overlap A or B. Called by all kT threads; ends with a barrier.
 // Each 64 x 64 output tile is split over the 16 warps as 16 x 16 blocks (two m16n8
-// accumulators per warp) on tf32 mma.sync with split operands (3xTF32); the operand tiles
-// go through shared memory in 32-deep k steps, the next one fetched into registers while
-// the current one is multiplied.
+// accumulators per warp) on tf32 mma.sync: with SPLIT the operands are split (3xTF32,
+// fp32-grade products; fp32 inputs), else rounded to tf32 once (10-bit mantissa products,
+// fp32 accumulation; bf16 inputs, whose gradients are rounded to bf16 or compared at that
+// level). The operand tiles go through shared memory in 32-deep k steps, the next one
+// fetched into registers while the current one is multiplied.
 constexpr int kSP = 72;  // row stride of the staged tiles (conflict-free fragment reads)
 constexpr int kStageFloats = 2 * kKS * kSP;
+template <bool SPLIT>
 __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int64_t am, int64_t ak,
                            const float *B, int64_t bk, int64_t bn, float *C, int64_t cm, int64_t cn, bool acc,
                            float *stage) {
@@ -160,20 +163,35 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
 #pragma unroll
                 for (int k8 = 0; k8 < kKS; k8 += 8) {
                     // A (16 x 8): rows mb + g, mb + g + 8; columns k8 + t, k8 + t + 4
+                    const float a0 = As[(k8 + t) * kSP + mb + g], a1 = As[(k8 + t) * kSP + mb + g + 8];
+                    const float a2 = As[(k8 + t + 4) * kSP + mb + g], a3 = As[(k8 + t + 4) * kSP + mb + g + 8];
                     uint32_t ah[4], al[4];
-                    split_tf32(As[(k8 + t) * kSP + mb + g], ah[0], al[0]);
-                    split_tf32(As[(k8 + t) * kSP + mb + g + 8], ah[1], al[1]);
-                    split_tf32(As[(k8 + t + 4) * kSP + mb + g], ah[2], al[2]);
-                    split_tf32(As[(k8 + t + 4) * kSP + mb + g + 8], ah[3], al[3]);
+                    if constexpr (SPLIT) {
+                        split_tf32(a0, ah[0], al[0]);
+                        split_tf32(a1, ah[1], al[1]);
+                        split_tf32(a2, ah[2], al[2]);
+                        split_tf32(a3, ah[3], al[3]);
+                    } else {
+                        ah[0] = to_tf32(a0);
+                        ah[1] = to_tf32(a1);
+                        ah[2] = to_tf32(a2);
+                        ah[3] = to_tf32(a3);
+                    }
 #pragma unroll
                     for (int f = 0; f < 2; ++f) {
                         // B (8 x 8): rows k8 + t, k8 + t + 4; column nb + 8 f + g
-                        uint32_t bh0, bl0, bh1, bl1;
-                        split_tf32(Bs[(k8 + t) * kSP + nb + 8 * f + g], bh0, bl0);
-                        split_tf32(Bs[(k8 + t + 4) * kSP + nb + 8 * f + g], bh1, bl1);
-                        mma_m16n8k8_tf32(c[f], al, bh0, bh1);
-                        mma_m16n8k8_tf32(c[f], ah, bl0, bl1);
-                        mma_m16n8k8_tf32(c[f], ah, bh0, bh1);
+                        const float b0 = Bs[(k8 + t) * kSP + nb + 8 * f + g];
+                        const float b1 = Bs[(k8 + t + 4) * kSP + nb + 8 * f + g];
+                        if constexpr (SPLIT) {
+                            uint32_t bh0, bl0, bh1, bl1;
+                            split_tf32(b0, bh0, bl0);
+                            split_tf32(b1, bh1, bl1);
+                            mma_m16n8k8_tf32(c[f], al, bh0, bh1);
+                            mma_m16n8k8_tf32(c[f], ah, bl0, bl1);
+                            mma_m16n8k8_tf32(c[f], ah, bh0, bh1);
+                        } else {
+                            mma_m16n8k8_tf32(c[f], ah, to_tf32(b0), to_tf32(b1));
+                        }
                     }
                 }
                 __syncthreads();
@@ -239,8 +257,10 @@ size_t prep_smem(int K) {
     return sizeof(float) * ((size_t)kStageFloats + 2 * 64 * 65 + kGroups * 64 + 64 * (size_t)K);
 }
 
+// two CTAs per SM (64 registers a thread): the kernel is latency-bound
 template <typename T, bool GATE_HEAD>
-__global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kT, 2) bwd_prep_kernel(const BwdArgs a) {
+    constexpr bool SPLIT = std::is_same<T, float>::value;
     extern __shared__ __align__(16) float psm[];
     float *stage = psm, *Lsh = stage + kStageFloats, *Tsh = Lsh + 64 * 65, *red = Tsh + 64 * 65;
     float *Gs = red + kGroups * 64;
@@ -299,8 +319,8 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
     }
     __syncthreads();
     // M = Kp Km^T (strictly lower), A = Qp Km^T (lower with the diagonal)
-    block_gemm(64, 64, K, 1.f, S + L.kp, K, 1, S + L.km, 1, K, S + L.m, 64, 1, false, stage);
-    block_gemm(64, 64, K, 1.f, S + L.qp, K, 1, S + L.km, 1, K, S + L.a, 64, 1, false, stage);
+    block_gemm<SPLIT>(64, 64, K, 1.f, S + L.kp, K, 1, S + L.km, 1, K, S + L.m, 64, 1, false, stage);
+    block_gemm<SPLIT>(64, 64, K, 1.f, S + L.qp, K, 1, S + L.km, 1, K, S + L.a, 64, 1, false, stage);
     for (int e = tid; e < 64 * 64; e += kT) {
         const int t = e >> 6, s = e & 63;
         if (s >= t) S[L.m + e] = 0.f;
@@ -335,11 +355,11 @@ __global__ void __launch_bounds__(kT) bwd_prep_kernel(const BwdArgs a) {
     float *Vbeta = S + L.dvt;
     for (int e = tid; e < 64 * V; e += kT) Vbeta[e] = S[L.bt + e / V] * S[L.vf + e];
     __syncthreads();
-    block_gemm(64, V, 64, 1.f, Tsh, 65, 1, Vbeta, V, 1, S + L.u, V, 1, false, stage);
+    block_gemm<SPLIT>(64, V, 64, 1.f, Tsh, 65, 1, Vbeta, V, 1, S + L.u, V, 1, false, stage);
     // W: T (64 x 64) times Kbeta (64 x K) into the dS' area (free until the adjoint scan),
     // then copied back over Kbeta
     float *Wtmp = S + L.dsx;
-    block_gemm(64, K, 64, 1.f, Tsh, 65, 1, Kbeta, K, 1, Wtmp, K, 1, false, stage);
+    block_gemm<SPLIT>(64, K, 64, 1.f, Tsh, 65, 1, Kbeta, K, 1, Wtmp, K, 1, false, stage);
     for (int e = tid; e < 64 * K; e += kT) S[L.wm + e] = Wtmp[e];
 }
 
@@ -358,6 +378,7 @@ __device__ __forceinline__ void stage_rows(float *dst, const float *src, int row
 // first, so that the products read no global memory.
 size_t states_smem(int K) { return sizeof(float) * ((size_t)K * 64 * 3 + 64 * 64 + K + kStageFloats); }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
@@ -389,12 +410,12 @@ __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
         cp_async_wait_all();
         __syncthreads();
         // Vt = U - W S (in U's place), stored for the gradient kernel
-        block_gemm(64, 64, K, -1.f, Ws, K, 1, St, 64, 1, Us, 64, 1, true, stage);
+        block_gemm<SPLIT>(64, 64, K, -1.f, Ws, K, 1, St, 64, 1, Us, 64, 1, true, stage);
         for (int e = tid; e < 64 * 64; e += kT) S[L.vt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = Us[e];
         // S <- diag(EG) S + Kb^T Vt
         for (int e = tid; e < K * 64; e += kT) St[e] *= EGs[e >> 6];
         __syncthreads();
-        block_gemm(K, 64, 64, 1.f, Kbs, 1, K, Us, 64, 1, St, 64, 1, true, stage);
+        block_gemm<SPLIT>(K, 64, 64, 1.f, Kbs, 1, K, Us, 64, 1, St, 64, 1, true, stage);
     }
 }
 
@@ -403,6 +424,7 @@ size_t adjoint_smem(int K) {
     return sizeof(float) * ((size_t)K * 64 * 4 + 3 * 64 * 64 + K + kStageFloats);
 }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
@@ -439,14 +461,14 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
         cp_async_wait_all();
         __syncthreads();
         // dVt = A^T dO + Kb dS', stored for the gradient kernel
-        block_gemm(64, 64, 64, 1.f, As, 1, 64, dOs, 64, 1, dVs, 64, 1, false, stage);
-        block_gemm(64, 64, K, 1.f, Kbs, K, 1, dS, 64, 1, dVs, 64, 1, true, stage);
+        block_gemm<SPLIT>(64, 64, 64, 1.f, As, 1, 64, dOs, 64, 1, dVs, 64, 1, false, stage);
+        block_gemm<SPLIT>(64, 64, K, 1.f, Kbs, K, 1, dS, 64, 1, dVs, 64, 1, true, stage);
         for (int e = tid; e < 64 * 64; e += kT) S[L.dvt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dVs[e];
         // dS <- diag(EG) dS' + Qp^T dO - W^T dVt
         for (int e = tid; e < K * 64; e += kT) dS[e] *= EGs[e >> 6];
         __syncthreads();
-        block_gemm(K, 64, 64, 1.f, Qps, 1, K, dOs, 64, 1, dS, 64, 1, true, stage);
-        block_gemm(K, 64, 64, -1.f, Ws, 1, K, dVs, 64, 1, dS, 64, 1, true, stage);
+        block_gemm<SPLIT>(K, 64, 64, 1.f, Qps, 1, K, dOs, 64, 1, dS, 64, 1, true, stage);
+        block_gemm<SPLIT>(K, 64, 64, -1.f, Ws, 1, K, dVs, 64, 1, dS, 64, 1, true, stage);
     }
     if (a.dh0 != nullptr)
         for (int e = tid; e < K * 64; e += kT)
@@ -458,6 +480,7 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
 // [64][64], small vectors and the GEMM stage.
 template <typename T, bool GATE_HEAD>
 __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
+    constexpr bool SPLIT = std::is_same<T, float>::value;
     extern __shared__ __align__(16) float sm[];
     int n, c, len;
     int64_t bos;
@@ -478,17 +501,17 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
     const int row0 = c * 64, nv = min(64, len - row0);
 
     // dQp = dO S^T;  dA = lower(dO Vt^T);  dQp += dA Km
-    block_gemm(64, K, V, 1.f, dOf, V, 1, Se, 1, V, dQp, K, 1, false, stage);
-    block_gemm(64, 64, V, 1.f, dOf, V, 1, Vt, 1, V, dA, 64, 1, false, stage);
+    block_gemm<SPLIT>(64, K, V, 1.f, dOf, V, 1, Se, 1, V, dQp, K, 1, false, stage);
+    block_gemm<SPLIT>(64, 64, V, 1.f, dOf, V, 1, Vt, 1, V, dA, 64, 1, false, stage);
     for (int e = tid; e < 4096; e += kT)
         if ((e & 63) > (e >> 6)) dA[e] = 0.f;
     __syncthreads();
-    block_gemm(64, K, 64, 1.f, dA, 64, 1, Km, K, 1, dQp, K, 1, true, stage);
+    block_gemm<SPLIT>(64, K, 64, 1.f, dA, 64, 1, Km, K, 1, dQp, K, 1, true, stage);
     // dKm = dA^T Qp (dA is not needed after this)
-    block_gemm(64, K, 64, 1.f, dA, 1, 64, Qp, K, 1, dKm, K, 1, false, stage);
+    block_gemm<SPLIT>(64, K, 64, 1.f, dA, 1, 64, Qp, K, 1, dKm, K, 1, false, stage);
     // dKb = Vt dS'^T;  dW = -dVt S^T;  dEG = rows of dS' . S
-    block_gemm(64, K, V, 1.f, Vt, V, 1, dSx, 1, V, dKb, K, 1, false, stage);
-    block_gemm(64, K, V, -1.f, dVt, V, 1, Se, 1, V, dW, K, 1, false, stage);
+    block_gemm<SPLIT>(64, K, V, 1.f, Vt, V, 1, dSx, 1, V, dKb, K, 1, false, stage);
+    block_gemm<SPLIT>(64, K, V, -1.f, dVt, V, 1, Se, 1, V, dW, K, 1, false, stage);
     const int warp = tid >> 5, lane = tid & 31;
     for (int i = warp; i < K; i += kT / 32) {  // a warp per row, lanes along it
         float s = 0.f;
@@ -500,15 +523,15 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
     __syncthreads();
     if (!a.decay_only) {
         // dT = (dW Kp^T + dVt V^T) diag(beta)
-        block_gemm(64, 64, K, 1.f, dW, K, 1, Kp, 1, K, dT, 64, 1, false, stage);
-        block_gemm(64, 64, V, 1.f, dVt, V, 1, Vf, 1, V, dT, 64, 1, true, stage);
+        block_gemm<SPLIT>(64, 64, K, 1.f, dW, K, 1, Kp, 1, K, dT, 64, 1, false, stage);
+        block_gemm<SPLIT>(64, 64, V, 1.f, dVt, V, 1, Vf, 1, V, dT, 64, 1, true, stage);
         for (int e = tid; e < 4096; e += kT) dT[e] *= Bt[e & 63];
         __syncthreads();
         // T^T dW -> dKp (then scaled by beta), dbeta += rows of (T^T dW) . Kp
-        block_gemm(64, K, 64, 1.f, Tm, 1, 64, dW, K, 1, dKp, K, 1, false, stage);
+        block_gemm<SPLIT>(64, K, 64, 1.f, Tm, 1, 64, dW, K, 1, dKp, K, 1, false, stage);
         // T^T dVt -> dW's area (dW is consumed)
         float *TtdU = dW;
-        block_gemm(64, V, 64, 1.f, Tm, 1, 64, dVt, V, 1, TtdU, V, 1, false, stage);
+        block_gemm<SPLIT>(64, V, 64, 1.f, Tm, 1, 64, dVt, V, 1, TtdU, V, 1, false, stage);
         for (int t = warp; t < 64; t += kT / 32) {
             float s = 0.f;
             for (int i = lane; i < K; i += 32) s = fmaf(dKp[t * K + i], Kp[t * K + i], s);
@@ -525,8 +548,8 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
             if (t < nv) stf<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j, Bt[t] * TtdU[e]);
         }
         // dL = -T^T dT T^T (strictly lower): X = dT T^T, dL = -T^T X into dT's area
-        block_gemm(64, 64, 64, 1.f, dT, 64, 1, Tm, 1, 64, X, 64, 1, false, stage);
-        block_gemm(64, 64, 64, -1.f, Tm, 1, 64, X, 64, 1, dT, 64, 1, false, stage);
+        block_gemm<SPLIT>(64, 64, 64, 1.f, dT, 64, 1, Tm, 1, 64, X, 64, 1, false, stage);
+        block_gemm<SPLIT>(64, 64, 64, -1.f, Tm, 1, 64, X, 64, 1, dT, 64, 1, false, stage);
         float *dL = dT;
         for (int e = tid; e < 4096; e += kT)
             if ((e & 63) >= (e >> 6)) dL[e] = 0.f;
@@ -542,8 +565,8 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         for (int e = tid; e < 4096; e += kT) dL[e] *= Bt[e >> 6];
         __syncthreads();
         // dKp += dM Km;  dKm += dM^T Kp
-        block_gemm(64, K, 64, 1.f, dL, 64, 1, Km, K, 1, dKp, K, 1, true, stage);
-        block_gemm(64, K, 64, 1.f, dL, 1, 64, Kp, K, 1, dKm, K, 1, true, stage);
+        block_gemm<SPLIT>(64, K, 64, 1.f, dL, 64, 1, Km, K, 1, dKp, K, 1, true, stage);
+        block_gemm<SPLIT>(64, K, 64, 1.f, dL, 1, 64, Kp, K, 1, dKm, K, 1, true, stage);
     } else {
         // decay-only: U = V, W = 0: dv = dVt
         T *dv = static_cast<T *>(a.dv);
@@ -621,6 +644,7 @@ size_t grads_smem(int K, int V) {
 
 template <typename T, bool GATE_HEAD>
 cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
+    constexpr bool kSplit = std::is_same<T, float>::value;  // fp32-grade products for fp32 inputs
     BwdArgs a = a0;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -663,19 +687,19 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
         e = cudaFuncSetAttribute(bwd_prep_kernel<T, GATE_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)psmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bwd_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+        e = cudaFuncSetAttribute(bwd_states_kernel<kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bwd_adjoint_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)asmem);
+        e = cudaFuncSetAttribute(bwd_adjoint_kernel<kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)asmem);
     if (e == cudaSuccess && windows > 0 && Ttot > 0) {
         const dim3 gw(a.H_v, (unsigned)windows);
         bwd_prep_kernel<T, GATE_HEAD><<<gw, kT, psmem, stream>>>(a);
         e = cudaGetLastError();
         if (e == cudaSuccess) {
-            bwd_states_kernel<<<dim3(V / 64, a.H_v, a.N), kT, ssmem, stream>>>(a);
+            bwd_states_kernel<kSplit><<<dim3(V / 64, a.H_v, a.N), kT, ssmem, stream>>>(a);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) {
-            bwd_adjoint_kernel<<<dim3(V / 64, a.H_v, a.N), kT, asmem, stream>>>(a);
+            bwd_adjoint_kernel<kSplit><<<dim3(V / 64, a.H_v, a.N), kT, asmem, stream>>>(a);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) {
