@@ -285,6 +285,8 @@ int kda_chunk_bwd(const kda_bwd_params *p, cudaStream_t stream) {
     b.scale = a.scale;
     b.gate_per_head = a.gate_per_head;
     b.decay_only = a.decay_only;
+    const cudaError_t e = device_error_ptr(&b.err);
+    if (e != cudaSuccess) return status_of(e);
     return status_of(kda::launch_bwd(b, p->dtype == KDA_DTYPE_F32, stream));
 }
 

@@ -215,15 +215,24 @@ __device__ __forceinline__ float warp_sum(float s) {
     return s;
 }
 
-// Sequence bounds (fixed-length batches or packed sequences).
-__device__ __forceinline__ void bounds(const BwdArgs &a, int n, int64_t &bos, int &len) {
+// Sequence bounds (fixed-length batches or packed sequences); false, with the device error
+// bit raised, when the offsets are malformed (the sequence is then skipped).
+__device__ __forceinline__ bool bounds(const BwdArgs &a, int n, int64_t &bos, int &len) {
     if (a.cu_seqlens == nullptr) {
         bos = (int64_t)n * a.T;
         len = a.T;
-    } else {
-        bos = a.cu_seqlens[n];
-        len = a.cu_seqlens[n + 1] - a.cu_seqlens[n];
+        return true;
     }
+    const int s = a.cu_seqlens[n], e = a.cu_seqlens[n + 1];
+    if (s < 0 || e < s || e > a.T) {
+        if (threadIdx.x == 0) atomicOr(a.err, kDeviceErrSeqlens);
+        bos = 0;
+        len = 0;
+        return false;
+    }
+    bos = s;
+    len = e - s;
+    return true;
 }
 // Slot of chunk c of sequence n (value head h): (bos / 64 + c + n) * H_v + h. Chunks of
 // different sequences never share a slot (there are at most T / 64 + N windows).
@@ -242,7 +251,7 @@ __device__ bool window_owner(const BwdArgs &a, int64_t s, int &n, int &c, int64_
         if ((b >> 6) + mid <= s) lo = mid; else hi = mid - 1;
     }
     n = lo;
-    bounds(a, n, bos, len);
+    if (!bounds(a, n, bos, len)) return false;
     const int64_t cc = s - (bos >> 6) - n;
     if (cc < 0 || cc * 64 >= len) return false;
     c = (int)cc;
@@ -392,7 +401,7 @@ __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     const Lay L = make_lay(K, V);
     int64_t bos;
     int len;
-    bounds(a, n, bos, len);
+    if (!bounds(a, n, bos, len)) return;
     const int nch = (len + 63) / 64;
     for (int e = tid; e < K * 64; e += kT) {
         const int i = e >> 6, j = e & 63;
@@ -441,7 +450,7 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     const Lay L = make_lay(K, V);
     int64_t bos;
     int len;
-    bounds(a, n, bos, len);
+    if (!bounds(a, n, bos, len)) return;
     const int nch = (len + 63) / 64;
     for (int e = tid; e < K * 64; e += kT) {
         const int i = e >> 6, j = e & 63;

@@ -248,6 +248,8 @@ int kda_recurrent_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cud
  *   dbeta  [B, T, H_v] fp32; must be NULL when beta is NULL (decay-only)
  *   dh0    [N, H_v, d_k, d_v] fp32, or NULL when not wanted (also when h0 is NULL: it is
  *          then the gradient with respect to the zero initial state)
+ * Malformed cu_seqlens (decreasing, negative, or past T) are caught on the device: the
+ * sequence is skipped, its outputs are left undefined and KDA_DEVICE_ERR_SEQLENS is raised.
  * Outputs are fully overwritten. Scratch: about 540 KB per (64-token chunk, value head)
  * at d = 128 (the chunk factors, entry states and their adjoints), plus fp32 accumulators
  * of dq and dk for bf16 outputs, all stream-ordered from the library's pool and freed on

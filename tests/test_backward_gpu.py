@@ -135,3 +135,22 @@ def test_benchmark_shape_sampled_units():
         print((n, h), " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
         for name, e in errs.items():
             assert e <= TOL_BF16_OUT, ((n, h), name, e)
+
+
+@pytest.mark.parametrize("bad", [[0, 90, 60], [0, 90, 150]])
+def test_malformed_cu_seqlens_raise_the_device_error(bad):
+    """Decreasing offsets, or offsets past the packed length, are caught on the device: the
+    sequence is skipped and the error bit raised (no access outside the tensors)."""
+    import torch
+
+    from chunkwise_gated_linear_gb300 import chunk_kda_bwd, kda_get_device_error
+
+    x = make_inputs((64, 36), 1, 1, 128, 128, seed=307, varlen=True)
+    d = to_device(x)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert kda_get_device_error(stream) == 0
+    cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+    do = torch.zeros_like(d["v"])
+    chunk_kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], do, scale=x.scale, cu_seqlens=cu)
+    assert kda_get_device_error(stream) == 1
+    assert kda_get_device_error(stream) == 0
