@@ -154,3 +154,16 @@ def test_malformed_cu_seqlens_raise_the_device_error(bad):
     chunk_kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], do, scale=x.scale, cu_seqlens=cu)
     assert kda_get_device_error(stream) == 1
     assert kda_get_device_error(stream) == 0
+
+
+@pytest.mark.parametrize("case", ["gqa4_head_decay", "bf16_d64", "f32_head_varlen"])
+def test_more_shapes(case):
+    if case == "gqa4_head_decay":
+        # four value heads per key head, scalar gate, no beta
+        x = make_inputs((100, 29), 1, 4, 128, 128, seed=308, h0=True, gate="head", beta=False)
+    elif case == "bf16_d64":
+        x = make_inputs((170,), 2, 2, 64, 64, seed=309, h0=True)
+    else:
+        x = make_inputs((5, 64, 0, 140), 2, 2, 128, 64, seed=310, dtype="f32", h0=True, gate="head",
+                        varlen=True)
+    _check(x, case)
