@@ -398,7 +398,8 @@ def run_ours(args, world, rank, local, pg):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     kernel = "kda_recurrent_kernel" if args.entry == "recurrent" else forward_kernel(x, sms)
     launches = 1
-    if fe_on and (args.frontend == "unfused" or (kernel != "kda_fwd_pc_kernel" and args.entry == "chunk")):
+    fused_here = kernel in ("kda_fwd_pc_kernel", "kda_fwd_tc_kernel", "kda_recurrent_kernel")
+    if fe_on and (args.frontend == "unfused" or not fused_here):
         # the separate front-end pass: q and k norms, the gate, the beta sigmoid
         launches += 3 + (1 if x.beta is not None else 0)
         kernel = "front-end pass + " + kernel

@@ -1,5 +1,5 @@
-"""Coefficients of the polynomial P(t) ~ log(1 + t) / t on [0, 1] used by the persistent
-kernel's front-end (``kLog1pPoly`` in kda_fwd_pc.cu): a degree-7 least-squares fit on
+"""Coefficients of the polynomial P(t) ~ log(1 + t) / t on [0, 1] used by the d = 128
+kernels' front-end (``log1p_01`` in tc_util.cuh): a degree-7 least-squares fit on
 Chebyshev nodes of [0, 1], in float64, printed highest power first as float32 literals.
 Run ``python fit_log1p.py`` to regenerate; it also prints the fit's worst relative error
 over a dense grid of [0, 1] (about 2e-7)."""

@@ -108,8 +108,8 @@ int prepare_frontend(const kda_frontend *fe, kda::FwdArgs &a) {
     return KDA_OK;
 }
 
-// The forward kernels without a front-end (none of them reads the fe_* fields but the
-// persistent kernel, which applies them).
+// The forward kernels (the d = 128 bf16 ones apply the fe_* fields themselves; the others
+// are only called with them cleared).
 cudaError_t dispatch(const kda_fwd_params &p, const kda::FwdArgs &a, cudaStream_t stream) {
     if (p.dtype == KDA_DTYPE_F32) return kda::launch_fwd_f32(a, stream);
     if (p.d_k == 128 && p.d_v == 128) {
@@ -139,13 +139,10 @@ int run(const kda_fwd_params &p, const kda_frontend *fe, cudaStream_t stream) {
     cudaError_t e = device_error_ptr(&a.err);
     if (e != cudaSuccess) return status_of(e);
     if (!kda::fe_any(a)) return status_of(dispatch(p, a, stream));
-    // the persistent kernel applies the front-end itself when it takes the call
-    if (!(p.flags & (KDA_FLAG_UNFUSED_FRONTEND | KDA_FLAG_ONE_CTA_PER_UNIT)) && p.dtype == KDA_DTYPE_BF16 &&
-        p.d_k == 128 && p.d_v == 128) {
-        bool launched = false;
-        e = kda::launch_fwd_pc(a, stream, &launched);
-        if (e != cudaSuccess || launched) return status_of(e);
-    }
+    // the d = 128 bf16 kernels (persistent and one CTA per unit) apply the front-end
+    // themselves
+    if (!(p.flags & KDA_FLAG_UNFUSED_FRONTEND) && p.dtype == KDA_DTYPE_BF16 && p.d_k == 128 && p.d_v == 128)
+        return status_of(dispatch(p, a, stream));
     // otherwise a separate pass prepares the inputs in scratch
     kda::FwdArgs b;
     void *scratch = nullptr;

@@ -276,73 +276,8 @@ __device__ __forceinline__ bool next_job(JobIt &it, const Ctx &x, const PcArgs &
     }
 }
 
-// ---- front-end arithmetic: one special-function op per value, the rest on the FMA pipe ----
-// log(1 + t) for t in [0, 1] as t P(t), P a degree-7 least-squares fit of log(1 + t) / t on
-// Chebyshev nodes of [0, 1] (fit_log1p.py beside this file; worst relative error 2.2e-7).
-__device__ __forceinline__ float log1p_01(float t) {
-    float p = -8.574675769e-03f;
-    p = fmaf(p, t, 4.421419278e-02f);
-    p = fmaf(p, t, -1.078536808e-01f);
-    p = fmaf(p, t, 1.775702387e-01f);
-    p = fmaf(p, t, -2.449961156e-01f);
-    p = fmaf(p, t, 3.327617645e-01f);
-    p = fmaf(p, t, -4.999744892e-01f);
-    p = fmaf(p, t, 9.999998212e-01f);
-    return p * t;
-}
-// softplus(x) = max(x, 0) + log(1 + e^-|x|), the exponential on the special-function unit
-__device__ __forceinline__ float softplus_fast(float x) { return fmaxf(x, 0.f) + log1p_01(ex2(-fabsf(x) * kLog2e)); }
-// 1 / (1 + e^-b)
-__device__ __forceinline__ float sigmoid_fast(float b) { return __fdividef(1.f, 1.f + ex2(-b * kLog2e)); }
-
 __device__ __forceinline__ unsigned char *slot_ptr(const PcArgs &pc, int u, int c) {
     return pc.ring + ((int64_t)u * pc.R + c % pc.R) * Slot::kStride;
-}
-
-// Front-end norms of the chunk's raw Q and K rows (64 each, row-major bf16, 256 B per row):
-// RN[t] = scale / sqrt(|q_t|^2 + 1e-6), RN[64 + t] = 1 / sqrt(|k_t|^2 + 1e-6). Warp w of the
-// 8 front warps sums rows 16 w .. 16 w + 15 of [Q; K]: in step i lane l reads the 16-byte
-// chunk l & 15 of row 2 i + (l >> 4) (a quarter-warp reads 128 contiguous bytes), then the
-// eight partial sums of each half-warp are reduced across its 16 lanes by halving, so that
-// lane l ends with the sum of row 2 (l >> 1 & 7) + (l >> 4).
-__device__ __forceinline__ void qk_row_norms(unsigned char *sm, int pw, int lane, float scale) {
-    const unsigned char *base = sm + (pw < 4 ? Prod::oRQ + pw * 4096 : Prod::oRK + (pw - 4) * 4096);
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(base + (2 * i + (lane >> 4)) * 256 + (lane & 15) * 16);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float lo = __uint_as_float(ws[j] << 16), hi = __uint_as_float(ws[j] & 0xffff0000u);
-            acc = fmaf(lo, lo, acc);
-            acc = fmaf(hi, hi, acc);
-        }
-        v[i] = acc;
-    }
-    // halving: after the step across lane bit 3, v[k] is row index 4 b3 + k; bit 2: 4 b3 + 2 b2 + k;
-    // bit 1: 4 b3 + 2 b2 + b1; bit 0: both lanes of a pair hold the full sum
-    const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float send = b3 ? v[k] : v[k + 4], keep = b3 ? v[k + 4] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const float send = b2 ? v[k] : v[k + 2], keep = b2 ? v[k + 2] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    {
-        const float send = b1 ? v[0] : v[1], keep = b1 ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-    if ((lane & 1) == 0) {
-        const int row = 16 * pw + 2 * ((lane >> 1) & 7) + (lane >> 4);  // 0..127 over [Q; K]
-        reinterpret_cast<float *>(sm + Prod::oRN)[row] = (pw < 4 ? scale : 1.f) * rsqrtf(v[0] + kL2NormEps);
-    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -555,7 +490,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         }
         if constexpr (FE) {
             if (a.fe_qk_l2norm) {
-                qk_row_norms(sm, pw, lane, a.scale);
+                qk_row_norms(sm + Prod::oRQ, sm + Prod::oRK, reinterpret_cast<float *>(sm + Prod::oRN), pw, lane, a.scale);
                 bar_named(1, 256);
             }
         }

@@ -48,6 +48,8 @@ struct WsLayout {
     static constexpr int oG = 49152;     // raw G fp32 [64][128]; then L and T fp32 [64][68]
     static constexpr int oL = oG;
     static constexpr int oT = oG + 17408;
+    static constexpr int oRN = oG;       // front-end norm factors [128] fp32 (between the gate
+                                         // sums and the Gram read-back)
     static constexpr int oWT = 83968;    // W^T [d][tok]        } WT, QP0, QP1, KP in this order:
     static constexpr int oQP0 = 100352;  // Qp^T [d][tok], slot 0} serial B operand (WT | QP[b]),
     static constexpr int oQP1 = 116736;  // Qp^T, slot 1          } Gram A operand (QP[b] | KP)
@@ -129,9 +131,12 @@ struct Unit {
 // ---------------------------------------------------------------------------------------
 // prep warps (4-11): TMA staging, gate pass, Gram, solve, WY factors for every chunk.
 // Returns the loads that may still be in flight (abort path): for Q/K, G and V, two bits
-// each holding 1 + the parity of the pending chunk, or 0.
+// each holding 1 + the parity of the pending chunk, or 0. With FE the front-end is applied
+// on the way: beta and the per-head gates as they land, the per-channel gates before the
+// cumulative sum, and the q / k norms as factors of the image rows (kept in the first 512
+// bytes of the G region, free between the gate sums and the Gram read-back).
 // ---------------------------------------------------------------------------------------
-template <bool GATE_HEAD>
+template <bool GATE_HEAD, bool FE>
 __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, const Unit &u) {
     using Lay = WsLayout;
     unsigned char *sm = u.sm;
@@ -173,6 +178,22 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         }
         pend_v = c & 1;
     };
+    // front-end constants of this unit: -exp(A_log[h]) and this thread's channel biases
+    float negA = 0.f, bias0 = 0.f, bias1 = 0.f;
+    if constexpr (FE) {
+        if (a.fe_A_log != nullptr) {
+            negA = -expf(a.fe_A_log[h]);
+            if (a.fe_dt_bias != nullptr) {
+                if constexpr (GATE_HEAD) {
+                    bias0 = a.fe_dt_bias[h];
+                } else {
+                    const int cb = 64 * (pw & 1) + lane;
+                    bias0 = a.fe_dt_bias[h * 128 + cb];
+                    bias1 = a.fe_dt_bias[h * 128 + cb + 32];
+                }
+            }
+        }
+    }
     auto stage_g = [&](int c) {
         const int row0 = c * kChunk;
         const int nvalid = min(kChunk, len - row0);
@@ -221,6 +242,14 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
 
         // G, beta of chunk p, and hand-off slot b released by the serial step of chunk p - 2
         cp_async_wait_all();
+        if constexpr (FE) {
+            // each thread transforms the values it loaded itself (rows past the end stay 0)
+            if (ptid < 64) {
+                if (a.fe_beta_sigmoid && !a.decay_only && ptid < nvalid) Bs[ptid] = sigmoid_fast(Bs[ptid]);
+            } else if (GATE_HEAD && ptid < 128 && a.fe_A_log != nullptr && ptid - 64 < nvalid) {
+                Gh[ptid - 64] = negA * softplus_fast(Gh[ptid - 64] + bias0);
+            }
+        }
         if constexpr (!GATE_HEAD) failed = !wait_bar(&bars[BAR_LG], (uint32_t)(p & 1), u.abort_flag);
         if (!failed && p >= 2)
             failed = !wait_bar(&bars[b ? BAR_FREE1 : BAR_FREE0], (uint32_t)(((p >> 1) - 1) & 1), u.abort_flag);
@@ -240,23 +269,48 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
             const int qr = pw >> 1;
             const int c0 = 64 * (pw & 1) + lane, c1 = c0 + 32;
             float gl0[16], gl1[16];
-            float acc0 = 0.f, acc1 = 0.f;
+            bool gate_done = false;
+            if constexpr (!GATE_HEAD && FE) {
+                if (a.fe_A_log != nullptr) {
+                    // every gate of the thread first (independent), then the running sums
+                    const float nAl = negA * kLog2e;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int r = 16 * qr + e;
-                if constexpr (!GATE_HEAD) {
-                    acc0 += G[r * 128 + c0] * kLog2e;
-                    acc1 += G[r * 128 + c1] * kLog2e;
-                } else {
-                    const float gr = Gh[r] * kLog2e;
-                    acc0 += gr;
-                    acc1 += gr;
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = 16 * qr + e;
+                        const float v0 = nAl * softplus_fast(G[r * 128 + c0] + bias0);
+                        const float v1 = nAl * softplus_fast(G[r * 128 + c1] + bias1);
+                        gl0[e] = r < nvalid ? v0 : 0.f;
+                        gl1[e] = r < nvalid ? v1 : 0.f;
+                    }
+#pragma unroll
+                    for (int e = 1; e < 16; ++e) {
+                        gl0[e] += gl0[e - 1];
+                        gl1[e] += gl1[e - 1];
+                    }
+                    Tot[qr * 128 + c0] = gl0[15];
+                    Tot[qr * 128 + c1] = gl1[15];
+                    gate_done = true;
                 }
-                gl0[e] = acc0;
-                gl1[e] = acc1;
             }
-            Tot[qr * 128 + c0] = acc0;
-            Tot[qr * 128 + c1] = acc1;
+            if (!gate_done) {
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = 16 * qr + e;
+                    if constexpr (!GATE_HEAD) {
+                        acc0 += G[r * 128 + c0] * kLog2e;
+                        acc1 += G[r * 128 + c1] * kLog2e;
+                    } else {
+                        const float gr = Gh[r] * kLog2e;
+                        acc0 += gr;
+                        acc1 += gr;
+                    }
+                    gl0[e] = acc0;
+                    gl1[e] = acc1;
+                }
+                Tot[qr * 128 + c0] = acc0;
+                Tot[qr * 128 + c1] = acc1;
+            }
             failed = !wait_bar(&bars[BAR_LQK], (uint32_t)(p & 1), u.abort_flag);
             if (bar_or(2, 256, failed)) { failed = true; break; }
             pend_qk = -1;
@@ -267,6 +321,13 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
                     *reinterpret_cast<uint4 *>(sm + Lay::oRK + r * 256 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 bar_prep();
+            }
+            if constexpr (FE) {
+                if (a.fe_qk_l2norm) {
+                    qk_row_norms(sm + Lay::oRQ, sm + Lay::oRK, reinterpret_cast<float *>(sm + Lay::oRN), pw, lane,
+                                 a.scale);
+                    bar_prep();
+                }
             }
             float off0 = 0.f, off1 = 0.f, gn0 = 0.f, gn1 = 0.f;
 #pragma unroll
@@ -287,6 +348,20 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int tc = 2 * qr + j;  // 16-byte chunk (8 tokens) of a 64-token row
+                // front-end: the factors of these 8 rows (q: scale / |q|, k: 1 / |k|)
+                float fq[8], fk[8];
+                if constexpr (FE) {
+                    const bool nrm = a.fe_qk_l2norm != 0;
+                    const float4 *RN4 = reinterpret_cast<const float4 *>(sm + Lay::oRN) + 4 * qr + 2 * j;
+                    const float4 q0 = nrm ? RN4[0] : make_float4(a.scale, a.scale, a.scale, a.scale);
+                    const float4 q1 = nrm ? RN4[1] : q0;
+                    const float4 k0 = nrm ? RN4[16] : make_float4(1.f, 1.f, 1.f, 1.f);
+                    const float4 k1 = nrm ? RN4[17] : k0;
+                    fq[0] = q0.x; fq[1] = q0.y; fq[2] = q0.z; fq[3] = q0.w;
+                    fq[4] = q1.x; fq[5] = q1.y; fq[6] = q1.z; fq[7] = q1.w;
+                    fk[0] = k0.x; fk[1] = k0.y; fk[2] = k0.z; fk[3] = k0.w;
+                    fk[4] = k1.x; fk[5] = k1.y; fk[6] = k1.z; fk[7] = k1.w;
+                }
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     const int cc = ch ? c1 : c0;
@@ -297,11 +372,16 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
                         const int r = 16 * qr + 8 * j + e;
                         const float gm = off + (ch ? gl1[8 * j + e] : gl0[8 * j + e]);
                         const float ep = ex2(gm), em = ex2(-gm);
-                        const float kv = __bfloat162float(RK[r * 128 + cc]);
+                        float kv = __bfloat162float(RK[r * 128 + cc]);
                         const float qv = __bfloat162float(RQ[r * 128 + cc]);
+                        float qs = a.scale;
+                        if constexpr (FE) {
+                            qs = fq[e];
+                            kv *= fk[e];
+                        }
                         kp[e] = a.decay_only ? 0.f : kv * ep;
                         km[e] = kv * em;
-                        qp[e] = a.scale * qv * ep;
+                        qp[e] = qs * qv * ep;
                         kb[e] = km[e] * eg;
                     }
                     const uint32_t sw = sw128(cc, tc);
@@ -658,7 +738,7 @@ __device__ __forceinline__ void serial_role(const FwdArgs &a, const Unit &u) {
     }
 }
 
-template <bool GATE_HEAD>
+template <bool GATE_HEAD, bool FE>
 __global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, const __grid_constant__ TcMaps maps) {
     using Lay = WsLayout;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -714,7 +794,7 @@ __global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, con
     if (tid < 128)
         serial_role(a, u);
     else
-        tma_pending = prep_role<GATE_HEAD>(a, maps, u);
+        tma_pending = prep_role<GATE_HEAD, FE>(a, maps, u);
 
     fence_before_sync();
     __syncthreads();
@@ -745,10 +825,10 @@ __global__ void __launch_bounds__(384, 1) kda_fwd_tc_kernel(const FwdArgs a, con
 }
 
 
-template <bool GATE_HEAD>
+template <bool GATE_HEAD, bool FE>
 cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
     constexpr int kSmem = WsLayout::kBytes;
-    auto kern = kda_fwd_tc_kernel<GATE_HEAD>;
+    auto kern = kda_fwd_tc_kernel<GATE_HEAD, FE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     TcMaps maps;
@@ -762,7 +842,9 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t stream) {
-    return a.gate_per_head ? launch_tc<true>(a, stream) : launch_tc<false>(a, stream);
+    if (fe_any(a))
+        return a.gate_per_head ? launch_tc<true, true>(a, stream) : launch_tc<false, true>(a, stream);
+    return a.gate_per_head ? launch_tc<true, false>(a, stream) : launch_tc<false, false>(a, stream);
 }
 
 }  // namespace kda

@@ -62,6 +62,72 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
     return u;
 }
 
+// ---- front-end arithmetic: one special-function op per value, the rest on the FMA pipe ----
+// log(1 + t) for t in [0, 1] as t P(t), P a degree-7 least-squares fit of log(1 + t) / t on
+// Chebyshev nodes of [0, 1] (fit_log1p.py beside this file; worst relative error 2.2e-7).
+__device__ __forceinline__ float log1p_01(float t) {
+    float p = -8.574675769e-03f;
+    p = fmaf(p, t, 4.421419278e-02f);
+    p = fmaf(p, t, -1.078536808e-01f);
+    p = fmaf(p, t, 1.775702387e-01f);
+    p = fmaf(p, t, -2.449961156e-01f);
+    p = fmaf(p, t, 3.327617645e-01f);
+    p = fmaf(p, t, -4.999744892e-01f);
+    p = fmaf(p, t, 9.999998212e-01f);
+    return p * t;
+}
+// softplus(x) = max(x, 0) + log(1 + e^-|x|), the exponential on the special-function unit
+__device__ __forceinline__ float softplus_fast(float x) { return fmaxf(x, 0.f) + log1p_01(ex2(-fabsf(x) * kLog2e)); }
+// 1 / (1 + e^-b)
+__device__ __forceinline__ float sigmoid_fast(float b) { return __fdividef(1.f, 1.f + ex2(-b * kLog2e)); }
+
+// Front-end norms of a chunk's raw Q and K tiles (64 rows each, row-major bf16, 256 B per
+// row): rn[t] = scale / sqrt(|q_t|^2 + 1e-6), rn[64 + t] = 1 / sqrt(|k_t|^2 + 1e-6). Warp w of
+// the 8 calling warps (pw = 0..7) sums rows 16 w .. 16 w + 15 of [Q; K]: in step i lane l reads the 16-byte
+// chunk l & 15 of row 2 i + (l >> 4) (a quarter-warp reads 128 contiguous bytes), then the
+// eight partial sums of each half-warp are reduced across its 16 lanes by halving, so that
+// lane l ends with the sum of row 2 (l >> 1 & 7) + (l >> 4).
+__device__ __forceinline__ void qk_row_norms(const unsigned char *rq, const unsigned char *rk, float *rn, int pw,
+                                             int lane, float scale) {
+    const unsigned char *base = pw < 4 ? rq + pw * 4096 : rk + (pw - 4) * 4096;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(base + (2 * i + (lane >> 4)) * 256 + (lane & 15) * 16);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(ws[j] << 16), hi = __uint_as_float(ws[j] & 0xffff0000u);
+            acc = fmaf(lo, lo, acc);
+            acc = fmaf(hi, hi, acc);
+        }
+        v[i] = acc;
+    }
+    // halving: after the step across lane bit 3, v[k] is row index 4 b3 + k; bit 2: 4 b3 + 2 b2 + k;
+    // bit 1: 4 b3 + 2 b2 + b1; bit 0: both lanes of a pair hold the full sum
+    const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float send = b3 ? v[k] : v[k + 4], keep = b3 ? v[k + 4] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float send = b2 ? v[k] : v[k + 2], keep = b2 ? v[k + 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+        const float send = b1 ? v[0] : v[1], keep = b1 ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    if ((lane & 1) == 0) {
+        const int row = 16 * pw + 2 * ((lane >> 1) & 7) + (lane >> 4);  // 0..127 over [Q; K]
+        rn[row] = (pw < 4 ? scale : 1.f) * rsqrtf(v[0] + kL2NormEps);
+    }
+}
+
 // K-major operand descriptor, K step s (16 elements) of a tile whose K atoms are `atom_bytes` apart.
 __device__ __forceinline__ uint64_t dK(uint32_t base, uint32_t atom_bytes, int s) {
     return desc_sw128(base + (uint32_t)(s >> 2) * atom_bytes + (uint32_t)(s & 3) * 32u, 0, 1024);

@@ -216,9 +216,9 @@ typedef struct kda_frontend {
 
 /*
  * kda_chunk_fwd_fused — kda_chunk_fwd_ex with the front-end `fe` applied to its inputs
- * (fe == NULL: exactly kda_chunk_fwd_ex). The persistent kernel (bf16, d_k = d_v = 128, few
- * units) applies it while staging each chunk, so q, k, g and beta are read once; the other
- * kernels get it as a separate pass that writes the prepared q and k (in the input dtype),
+ * (fe == NULL: exactly kda_chunk_fwd_ex). With bf16 and d_k = d_v = 128 the kernels apply it
+ * while staging each chunk, so q, k, g and beta are read once; the d = 64 and fp32 kernels
+ * get it as a separate pass that writes the prepared q and k (in the input dtype),
  * g and beta (fp32) to stream-ordered scratch from the library's pool (freed on the same
  * stream), about 2 * T * H_k * d_k * elem + T * H_v * (d_k or 1) * 4 + T * H_v * 4 bytes.
  * Errors as kda_chunk_fwd_ex, and KDA_ERR_INVALID_ARG for beta_sigmoid with beta == NULL or

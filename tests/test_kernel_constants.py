@@ -1,5 +1,5 @@
-"""Constants written into the kernels, checked on the host: the polynomial the persistent
-kernel's front-end uses for log(1 + t) on [0, 1] is read out of its source and evaluated
+"""Constants written into the kernels, checked on the host: the polynomial the d = 128
+kernels' front-end uses for log(1 + t) on [0, 1] is read out of its source and evaluated
 in float32 against numpy's log1p (worst relative error below 5e-7), and the fit script
 beside it regenerates the same coefficients."""
 
@@ -17,7 +17,7 @@ CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 
 
 def _coefficients():
-    src = open(os.path.join(CSRC, "kda_fwd_pc.cu"), encoding="utf-8").read()
+    src = open(os.path.join(CSRC, "tc_util.cuh"), encoding="utf-8").read()
     body = re.search(r"float log1p_01\(float t\) \{(.*?)\n\}", src, flags=re.S).group(1)
     return [float(v) for v in re.findall(r"([-+]?\d\.\d+e[-+]\d+)f", body)]
 
