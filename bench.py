@@ -274,6 +274,9 @@ def run_reference(args, world, rank, pg):
     print(json.dumps(line), flush=True)
 
 
+E2E_H2D_STREAMS = 1
+
+
 def run_ours(args, world, rank, local, pg):
     import numpy as np
     import torch
@@ -321,40 +324,78 @@ def run_ours(args, world, rank, local, pg):
     cu = torch.from_numpy(x.cu_seqlens.astype(np.int32)).to(dev) if x.varlen else None
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
-    ptr = lambda key: D[key].data_ptr() if key in D else None  # noqa: E731
-    params = kda.kda_fwd_params(
-        ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"), ptr("ht"), B, T, x.H_k,
-        x.H_v, x.d_k, x.d_v, 64, x.scale, None if cu is None else cu.data_ptr(),
-        kda.KDA_DTYPE_BF16 if x.dtype == "bf16" else kda.KDA_DTYPE_F32,
-        kda.KDA_GATE_PER_CHANNEL if x.gate == "channel" else kda.KDA_GATE_PER_HEAD,
-        kda.KDA_FLAG_UNFUSED_FRONTEND if args.frontend == "unfused" else 0)
-    fe = kda.kda_frontend(1, 1 if x.beta is not None else 0, ptr("A_log"), ptr("dt_bias")) if fe_on else None
     north_star = args.entry == "chunk" and x.dtype == "bf16" and x.gate == "channel" and not fe_on
 
-    def call():
-        # kda_chunk_fwd (the spec symbol) when the workload fits its argument list,
-        # else the struct entry points of the same ABI
-        if fe_on:
-            fn = lib.kda_recurrent_fwd_fused if args.entry == "recurrent" else lib.kda_chunk_fwd_fused
-            st = fn(ctypes.byref(params), ctypes.byref(fe), sh)
-        elif north_star:
-            st = lib.kda_chunk_fwd(ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"),
-                                   ptr("ht"), B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale,
-                                   None if cu is None else cu.data_ptr(), sh)
-        elif args.entry == "recurrent":
-            st = lib.kda_recurrent_fwd_ex(ctypes.byref(params), sh)
-        else:
-            st = lib.kda_chunk_fwd_ex(ctypes.byref(params), sh)
-        if st != 0:
-            raise RuntimeError(kda.status_string(st))
+    def make_call(Ds):
+        """One library call on the device buffers Ds, on `stream`."""
+        ptr = lambda key: Ds[key].data_ptr() if key in Ds else None  # noqa: E731
+        params = kda.kda_fwd_params(
+            ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"), ptr("ht"), B, T, x.H_k,
+            x.H_v, x.d_k, x.d_v, 64, x.scale, None if cu is None else cu.data_ptr(),
+            kda.KDA_DTYPE_BF16 if x.dtype == "bf16" else kda.KDA_DTYPE_F32,
+            kda.KDA_GATE_PER_CHANNEL if x.gate == "channel" else kda.KDA_GATE_PER_HEAD,
+            kda.KDA_FLAG_UNFUSED_FRONTEND if args.frontend == "unfused" else 0)
+        fe = kda.kda_frontend(1, 1 if x.beta is not None else 0, ptr("A_log"), ptr("dt_bias")) if fe_on else None
+
+        def call():
+            # kda_chunk_fwd (the north-star symbol) when the workload fits its argument list,
+            # else the struct entry points of the same ABI
+            if fe_on:
+                fn = lib.kda_recurrent_fwd_fused if args.entry == "recurrent" else lib.kda_chunk_fwd_fused
+                st = fn(ctypes.byref(params), ctypes.byref(fe), sh)
+            elif north_star:
+                st = lib.kda_chunk_fwd(ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"),
+                                       ptr("ht"), B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale,
+                                       None if cu is None else cu.data_ptr(), sh)
+            elif args.entry == "recurrent":
+                st = lib.kda_recurrent_fwd_ex(ctypes.byref(params), sh)
+            else:
+                st = lib.kda_chunk_fwd_ex(ctypes.byref(params), sh)
+            if st != 0:
+                raise RuntimeError(kda.status_string(st))
+        return call
+
+    call = make_call(D)
+
+    # End to end: every step copies its inputs from pinned host memory and reads its results
+    # back. Steps are double-buffered over two sets of device buffers, with one copy stream
+    # per direction, so that step i + 1's inputs travel while step i computes and step i - 1's
+    # results come back (as a serving loop would run it).
+    D2 = {key: torch.empty_like(D[key]) for key in inputs + ["o", "ht"]}
+    sets = [D, D2]
+    calls = [call, make_call(D2)]
+    s_out = torch.cuda.Stream(device=dev)
+    # input copy streams (more than one measured no faster: the host link is saturated)
+    s_ins = [torch.cuda.Stream(device=dev) for _ in range(E2E_H2D_STREAMS)]
+    s_in = s_ins[0]
+    ev_in = [[torch.cuda.Event() for _ in range(E2E_H2D_STREAMS)] for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    step_no = [0]
 
     def e2e_step():
-        with torch.cuda.stream(stream):
-            for key in inputs:
-                D[key].copy_(H[key], non_blocking=True)
-            call()
-            H["o"].copy_(D["o"], non_blocking=True)
-            H["ht"].copy_(D["ht"], non_blocking=True)
+        i = step_no[0]
+        step_no[0] += 1
+        j = i & 1
+        Dj = sets[j]
+        for si, st_in in enumerate(s_ins):
+            with torch.cuda.stream(st_in):
+                if i >= 2:
+                    st_in.wait_event(ev_done[j])  # step i - 2 has read set j's inputs
+                for key in inputs[si::E2E_H2D_STREAMS]:
+                    Dj[key].copy_(H[key], non_blocking=True)
+                ev_in[j][si].record(st_in)
+        for ev in ev_in[j]:
+            stream.wait_event(ev)
+        if i >= 2:
+            stream.wait_event(ev_out[j])  # step i - 2's results in set j have been read back
+        calls[j]()
+        ev_done[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[j])
+            H["o"].copy_(Dj["o"], non_blocking=True)
+            H["ht"].copy_(Dj["ht"], non_blocking=True)
+            ev_out[j].record(s_out)
 
     for _ in range(args.warmup):
         call()
@@ -378,15 +419,19 @@ def run_ours(args, world, rank, local, pg):
     value = tokens * world / (ms_max / 1000.0)
 
     # end to end through the C ABI with host buffers: H2D inputs, call, D2H results
-    for _ in range(max(1, args.warmup // 2)):
+    for _ in range(max(2, args.warmup // 2)):
         e2e_step()
     torch.cuda.synchronize(dev)
     barrier(pg)
     ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev2.record(stream)
+    step_no[0] = 0  # the timed steps start with empty pipelines
+    ev2.record(s_in)
+    for st_in in s_ins[1:]:
+        st_in.wait_stream(s_in)
     for _ in range(args.steps):
         e2e_step()
-    ev3.record(stream)
+    s_out.wait_event(ev_done[(step_no[0] - 1) & 1])
+    ev3.record(s_out)
     torch.cuda.synchronize(dev)
     barrier(pg)
     ms_e2e = max_over_ranks(pg, ev2.elapsed_time(ev3) / args.steps)
@@ -436,7 +481,8 @@ def run_ours(args, world, rank, local, pg):
                        "l2": f"inputs larger than L2 ({abytes / 1e6:.0f} MB per step), no flush"
                        if abytes > 129e6 else f"{abytes / 1e6:.0f} MB per step (not flushed)"},
             "e2e": {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "schedule": "double-buffered: step i+1's H2D and step i-1's D2H overlap step i"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": abytes,
