@@ -125,7 +125,7 @@ template <bool SPLIT>
 __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int64_t am, int64_t ak,
                            const float *B, int64_t bk, int64_t bn, float *C, int64_t cm, int64_t cn, bool acc,
                            float *stage) {
-    static_assert(kT == 512, "16 warps: 4 x 4 blocks of 16 x 16 per 64 x 64 tile");
+    static_assert(kT == 512 && kKS == 32, "16 warps: 4 x 4 blocks of 16 x 16 per 64 x 64 tile");
     float *As = stage, *Bs = stage + kKS * kSP;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -134,29 +134,34 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
         for (int n0 = 0; n0 < N; n0 += 64) {
             float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             float ra[kLoads], rb[kLoads];
+            // Element r of this thread's share of the staged tiles: e = tid + kT r. With the k
+            // index fastest (ak == 1) k = lane and m = e / 32; else m = tid % 64 and k = e / 64.
+            // Its global offset and shared-memory slot are a base plus r times a step, and
+            // move by k0 * ak (k0 * bk) from one k step to the next.
+            const bool akf = ak == 1, bnf = bn == 1;
+            const int ma = akf ? (tid >> 5) : (tid & 63), ka = akf ? lane : (tid >> 6);
+            const int64_t a_base = (int64_t)(m0 + ma) * am + (int64_t)ka * ak;
+            const int64_t a_step = akf ? 16 * am : 8 * ak;  // r -> r + 1 (kT = 512, kKS = 32)
+            const int as_base = ka * kSP + ma, as_step = akf ? 16 : 8 * kSP;
+            const int nb_ = bnf ? (tid & 63) : (tid >> 5), kb_ = bnf ? (tid >> 6) : lane;
+            const int64_t b_base = (int64_t)kb_ * bk + (int64_t)(n0 + nb_) * bn;
+            const int64_t b_step = bnf ? 8 * bk : 16 * bn;
+            const int bs_base = kb_ * kSP + nb_, bs_step = bnf ? 8 * kSP : 16;
             auto fetch = [&](int k0) {
+                const float *Ak = A + (int64_t)k0 * ak + a_base;
+                const float *Bk = B + (int64_t)k0 * bk + b_base;
 #pragma unroll
                 for (int r = 0; r < kLoads; ++r) {
-                    const int e = tid + kT * r;
-                    int m, k;
-                    if (ak == 1) { k = e & (kKS - 1); m = e / kKS; } else { m = e & 63; k = e >> 6; }
-                    ra[r] = A[(int64_t)(m0 + m) * am + (int64_t)(k0 + k) * ak];
-                    int kb, n;
-                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & (kKS - 1); n = e / kKS; }
-                    rb[r] = B[(int64_t)(k0 + kb) * bk + (int64_t)(n0 + n) * bn];
+                    ra[r] = Ak[r * a_step];
+                    rb[r] = Bk[r * b_step];
                 }
             };
             fetch(0);
             for (int k0 = 0; k0 < K; k0 += kKS) {
 #pragma unroll
                 for (int r = 0; r < kLoads; ++r) {
-                    const int e = tid + kT * r;
-                    int m, k;
-                    if (ak == 1) { k = e & (kKS - 1); m = e / kKS; } else { m = e & 63; k = e >> 6; }
-                    As[k * kSP + m] = ra[r];
-                    int kb, n;
-                    if (bn == 1) { n = e & 63; kb = e >> 6; } else { kb = e & (kKS - 1); n = e / kKS; }
-                    Bs[kb * kSP + n] = rb[r];
+                    As[as_base + r * as_step] = ra[r];
+                    Bs[bs_base + r * bs_step] = rb[r];
                 }
                 __syncthreads();
                 if (k0 + kKS < K) fetch(k0 + kKS);
