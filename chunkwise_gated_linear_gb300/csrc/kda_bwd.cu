@@ -592,8 +592,10 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         __syncthreads();
     }
 
-    // dq, dk (atomically: value heads of one key head share rows), dgamma in dQp's area
+    // dq, dk (atomically when several value heads share a key head's rows, else written
+    // once each), dgamma in dQp's area
     float *dqa = a.dq_acc, *dka = a.dk_acc;
+    T *dq = static_cast<T *>(a.dq), *dk = static_cast<T *>(a.dk);
     for (int e = tid; e < 64 * K; e += kT) {
         const int t = e / K, i = e - t * K;
         const float gam = Gm[e], gn = Gm[63 * K + i];
@@ -601,8 +603,14 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         const float vq = dQp[e], vkp = dKp[e], vkm = dKm[e], vkb = dKb[e];
         if (t < nv) {
             const int64_t o = ((bos + row0 + t) * a.H_k + hk) * K + i;
-            atomicAdd(dqa + o, a.scale * ep * vq);
-            atomicAdd(dka + o, ep * vkp + em * vkm + eb * vkb);
+            const float gq = a.scale * ep * vq, gk = ep * vkp + em * vkm + eb * vkb;
+            if (a.direct_qk) {
+                stf<T>(dq + o, gq);
+                stf<T>(dk + o, gk);
+            } else {
+                atomicAdd(dqa + o, gq);
+                atomicAdd(dka + o, gk);
+            }
         }
         dQp[e] = vq * Qp[e] + vkp * Kp[e] - vkm * Km[e] - vkb * Kb[e];  // dgamma
         dKb[e] = vkb * Kb[e];                                             // for dGn
@@ -671,7 +679,9 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
     const size_t slot_bytes = sizeof(float) * (size_t)L.total;
     const size_t scratch_bytes = slot_bytes * (size_t)(windows * a.H_v);
     const size_t acc_elems = (size_t)Ttot * a.H_k * K;
-    const bool own_acc = !std::is_same<T, float>::value;  // bf16 outputs: fp32 accumulators
+    a.direct_qk = a.group == 1 ? 1 : 0;  // each (token, key head) row then has one writer
+    // grouped heads with bf16 outputs: fp32 accumulators, converted at the end
+    const bool own_acc = !a.direct_qk && !std::is_same<T, float>::value;
     const size_t acc_bytes = own_acc ? 2 * sizeof(float) * acc_elems : 0;
     cudaMemPool_t pool = nullptr;
     e = scratch_pool(dev, &pool);
@@ -687,7 +697,7 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
         a.dq_acc = static_cast<float *>(a.dq);
         a.dk_acc = static_cast<float *>(a.dk);
     }
-    if (acc_elems > 0) {
+    if (acc_elems > 0 && !a.direct_qk) {
         e = cudaMemsetAsync(a.dq_acc, 0, sizeof(float) * acc_elems, stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(a.dk_acc, 0, sizeof(float) * acc_elems, stream);
     }

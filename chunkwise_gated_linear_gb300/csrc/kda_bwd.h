@@ -19,6 +19,7 @@ struct BwdArgs {
     int gate_per_head, decay_only;
     float *scratch;            // per-chunk factors (set by the launcher)
     float *dq_acc, *dk_acc;    // fp32 accumulators of dq, dk (set by the launcher)
+    int direct_qk;             // one value head per key head: dq, dk written directly
     unsigned int *err;         // device error word (KDA_DEVICE_ERR_*)
 };
 
