@@ -69,16 +69,6 @@ __host__ __device__ inline Lay make_lay(int K, int V) {
 }
 
 template <typename T>
-__device__ __forceinline__ float ldf(const T *p);
-template <>
-__device__ __forceinline__ float ldf<float>(const float *p) {
-    return *p;
-}
-template <>
-__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) {
-    return __bfloat162float(*p);
-}
-template <typename T>
 __device__ __forceinline__ void stf(T *p, float v);
 template <>
 __device__ __forceinline__ void stf<float>(float *p, float v) {
@@ -88,6 +78,40 @@ template <>
 __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
     *p = __float2bfloat16_rn(v);
 }
+
+// Four consecutive elements of a tensor that nothing writes while the kernel runs, through
+// the read-only path (so that the compiler may issue the loads of later iterations ahead of
+// earlier stores), as floats; zeros when !ok. p is 16-byte (fp32) or 8-byte (bf16) aligned.
+template <typename T>
+__device__ __forceinline__ float4 ld4(const T *p, bool ok);
+template <>
+__device__ __forceinline__ float4 ld4<float>(const float *p, bool ok) {
+    return ok ? __ldg(reinterpret_cast<const float4 *>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+template <>
+__device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16 *p, bool ok) {
+    if (!ok) return make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));  // element 0 in the low half
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+// Four consecutive outputs (16-byte aligned fp32, 8-byte aligned bf16, rounded to nearest).
+template <typename T>
+__device__ __forceinline__ void st4(T *p, float4 v);
+template <>
+__device__ __forceinline__ void st4<float>(float *p, float4 v) {
+    *reinterpret_cast<float4 *>(p) = v;
+}
+template <>
+__device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&lo);
+    u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+__device__ __forceinline__ float4 ld4f(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4f(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 
 // tf32 tensor-core product on split operands: x = hi + lo with hi = tf32(x), lo = tf32(x -
 // hi); a b ~ hi_a hi_b + hi_a lo_b + lo_a hi_b ("3xTF32"), whose error is about that of an
@@ -117,9 +141,12 @@ __device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (
 // accumulators per warp) on tf32 mma.sync: with SPLIT the operands are split (3xTF32,
 // fp32-grade products; fp32 inputs), else rounded to tf32 once (10-bit mantissa products,
 // fp32 accumulation; bf16 inputs, whose gradients are rounded to bf16 or compared at that
-// level). The operand tiles go through shared memory in 32-deep k steps, the next one
-// fetched into registers while the current one is multiplied.
-constexpr int kSP = 72;  // row stride of the staged tiles (conflict-free fragment reads)
+// level; the rounding is done once per element, when it is staged). The operand tiles go
+// through shared memory in 32-deep k steps, the next one fetched into registers while the
+// current one is multiplied.
+constexpr int kSP = 72;  // row stride of a tile staged [k][64] (conflict-free fragment reads)
+constexpr int kSA = 36;  // row stride of a tile staged [64][k]
+static_assert(64 * kSA <= kKS * kSP, "both layouts fit one stage");
 constexpr int kStageFloats = 2 * kKS * kSP;
 template <bool SPLIT>
 __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int64_t am, int64_t ak,
@@ -137,16 +164,23 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
             // Element r of this thread's share of the staged tiles: e = tid + kT r. With the k
             // index fastest (ak == 1) k = lane and m = e / 32; else m = tid % 64 and k = e / 64.
             // Its global offset and shared-memory slot are a base plus r times a step, and
-            // move by k0 * ak (k0 * bk) from one k step to the next.
+            // move by k0 * ak (k0 * bk) from one k step to the next. A tile is staged in the
+            // order of its source, [m][k] (row stride kSA) when k is contiguous, else [k][m]
+            // (row stride kSP), and B likewise: both the staging stores and the fragment reads
+            // are then free of bank conflicts.
             const bool akf = ak == 1, bnf = bn == 1;
+            const int sam = akf ? kSA : 1, sak = akf ? 1 : kSP;    // A(m, k) at As[m sam + k sak]
+            const int sbk = bnf ? kSP : 1, sbn = bnf ? 1 : kSA;    // B(k, n) at Bs[k sbk + n sbn]
             const int ma = akf ? (tid >> 5) : (tid & 63), ka = akf ? lane : (tid >> 6);
             const int64_t a_base = (int64_t)(m0 + ma) * am + (int64_t)ka * ak;
             const int64_t a_step = akf ? 16 * am : 8 * ak;  // r -> r + 1 (kT = 512, kKS = 32)
-            const int as_base = ka * kSP + ma, as_step = akf ? 16 : 8 * kSP;
+            const int as_base = ma * sam + ka * sak, as_step = akf ? 16 * kSA : 8 * kSP;
             const int nb_ = bnf ? (tid & 63) : (tid >> 5), kb_ = bnf ? (tid >> 6) : lane;
             const int64_t b_base = (int64_t)kb_ * bk + (int64_t)(n0 + nb_) * bn;
             const int64_t b_step = bnf ? 8 * bk : 16 * bn;
-            const int bs_base = kb_ * kSP + nb_, bs_step = bnf ? 8 * kSP : 16;
+            const int bs_base = kb_ * sbk + nb_ * sbn, bs_step = bnf ? 8 * kSP : 16 * kSA;
+            // fragment offsets: A(mb + g, t), B(t, nb + g)
+            const int fa = (mb + g) * sam + t * sak, fb = t * sbk + (nb + g) * sbn;
             auto fetch = [&](int k0) {
                 const float *Ak = A + (int64_t)k0 * ak + a_base;
                 const float *Bk = B + (int64_t)k0 * bk + b_base;
@@ -158,18 +192,20 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
             };
             fetch(0);
             for (int k0 = 0; k0 < K; k0 += kKS) {
+                // without SPLIT the operands are rounded to tf32 here, once per element, and
+                // the fragments below are read as they are
 #pragma unroll
                 for (int r = 0; r < kLoads; ++r) {
-                    As[as_base + r * as_step] = ra[r];
-                    Bs[bs_base + r * bs_step] = rb[r];
+                    As[as_base + r * as_step] = SPLIT ? ra[r] : __uint_as_float(to_tf32(ra[r]));
+                    Bs[bs_base + r * bs_step] = SPLIT ? rb[r] : __uint_as_float(to_tf32(rb[r]));
                 }
                 __syncthreads();
                 if (k0 + kKS < K) fetch(k0 + kKS);
 #pragma unroll
                 for (int k8 = 0; k8 < kKS; k8 += 8) {
                     // A (16 x 8): rows mb + g, mb + g + 8; columns k8 + t, k8 + t + 4
-                    const float a0 = As[(k8 + t) * kSP + mb + g], a1 = As[(k8 + t) * kSP + mb + g + 8];
-                    const float a2 = As[(k8 + t + 4) * kSP + mb + g], a3 = As[(k8 + t + 4) * kSP + mb + g + 8];
+                    const float *Af = As + fa + k8 * sak;
+                    const float a0 = Af[0], a1 = Af[8 * sam], a2 = Af[4 * sak], a3 = Af[8 * sam + 4 * sak];
                     uint32_t ah[4], al[4];
                     if constexpr (SPLIT) {
                         split_tf32(a0, ah[0], al[0]);
@@ -177,16 +213,16 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
                         split_tf32(a2, ah[2], al[2]);
                         split_tf32(a3, ah[3], al[3]);
                     } else {
-                        ah[0] = to_tf32(a0);
-                        ah[1] = to_tf32(a1);
-                        ah[2] = to_tf32(a2);
-                        ah[3] = to_tf32(a3);
+                        ah[0] = __float_as_uint(a0);
+                        ah[1] = __float_as_uint(a1);
+                        ah[2] = __float_as_uint(a2);
+                        ah[3] = __float_as_uint(a3);
                     }
 #pragma unroll
                     for (int f = 0; f < 2; ++f) {
                         // B (8 x 8): rows k8 + t, k8 + t + 4; column nb + 8 f + g
-                        const float b0 = Bs[(k8 + t) * kSP + nb + 8 * f + g];
-                        const float b1 = Bs[(k8 + t + 4) * kSP + nb + 8 * f + g];
+                        const float *Bf = Bs + fb + k8 * sbk + 8 * f * sbn;
+                        const float b0 = Bf[0], b1 = Bf[4 * sbk];
                         if constexpr (SPLIT) {
                             uint32_t bh0, bl0, bh1, bl1;
                             split_tf32(b0, bh0, bl0);
@@ -195,7 +231,7 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
                             mma_m16n8k8_tf32(c[f], ah, bl0, bl1);
                             mma_m16n8k8_tf32(c[f], ah, bh0, bh1);
                         } else {
-                            mma_m16n8k8_tf32(c[f], ah, to_tf32(b0), to_tf32(b1));
+                            mma_m16n8k8_tf32(c[f], ah, __float_as_uint(b0), __float_as_uint(b1));
                         }
                     }
                 }
@@ -264,20 +300,16 @@ __device__ bool window_owner(const BwdArgs &a, int64_t s, int &n, int &c, int64_
 }
 
 // ---- prep: the chunk factors -----------------------------------------------------------------
-// Shared memory: GEMM stage, L and T [64][65], the row partial sums of T [kT / 64][64],
-// gamma [64][K].
-constexpr int kGroups = kT / 64;
-size_t prep_smem(int K) {
-    return sizeof(float) * ((size_t)kStageFloats + 2 * 64 * 65 + kGroups * 64 + 64 * (size_t)K);
-}
+// Shared memory: GEMM stage, L and T [64][65], gamma [64][K].
+size_t prep_smem(int K) { return sizeof(float) * ((size_t)kStageFloats + 2 * 64 * 65 + 64 * (size_t)K); }
 
 // two CTAs per SM (64 registers a thread): the kernel is latency-bound
 template <typename T, bool GATE_HEAD>
 __global__ void __launch_bounds__(kT, 2) bwd_prep_kernel(const BwdArgs a) {
     constexpr bool SPLIT = std::is_same<T, float>::value;
     extern __shared__ __align__(16) float psm[];
-    float *stage = psm, *Lsh = stage + kStageFloats, *Tsh = Lsh + 64 * 65, *red = Tsh + 64 * 65;
-    float *Gs = red + kGroups * 64;
+    float *stage = psm, *Lsh = stage + kStageFloats, *Tsh = Lsh + 64 * 65;
+    float *Gs = Tsh + 64 * 65;
     int n, c, len;
     int64_t bos;
     if (!window_owner(a, blockIdx.y, n, c, bos, len)) return;
@@ -294,11 +326,24 @@ __global__ void __launch_bounds__(kT, 2) bwd_prep_kernel(const BwdArgs a) {
     const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * K;
 
     // gamma (natural log), per channel: the gate tile into shared memory (rows past the end
-    // zero, so that they keep the last valid value), then a running sum per channel
-    for (int e = tid; e < 64 * K; e += kT) {
-        const int t = e / K, i = e - t * K;
+    // zero, so that they keep the last valid value), then a running sum per channel. The
+    // element loops below take four consecutive channels (or value columns) of one token per
+    // step: e4 indexes float4 groups, 4 e4 = t K + i.
+    const int pk = K / 4, pv = V / 4;
+#pragma unroll 4
+    for (int e4 = tid; e4 < 16 * K; e4 += kT) {
+        const int t = e4 / pk, i = 4 * (e4 - t * pk);
         const int64_t r = bos + row0 + t;
-        Gs[e] = t < nv ? (GATE_HEAD ? a.g[r * sg + h] : a.g[r * sg + (int64_t)h * K + i]) : 0.f;
+        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < nv) {
+            if (GATE_HEAD) {
+                const float x = __ldg(a.g + r * sg + h);
+                gv = make_float4(x, x, x, x);
+            } else {
+                gv = __ldg(reinterpret_cast<const float4 *>(a.g + r * sg + (int64_t)h * K + i));
+            }
+        }
+        st4f(Gs + 4 * e4, gv);
     }
     __syncthreads();
     for (int i = tid; i < K; i += kT) {
@@ -310,26 +355,51 @@ __global__ void __launch_bounds__(kT, 2) bwd_prep_kernel(const BwdArgs a) {
         S[L.eg + i] = expf(acc);
     }
     __syncthreads();
-    for (int e = tid; e < 64 * K; e += kT) S[L.gm + e] = Gs[e];
+    for (int e4 = tid; e4 < 16 * K; e4 += kT) st4f(S + L.gm + 4 * e4, ld4f(Gs + 4 * e4));
     for (int t = tid; t < 64; t += kT)
         S[L.bt + t] = t < nv ? (a.decay_only ? 1.f : a.beta[(bos + row0 + t) * a.H_v + h]) : 0.f;
-    __syncthreads();
-    for (int e = tid; e < 64 * K; e += kT) {
-        const int t = e / K, i = e - t * K;
+    // Qp, Kp, Km, Kb, and diag(beta) Kp for the W product (in the dS' area, free until the
+    // adjoint scan)
+    float *Kbeta = S + L.dsx;
+#pragma unroll 2
+    for (int e4 = tid; e4 < 16 * K; e4 += kT) {
+        const int t = e4 / pk, i = 4 * (e4 - t * pk);
         const int64_t r = bos + row0 + t;
-        const float kv = t < nv ? ldf<T>(k + r * sqk + (int64_t)hk * K + i) : 0.f;
-        const float qv = t < nv ? ldf<T>(q + r * sqk + (int64_t)hk * K + i) : 0.f;
-        const float gam = Gs[e], gn = Gs[63 * K + i];
-        S[L.qp + e] = a.scale * qv * expf(gam);
-        S[L.kp + e] = a.decay_only ? 0.f : kv * expf(gam);
-        S[L.km + e] = kv * expf(-gam);
-        S[L.kb + e] = kv * expf(gn - gam);
+        const bool ok = t < nv;
+        const float4 k4 = ld4<T>(k + r * sqk + (int64_t)hk * K + i, ok);
+        const float4 q4 = ld4<T>(q + r * sqk + (int64_t)hk * K + i, ok);
+        const float bt = ok ? (a.decay_only ? 1.f : __ldg(a.beta + r * a.H_v + h)) : 0.f;
+        const float4 g4 = ld4f(Gs + 4 * e4), n4 = ld4f(Gs + 63 * K + i);
+        const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+        const float gam[4] = {g4.x, g4.y, g4.z, g4.w}, gn[4] = {n4.x, n4.y, n4.z, n4.w};
+        float qp[4], kp[4], km[4], kb[4], kbt[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            qp[j] = a.scale * qv[j] * expf(gam[j]);
+            kp[j] = a.decay_only ? 0.f : kv[j] * expf(gam[j]);
+            km[j] = kv[j] * expf(-gam[j]);
+            kb[j] = kv[j] * expf(gn[j] - gam[j]);
+            kbt[j] = bt * kp[j];
+        }
+        st4f(S + L.qp + 4 * e4, make_float4(qp[0], qp[1], qp[2], qp[3]));
+        st4f(S + L.kp + 4 * e4, make_float4(kp[0], kp[1], kp[2], kp[3]));
+        st4f(S + L.km + 4 * e4, make_float4(km[0], km[1], km[2], km[3]));
+        st4f(S + L.kb + 4 * e4, make_float4(kb[0], kb[1], kb[2], kb[3]));
+        st4f(Kbeta + 4 * e4, make_float4(kbt[0], kbt[1], kbt[2], kbt[3]));
     }
-    for (int e = tid; e < 64 * V; e += kT) {
-        const int t = e / V, j = e - t * V;
+    // V, dO, and diag(beta) V for the U product (in the dVt area, free until the adjoint scan)
+    float *Vbeta = S + L.dvt;
+#pragma unroll 2
+    for (int e4 = tid; e4 < 16 * V; e4 += kT) {
+        const int t = e4 / pv, j = 4 * (e4 - t * pv);
         const int64_t r = bos + row0 + t;
-        S[L.vf + e] = t < nv ? ldf<T>(v + r * sv + (int64_t)h * V + j) : 0.f;
-        S[L.dof + e] = t < nv ? ldf<T>(dO + r * sv + (int64_t)h * V + j) : 0.f;
+        const bool ok = t < nv;
+        const float4 v4 = ld4<T>(v + r * sv + (int64_t)h * V + j, ok);
+        const float4 o4 = ld4<T>(dO + r * sv + (int64_t)h * V + j, ok);
+        const float bt = ok ? (a.decay_only ? 1.f : __ldg(a.beta + r * a.H_v + h)) : 0.f;
+        st4f(S + L.vf + 4 * e4, v4);
+        st4f(S + L.dof + 4 * e4, o4);
+        st4f(Vbeta + 4 * e4, make_float4(bt * v4.x, bt * v4.y, bt * v4.z, bt * v4.w));
     }
     __syncthreads();
     // M = Kp Km^T (strictly lower), A = Qp Km^T (lower with the diagonal)
@@ -342,39 +412,56 @@ __global__ void __launch_bounds__(kT, 2) bwd_prep_kernel(const BwdArgs a) {
         Lsh[t * 65 + s] = s < t ? S[L.bt + t] * S[L.m + e] : 0.f;  // L = diag(beta) M
     }
     __syncthreads();
-    // T = (I + L)^-1 by forward substitution, row by row: T[i] = e_i - sum_{j<i} L[i][j] T[j];
-    // each row's sum is split over kGroups groups of 64 threads (j = grp, grp + kGroups, ...)
+    // T = (I + L)^-1 in 16 x 16 blocks. The four diagonal blocks at once: column c of block
+    // b solves (I + L_bb) x = e_c by forward substitution over the block's rows, x_i = [i ==
+    // c] - sum_{c <= k < i} L[i][k] x_k, eight lanes of one warp per column (k = c + sub,
+    // c + sub + 8) adding their parts by shuffles. Then the blocks below the diagonal, one
+    // sub-diagonal d at a time: T_(j+d) j = -T_(j+d)(j+d) sum_{j <= k < j+d} L_(j+d) k T_kj.
     {
-        const int col = tid & 63, grp = tid >> 6;
-        for (int i = 0; i < 64; ++i) {
+        static_assert(kT == 512, "16 warps x 4 columns");
+        const int lane = tid & 31, sub = lane & 7, c = 4 * (tid >> 5) + (lane >> 3);
+        const int b0 = c & ~15;
+        for (int i = b0; i < b0 + 16; ++i) {
             float part = 0.f;
-            for (int j = grp; j < i; j += kGroups) part = fmaf(Lsh[i * 65 + j], Tsh[j * 65 + col], part);
-            red[grp * 64 + col] = part;
+            for (int kk = c + sub; kk < i; kk += 8) part = fmaf(Lsh[i * 65 + kk], Tsh[kk * 65 + c], part);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            part += __shfl_xor_sync(0xffffffffu, part, 4);
+            if (sub == 0) Tsh[i * 65 + c] = (i == c ? 1.f : 0.f) - part;
+            __syncwarp();
+        }
+        for (int e = tid; e < 4096; e += kT) {
+            const int r = e >> 6, cc = e & 63;
+            if ((r >> 4) < (cc >> 4)) Tsh[r * 65 + cc] = 0.f;
+        }
+        __syncthreads();
+        float *P = stage;  // sum_k L_(j+d) k T_kj of each block of the sub-diagonal [j][16][16]
+        for (int d = 1; d < 4; ++d) {
+            const int nb = 4 - d;
+            for (int e = tid; e < nb * 256; e += kT) {
+                const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                const int row = 16 * (j + d) + r, col = 16 * j + cc;
+                float acc = 0.f;
+                for (int kk = 16 * j; kk < 16 * (j + d); ++kk) acc = fmaf(Lsh[row * 65 + kk], Tsh[kk * 65 + col], acc);
+                P[e] = acc;
+            }
             __syncthreads();
-            if (grp == 0) {
-                float sum = 0.f;
+            for (int e = tid; e < nb * 256; e += kT) {
+                const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+                const int row = 16 * (j + d) + r, col = 16 * j + cc;
+                float acc = 0.f;
 #pragma unroll
-                for (int q = 0; q < kGroups; ++q) sum += red[q * 64 + col];
-                Tsh[i * 65 + col] = (col == i ? 1.f : 0.f) - sum;
+                for (int kk = 0; kk < 16; ++kk) acc = fmaf(Tsh[row * 65 + 16 * (j + d) + kk], P[(j << 8) + kk * 16 + cc], acc);
+                Tsh[row * 65 + col] = -acc;
             }
             __syncthreads();
         }
     }
     float *Tm = S + L.t;
     for (int e = tid; e < 4096; e += kT) Tm[e] = Tsh[(e >> 6) * 65 + (e & 63)];
-    // W = T diag(beta) Kp, U = T diag(beta) V: scale the rows first (beta of row s)
-    // (Kb as a temporary would be overwritten: use the dVt and Vt areas, free until the scans)
-    float *Kbeta = S + L.wm;  // W's own area: the product goes to Vt's area first
-    for (int e = tid; e < 64 * K; e += kT) Kbeta[e] = S[L.bt + e / K] * S[L.kp + e];
-    float *Vbeta = S + L.dvt;
-    for (int e = tid; e < 64 * V; e += kT) Vbeta[e] = S[L.bt + e / V] * S[L.vf + e];
-    __syncthreads();
+    // W = T diag(beta) Kp, U = T diag(beta) V (the row-scaled operands were written above)
     block_gemm<SPLIT>(64, V, 64, 1.f, Tsh, 65, 1, Vbeta, V, 1, S + L.u, V, 1, false, stage);
-    // W: T (64 x 64) times Kbeta (64 x K) into the dS' area (free until the adjoint scan),
-    // then copied back over Kbeta
-    float *Wtmp = S + L.dsx;
-    block_gemm<SPLIT>(64, K, 64, 1.f, Tsh, 65, 1, Kbeta, K, 1, Wtmp, K, 1, false, stage);
-    for (int e = tid; e < 64 * K; e += kT) S[L.wm + e] = Wtmp[e];
+    block_gemm<SPLIT>(64, K, 64, 1.f, Tsh, 65, 1, Kbeta, K, 1, S + L.wm, K, 1, false, stage);
 }
 
 // Copy n floats (a multiple of 4, both ends 16-byte aligned) global -> shared with cp.async,
@@ -539,7 +626,7 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         // dT = (dW Kp^T + dVt V^T) diag(beta)
         block_gemm<SPLIT>(64, 64, K, 1.f, dW, K, 1, Kp, 1, K, dT, 64, 1, false, stage);
         block_gemm<SPLIT>(64, 64, V, 1.f, dVt, V, 1, Vf, 1, V, dT, 64, 1, true, stage);
-        for (int e = tid; e < 4096; e += kT) dT[e] *= Bt[e & 63];
+        for (int e = tid; e < 4096; e += kT) dT[e] *= __ldg(Bt + (e & 63));
         __syncthreads();
         // T^T dW -> dKp (then scaled by beta), dbeta += rows of (T^T dW) . Kp
         block_gemm<SPLIT>(64, K, 64, 1.f, Tm, 1, 64, dW, K, 1, dKp, K, 1, false, stage);
@@ -554,12 +641,16 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
             if (lane == 0) dbeta[t] = s;
         }
         __syncthreads();
-        for (int e = tid; e < 64 * K; e += kT) dKp[e] *= Bt[e / K];
+        for (int e = tid; e < 64 * K; e += kT) dKp[e] *= __ldg(Bt + e / K);
         // dv = diag(beta) T^T dVt
         T *dv = static_cast<T *>(a.dv);
-        for (int e = tid; e < 64 * V; e += kT) {
-            const int t = e / V, j = e - t * V;
-            if (t < nv) stf<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j, Bt[t] * TtdU[e]);
+        for (int e4 = tid; e4 < 16 * V; e4 += kT) {
+            const int t = e4 / (V / 4), j = 4 * e4 - t * V;
+            const float b = __ldg(Bt + t);
+            const float4 x = ld4f(TtdU + 4 * e4);
+            if (t < nv)
+                st4<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j,
+                       make_float4(b * x.x, b * x.y, b * x.z, b * x.w));
         }
         // dL = -T^T dT T^T (strictly lower): X = dT T^T, dL = -T^T X into dT's area
         block_gemm<SPLIT>(64, 64, 64, 1.f, dT, 64, 1, Tm, 1, 64, X, 64, 1, false, stage);
@@ -576,7 +667,7 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
             if (lane == 0) dbeta[t] += s;
         }
         __syncthreads();
-        for (int e = tid; e < 4096; e += kT) dL[e] *= Bt[e >> 6];
+        for (int e = tid; e < 4096; e += kT) dL[e] *= __ldg(Bt + (e >> 6));
         __syncthreads();
         // dKp += dM Km;  dKm += dM^T Kp
         block_gemm<SPLIT>(64, K, 64, 1.f, dL, 64, 1, Km, K, 1, dKp, K, 1, true, stage);
@@ -584,9 +675,10 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
     } else {
         // decay-only: U = V, W = 0: dv = dVt
         T *dv = static_cast<T *>(a.dv);
-        for (int e = tid; e < 64 * V; e += kT) {
-            const int t = e / V, j = e - t * V;
-            if (t < nv) stf<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j, dVt[e]);
+        for (int e4 = tid; e4 < 16 * V; e4 += kT) {
+            const int t = e4 / (V / 4), j = 4 * e4 - t * V;
+            if (t < nv) st4<T>(dv + (bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + j, __ldg(
+                                   reinterpret_cast<const float4 *>(dVt) + e4));
         }
         for (int e = tid; e < 64 * K; e += kT) dKp[e] = 0.f;
         __syncthreads();
@@ -596,24 +688,46 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
     // once each), dgamma in dQp's area
     float *dqa = a.dq_acc, *dka = a.dk_acc;
     T *dq = static_cast<T *>(a.dq), *dk = static_cast<T *>(a.dk);
-    for (int e = tid; e < 64 * K; e += kT) {
-        const int t = e / K, i = e - t * K;
-        const float gam = Gm[e], gn = Gm[63 * K + i];
-        const float ep = expf(gam), em = expf(-gam), eb = expf(gn - gam);
-        const float vq = dQp[e], vkp = dKp[e], vkm = dKm[e], vkb = dKb[e];
+#pragma unroll 2
+    for (int e4 = tid; e4 < 16 * K; e4 += kT) {
+        const int t = e4 / (K / 4), i = 4 * e4 - t * K;
+        const float4 g4 = __ldg(reinterpret_cast<const float4 *>(Gm) + e4);
+        const float4 n4 = __ldg(reinterpret_cast<const float4 *>(Gm + 63 * K + i));
+        const float4 qp4 = __ldg(reinterpret_cast<const float4 *>(Qp) + e4);
+        const float4 kp4 = __ldg(reinterpret_cast<const float4 *>(Kp) + e4);
+        const float4 km4 = __ldg(reinterpret_cast<const float4 *>(Km) + e4);
+        const float4 kb4 = __ldg(reinterpret_cast<const float4 *>(Kb) + e4);
+        const float4 vq4 = ld4f(dQp + 4 * e4), vkp4 = ld4f(dKp + 4 * e4), vkm4 = ld4f(dKm + 4 * e4),
+                     vkb4 = ld4f(dKb + 4 * e4);
+        const float gam[4] = {g4.x, g4.y, g4.z, g4.w}, gn[4] = {n4.x, n4.y, n4.z, n4.w};
+        const float qp[4] = {qp4.x, qp4.y, qp4.z, qp4.w}, kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
+        const float km[4] = {km4.x, km4.y, km4.z, km4.w}, kb[4] = {kb4.x, kb4.y, kb4.z, kb4.w};
+        const float vq[4] = {vq4.x, vq4.y, vq4.z, vq4.w}, vkp[4] = {vkp4.x, vkp4.y, vkp4.z, vkp4.w};
+        const float vkm[4] = {vkm4.x, vkm4.y, vkm4.z, vkm4.w}, vkb[4] = {vkb4.x, vkb4.y, vkb4.z, vkb4.w};
+        float gq[4], gk[4], dgam[4], dkb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float ep = expf(gam[j]), em = expf(-gam[j]), eb = expf(gn[j] - gam[j]);
+            gq[j] = a.scale * ep * vq[j];
+            gk[j] = ep * vkp[j] + em * vkm[j] + eb * vkb[j];
+            dgam[j] = vq[j] * qp[j] + vkp[j] * kp[j] - vkm[j] * km[j] - vkb[j] * kb[j];
+            dkb[j] = vkb[j] * kb[j];
+        }
         if (t < nv) {
             const int64_t o = ((bos + row0 + t) * a.H_k + hk) * K + i;
-            const float gq = a.scale * ep * vq, gk = ep * vkp + em * vkm + eb * vkb;
             if (a.direct_qk) {
-                stf<T>(dq + o, gq);
-                stf<T>(dk + o, gk);
+                st4<T>(dq + o, make_float4(gq[0], gq[1], gq[2], gq[3]));
+                st4<T>(dk + o, make_float4(gk[0], gk[1], gk[2], gk[3]));
             } else {
-                atomicAdd(dqa + o, gq);
-                atomicAdd(dka + o, gk);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    atomicAdd(dqa + o + j, gq[j]);
+                    atomicAdd(dka + o + j, gk[j]);
+                }
             }
         }
-        dQp[e] = vq * Qp[e] + vkp * Kp[e] - vkm * Km[e] - vkb * Kb[e];  // dgamma
-        dKb[e] = vkb * Kb[e];                                             // for dGn
+        st4f(dQp + 4 * e4, make_float4(dgam[0], dgam[1], dgam[2], dgam[3]));  // dgamma
+        st4f(dKb + 4 * e4, make_float4(dkb[0], dkb[1], dkb[2], dkb[3]));      // for dGn
     }
     __syncthreads();
     for (int i = tid; i < K; i += kT) {
