@@ -474,42 +474,52 @@ __device__ __forceinline__ void stage_rows(float *dst, const float *src, int row
     }
 }
 
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;\n" ::); }
+
 // ---- states: the forward scan, S slice [K][64 columns] in shared memory -----------------------
-// Per chunk the operands (W, Kb [64][K], U's 64 columns, e^Gn) are copied into shared memory
-// first, so that the products read no global memory.
-size_t states_smem(int K) { return sizeof(float) * ((size_t)K * 64 * 3 + 64 * 64 + K + kStageFloats); }
+// Per chunk the operands (W, Kb [64][K], U's 64 columns, e^Gn) are copied into shared memory,
+// so that the products read no global memory; two buffers, the next chunk's copy in flight
+// while the current chunk is computed.
+size_t states_smem(int K) {
+    return sizeof(float) * ((size_t)K * 64 + 2 * ((size_t)K * 64 * 2 + 64 * 64 + K) + kStageFloats);
+}
 
 template <bool SPLIT>
 __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
-    float *St = sm;              // S [K][64]
-    float *Ws = St + K * 64;     // W [64][K]
-    float *Kbs = Ws + 64 * K;    // Kb [64][K]
-    float *Us = Kbs + 64 * K;    // U, then Vt [64][64]
-    float *EGs = Us + 64 * 64;   // e^Gn [K]
-    float *stage = EGs + K;
+    float *St = sm;                          // S [K][64]
+    float *buf = St + K * 64;                // two buffers of the chunk operands
+    const int bstride = K * 64 * 2 + 64 * 64 + K;
+    float *stage = buf + 2 * bstride;
     const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const Lay L = make_lay(K, V);
     int64_t bos;
     int len;
     if (!bounds(a, n, bos, len)) return;
     const int nch = (len + 63) / 64;
-    for (int e = tid; e < K * 64; e += kT) {
-        const int i = e >> 6, j = e & 63;
-        St[e] = a.h0 ? a.h0[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
-    }
-    __syncthreads();
-    for (int c = 0; c < nch; ++c) {
-        float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+    // buffer b: W [64][K], Kb [64][K], U, then Vt [64][64], e^Gn [K]
+    auto issue = [&](int c) {
+        const float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+        float *Ws = buf + (c & 1) * bstride, *Kbs = Ws + 64 * K, *Us = Kbs + 64 * K, *EGs = Us + 64 * 64;
         stage_rows(Ws, S + L.wm, 64, K, K);
         stage_rows(Kbs, S + L.kb, 64, K, K);
         stage_rows(Us, S + L.u + j0, 64, 64, V);
         stage_rows(EGs, S + L.eg, 1, K, K);
         cp_async_commit();
-        for (int e = tid; e < K * 64; e += kT) S[L.se + (int64_t)(e >> 6) * V + j0 + (e & 63)] = St[e];
+    };
+    if (nch > 0) issue(0);
+    for (int e = tid; e < K * 64; e += kT) {
+        const int i = e >> 6, j = e & 63;
+        St[e] = a.h0 ? a.h0[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
+    }
+    for (int c = 0; c < nch; ++c) {
+        float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+        float *Ws = buf + (c & 1) * bstride, *Kbs = Ws + 64 * K, *Us = Kbs + 64 * K, *EGs = Us + 64 * 64;
         cp_async_wait_all();
         __syncthreads();
+        if (c + 1 < nch) issue(c + 1);  // into the buffer chunk c - 1 used
+        for (int e = tid; e < K * 64; e += kT) S[L.se + (int64_t)(e >> 6) * V + j0 + (e & 63)] = St[e];
         // Vt = U - W S (in U's place), stored for the gradient kernel
         block_gemm<SPLIT>(64, 64, K, -1.f, Ws, K, 1, St, 64, 1, Us, 64, 1, true, stage);
         for (int e = tid; e < 64 * 64; e += kT) S[L.vt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = Us[e];
@@ -521,8 +531,11 @@ __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
 }
 
 // ---- adjoint: the reverse scan, dS slice [K][64 columns] in shared memory -------------------
+// The chunk's operands are copied into shared memory in two sets: A, Kb, e^Gn and dO for the
+// first products, Qp and W for the second. Each set's buffer is refilled with the next chunk's
+// set as soon as the current chunk is done with it (dO, used by both, has two buffers).
 size_t adjoint_smem(int K) {
-    return sizeof(float) * ((size_t)K * 64 * 4 + 3 * 64 * 64 + K + kStageFloats);
+    return sizeof(float) * ((size_t)K * 64 * 4 + 4 * 64 * 64 + 2 * K + kStageFloats);
 }
 
 template <bool SPLIT>
@@ -534,42 +547,63 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     float *Qps = Kbs + 64 * K;    // Qp [64][K]
     float *Ws = Qps + 64 * K;     // W [64][K]
     float *As = Ws + 64 * K;      // A [64][64]
-    float *dOs = As + 64 * 64;    // dO's 64 columns [64][64]
-    float *dVs = dOs + 64 * 64;   // dVt [64][64]
-    float *EGs = dVs + 64 * 64;   // e^Gn [K]
-    float *stage = EGs + K;
+    float *dOb = As + 64 * 64;    // dO's 64 columns [64][64], two buffers
+    float *dVs = dOb + 2 * 64 * 64;  // dVt [64][64]
+    float *EGb = dVs + 64 * 64;   // e^Gn [K], two buffers
+    float *stage = EGb + 2 * K;
     const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const Lay L = make_lay(K, V);
     int64_t bos;
     int len;
     if (!bounds(a, n, bos, len)) return;
     const int nch = (len + 63) / 64;
+    auto slot = [&](int c) { return a.scratch + slot_of(a, bos, n, c, h) * L.total; };
+    auto issue_first = [&](int c) {
+        const float *S = slot(c);
+        stage_rows(Kbs, S + L.kb, 64, K, K);
+        stage_rows(As, S + L.a, 64, 64, 64);
+        stage_rows(dOb + (c & 1) * 4096, S + L.dof + j0, 64, 64, V);
+        stage_rows(EGb + (c & 1) * K, S + L.eg, 1, K, K);
+        cp_async_commit();
+    };
+    auto issue_second = [&](int c) {
+        const float *S = slot(c);
+        stage_rows(Qps, S + L.qp, 64, K, K);
+        stage_rows(Ws, S + L.wm, 64, K, K);
+        cp_async_commit();
+    };
+    if (nch > 0) {
+        issue_first(nch - 1);
+        issue_second(nch - 1);
+    }
     for (int e = tid; e < K * 64; e += kT) {
         const int i = e >> 6, j = e & 63;
         dS[e] = a.dht ? a.dht[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
     }
-    __syncthreads();
     for (int c = nch - 1; c >= 0; --c) {
-        float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
-        stage_rows(Kbs, S + L.kb, 64, K, K);
-        stage_rows(Qps, S + L.qp, 64, K, K);
-        stage_rows(Ws, S + L.wm, 64, K, K);
-        stage_rows(As, S + L.a, 64, 64, 64);
-        stage_rows(dOs, S + L.dof + j0, 64, 64, V);
-        stage_rows(EGs, S + L.eg, 1, K, K);
-        cp_async_commit();
-        for (int e = tid; e < K * 64; e += kT) S[L.dsx + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dS[e];
-        cp_async_wait_all();
+        float *S = slot(c);
+        float *dOs = dOb + (c & 1) * 4096, *EGs = EGb + (c & 1) * K;
+        // the groups in flight are this chunk's two sets, oldest first
+        cp_async_wait_one();
         __syncthreads();
+        for (int e = tid; e < K * 64; e += kT) S[L.dsx + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dS[e];
         // dVt = A^T dO + Kb dS', stored for the gradient kernel
         block_gemm<SPLIT>(64, 64, 64, 1.f, As, 1, 64, dOs, 64, 1, dVs, 64, 1, false, stage);
         block_gemm<SPLIT>(64, 64, K, 1.f, Kbs, K, 1, dS, 64, 1, dVs, 64, 1, true, stage);
+        // A and Kb are consumed: the previous chunk's first set (its dO into the other buffer)
+        if (c > 0) {
+            issue_first(c - 1);
+            cp_async_wait_one();  // this chunk's second set
+        } else {
+            cp_async_wait_all();
+        }
         for (int e = tid; e < 64 * 64; e += kT) S[L.dvt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dVs[e];
         // dS <- diag(EG) dS' + Qp^T dO - W^T dVt
         for (int e = tid; e < K * 64; e += kT) dS[e] *= EGs[e >> 6];
         __syncthreads();
         block_gemm<SPLIT>(K, 64, 64, 1.f, Qps, 1, K, dOs, 64, 1, dS, 64, 1, true, stage);
         block_gemm<SPLIT>(K, 64, 64, -1.f, Ws, 1, K, dVs, 64, 1, dS, 64, 1, true, stage);
+        if (c > 0) issue_second(c - 1);  // Qp and W are consumed
     }
     if (a.dh0 != nullptr)
         for (int e = tid; e < K * 64; e += kT)
