@@ -103,7 +103,8 @@ struct Common {
     static constexpr int oFlag = oTmemAddr + 16;   // CTA abort flag
     static constexpr int oUnits = oFlag + 16;      // UnitInfo [kMaxUnits]
     static constexpr int oSeen = oUnits + 16 * kMaxUnits;  // producer: done[u] last observed
-    static constexpr int kEnd = oSeen + 4 * kMaxUnits;
+    static constexpr int oJobq = oSeen + 4 * kMaxUnits;    // producer: claimed jobs [4]
+    static constexpr int kEnd = oJobq + 16;
     static constexpr int kBytes = kEnd + 1024;      // + slack to align the base
 };
 
@@ -141,6 +142,7 @@ struct PcArgs {
     int *ready;            // [U][R]: c + 1 once chunk c is in slot c % R
     int *done;             // [U]: chunks whose slot image has been copied out
     int *abort;            // set by any CTA that gave up
+    int *jobs;             // equal-length units: the next job not yet claimed by a producer
     int U, P;              // units (= consumer CTAs), producer CTAs
     int R;                 // ring slots per unit
 };
@@ -231,6 +233,7 @@ struct Ctx {
     volatile int *flag;     // this CTA is aborting
     volatile int *stored;   // producer: jobs whose front image is written to the ring
     int *seen;              // producer, thread 0: done[u] as last acquired, per unit
+    volatile int *jobq;     // producer, equal-length units: claimed job of ordinal jo at [jo % 4]
     const UnitInfo *units;  // [U]
     int maxc, uniform;      // over the units of this launch
     int p;                  // producer index (producer CTAs)
@@ -259,13 +262,17 @@ __device__ __forceinline__ bool wait_count(const volatile int *p, int target, vo
 struct JobIt {
     int c, u, k;  // current pair and its index among all jobs
 };
+// Jobs are taken in the order (chunk, unit). With units of equal length a producer claims
+// its next job from a global counter (set_job), so that faster producers take more jobs and
+// every producer stays near the common front of that order; otherwise producer p takes the
+// jobs p, p + P, p + 2P, ... of the order (next_job), skipping the chunks a unit lacks.
+__device__ __forceinline__ bool set_job(JobIt &it, int k, const Ctx &x, const PcArgs &pc) {
+    it.k = k;
+    it.c = k / pc.U;
+    it.u = k - it.c * pc.U;
+    return it.c < x.maxc;
+}
 __device__ __forceinline__ bool next_job(JobIt &it, const Ctx &x, const PcArgs &pc) {
-    if (x.uniform) {
-        it.k = it.k < 0 ? x.p : it.k + pc.P;
-        it.c = it.k / pc.U;
-        it.u = it.k - it.c * pc.U;
-        return it.c < x.maxc;
-    }
     const int want = it.k < 0 ? x.p : it.k + pc.P;
     while (true) {
         if (++it.u == pc.U) {
@@ -358,20 +365,30 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
     };
 
     JobIt it{0, -1, -1};
-    bool have = next_job(it, x, pc);
+    bool have = x.uniform ? set_job(it, x.jobq[0], x, pc) : next_job(it, x, pc);
     if (have) {
         stage_g(it, 0);
         stage_qk(it, 0);
     }
     bool failed = false;
     int jo = 0;
+    int claimed = 0;  // thread 0, equal lengths: the job claimed for ordinal jo + 2
     for (; have; ++jo) {
         const int u = it.u, c = it.c, b = jo & 1;
         const int row0 = c * kChunk;
         const int nvalid = min(kChunk, x.units[u].len - row0);
         const int nz = kChunk - nvalid;  // rows past the sequence end: zero in every operand
+        // The next job (equal lengths): thread 0 claimed it at the top of the previous job
+        // (the atomic's latency is then off the path) and publishes it here; every thread
+        // reads it after the first barrier below, the back stage after this job's hand-off.
         JobIt nx = it;
-        const bool have_next = next_job(nx, x, pc);
+        bool have_next = false;
+        if (!x.uniform) {
+            have_next = next_job(nx, x, pc);
+        } else if (ptid == 0) {
+            if (jo > 0) x.jobq[(jo + 1) & 3] = claimed;  // jobs 0 and 1 were claimed at the start
+            claimed = atomicAdd(pc.jobs, 1);              // job jo + 2
+        }
         const uint32_t oKP = b ? Prod::oKP1 : Prod::oKP0;
         float *Bf = reinterpret_cast<float *>(sm + (b ? Prod::oBF1 : Prod::oBF0));
         float *Gh = reinterpret_cast<float *>(sm + (b ? Prod::oGh1 : Prod::oGh0));
@@ -404,6 +421,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         }
         if constexpr (!GATE_HEAD) failed = !wait_bar(&bars[B_LG], (uint32_t)(jo & 1), x.flag, a, pc);
         if (bar_or(1, 256, failed)) { failed = true; break; }
+        if (x.uniform) have_next = set_job(nx, x.jobq[(jo + 1) & 3], x, pc);
         pend &= ~2u;
         if (!GATE_HEAD && nz > 0) {
             for (int i = ptid; i < nz * 32; i += 256) {
@@ -674,7 +692,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
     };
 
     JobIt it{0, -1, -1};
-    bool have = next_job(it, x, pc);
+    bool have = x.uniform ? set_job(it, x.jobq[0], x, pc) : next_job(it, x, pc);
     if (have) stage_v(it, 0);
     bool failed = false;
     int prev_u = -1, prev_c = 0;
@@ -685,7 +703,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         const int nvalid = min(kChunk, x.units[u].len - row0);
         const int nz = kChunk - nvalid;
         JobIt nx = it;
-        const bool have_next = next_job(nx, x, pc);
+        bool have_next = x.uniform ? false : next_job(nx, x, pc);  // equal lengths: after the hand-off
         unsigned char *slot = slot_ptr(pc, u, c);
         const uint32_t oKP = b ? Prod::oKP1 : Prod::oKP0;
 
@@ -700,6 +718,8 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         }
         if (!failed) failed = !wait_bar(&bars[B_HFULL0 + b], (uint32_t)((jo >> 1) & 1), x.flag, a, pc);
         if (bar_or(2, 256, failed)) { failed = true; break; }
+        // the front stage claimed the next job before it handed this one off
+        if (x.uniform) have_next = set_job(nx, x.jobq[(jo + 1) & 3], x, pc);
 
         // ---- solve: T = (I + L)^-1 -----------------------------------------------------------
         // Warps 0-3 invert (I + L) as a 2 x 2 block matrix of 32 x 32 blocks A (tokens 0-31)
@@ -1116,6 +1136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *stored = reinterpret_cast<volatile int *>(sm + Common::oFlag + 12);
     UnitInfo *units = reinterpret_cast<UnitInfo *>(sm + Common::oUnits);
     int *seen = reinterpret_cast<int *>(sm + Common::oSeen);
+    volatile int *jobq = reinterpret_cast<volatile int *>(sm + Common::oJobq);
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool consumer = (int)blockIdx.x < pc.U;
     const uint32_t ncols = consumer ? kTmemCons : kTmemProd;
@@ -1156,6 +1177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < pc.U; ++i) uni &= units[i].nch == mx ? 1 : 0;
         stats[0] = mx;
         stats[1] = uni;
+        if (uni && !consumer) {  // this producer's first two jobs
+            jobq[0] = atomicAdd(pc.jobs, 1);
+            jobq[1] = atomicAdd(pc.jobs, 1);
+        }
     }
     __syncthreads();
 
@@ -1167,6 +1192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.flag = flag;
     x.stored = stored;
     x.seen = seen;
+    x.jobq = jobq;
     x.units = units;
     x.maxc = stats[0];
     x.uniform = stats[1];
@@ -1284,7 +1310,7 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     // inside L2), so that producers taking jobs in order rarely wait for a slow consumer
     const int R = (int)std::max<int64_t>(kRing, std::min<int64_t>(4 * kRing, 512 / U));
     const size_t ring_bytes = (size_t)U * R * Slot::kStride;
-    const size_t flag_words = (size_t)U * R + (size_t)U + 1;
+    const size_t flag_words = (size_t)U * R + (size_t)U + 2;  // ready, done, abort, jobs
     const size_t flag_bytes = (flag_words * sizeof(int) + 255) & ~(size_t)255;
     cudaMemPool_t pool = nullptr;
     e = scratch_pool(dev, &pool);
@@ -1297,6 +1323,7 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     pc.ready = reinterpret_cast<int *>(pc.ring + ring_bytes);
     pc.done = pc.ready + (size_t)U * R;
     pc.abort = pc.done + U;
+    pc.jobs = pc.abort + 1;
     pc.U = (int)U;
     pc.P = sms - (int)U;
     pc.R = R;
@@ -1316,8 +1343,8 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
 // not overlap (on any stream or thread): they share this one array.
 constexpr int kStaticUnits = 16;
 constexpr size_t kStaticRingBytes = (size_t)kStaticUnits * kRing * Slot::kStride;      // 9,568,256 B
-constexpr size_t kStaticFlagBytes = 1024;  // >= (kStaticUnits * (kRing + 1) + 1) ints
-static_assert((kStaticUnits * (kRing + 1) + 1) * sizeof(int) <= kStaticFlagBytes, "flag room");
+constexpr size_t kStaticFlagBytes = 1024;  // >= (kStaticUnits * (kRing + 1) + 2) ints
+static_assert((kStaticUnits * (kRing + 1) + 2) * sizeof(int) <= kStaticFlagBytes, "flag room");
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticRingBytes + kStaticFlagBytes];
 
 std::mutex g_static_mu;
@@ -1367,6 +1394,7 @@ cudaError_t launch_pc_static(const FwdArgs &a, cudaStream_t stream) {
     pc.ready = reinterpret_cast<int *>(base + kStaticRingBytes);
     pc.done = pc.ready + (size_t)U * kRing;
     pc.abort = pc.done + U;
+    pc.jobs = pc.abort + 1;
     pc.U = (int)U;
     pc.P = sms - (int)U;
     pc.R = kRing;
