@@ -237,13 +237,22 @@ __device__ void block_gemm(int M, int N, int K, float alpha, const float *A, int
                 }
                 __syncthreads();
             }
+            // The accumulators of a row half (c[f][2 hq + qi]: row mb + g + 8 hq, column nb +
+            // 8 f + 2 t + qi) go out in four rounds; in round rr lane g writes choice (g + rr)
+            // % 4 of (f, qi), so that one store touches 16 columns instead of 4 (C's rows are
+            // often a multiple of 32 words apart in shared memory: 2-way instead of 8-way
+            // bank conflicts).
 #pragma unroll
-            for (int f = 0; f < 2; ++f)
+            for (int hq = 0; hq < 2; ++hq)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int m = m0 + mb + g + (q >= 2 ? 8 : 0), n = n0 + nb + 8 * f + 2 * t + (q & 1);
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int j = (g + rr) & 3, f = j >> 1, qi = j & 1;
+                    const float v0 = qi ? c[0][2 * hq + 1] : c[0][2 * hq];
+                    const float v1 = qi ? c[1][2 * hq + 1] : c[1][2 * hq];
+                    const float v = f ? v1 : v0;
+                    const int m = m0 + mb + g + 8 * hq, n = n0 + nb + 8 * f + 2 * t + qi;
                     float *p = C + (int64_t)m * cm + (int64_t)n * cn;
-                    *p = acc ? fmaf(alpha, c[f][q], *p) : alpha * c[f][q];
+                    *p = acc ? fmaf(alpha, v, *p) : alpha * v;
                 }
         }
     }
