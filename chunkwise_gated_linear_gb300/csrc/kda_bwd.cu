@@ -26,11 +26,12 @@
 //   states   (unit, 64 columns of d_v): the forward state scan, storing S and Vt per chunk
 //   adjoint  (unit, 64 columns of d_v): the reverse scan of dS, storing dS' and dVt per
 //            chunk, and dh0
-//   grads    (chunk, unit) parallel: every gradient above; dq and dk added atomically into
-//            fp32 accumulators (value heads that share a key head add into the same rows)
-//   finish   the accumulators to the output dtype (bf16 outputs)
-// Every contraction goes through one CTA-wide fp32 GEMM (64 x 64 output tiles, 16-deep
-// k steps staged in shared memory, 4 x 4 outputs per thread).
+//   grads    (chunk, unit) parallel: every gradient above; dq and dk written directly when
+//            each key head has one value head, else added atomically into fp32
+//            accumulators (value heads that share a key head add into the same rows)
+//   finish   the accumulators to the output dtype (grouped heads, bf16 outputs)
+// Every contraction goes through one CTA-wide GEMM on tf32 tensor cores (block_gemm: 64 x 64
+// output tiles, 32-deep k steps staged in shared memory, fp32 accumulation).
 #include <algorithm>
 #include <cstdint>
 #include <type_traits>
