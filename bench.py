@@ -468,7 +468,7 @@ def run_ours(args, world, rank, local, pg):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import oracle_threads
 
-        n_units = min(32, x.N * x.H_v)  # about 20-30 s of CPU work
+        n_units = min(64, x.N * x.H_v)  # about 15-30 s of CPU work (0.25 s per unit-core of 8192 tokens)
         dt_cpu, tok_cpu, used = oracle_sample(x, n_units)
         cpu = {"value": tok_cpu / dt_cpu, "unit": "tokens/s", "cores": used, "kind": "oracle",
                "sample": f"{n_units} of {x.N * x.H_v} (sequence, head) units of {args.workload} "
