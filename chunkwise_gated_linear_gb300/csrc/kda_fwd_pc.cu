@@ -707,6 +707,14 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         unsigned char *slot = slot_ptr(pc, u, c);
         const uint32_t oKP = b ? Prod::oKP1 : Prod::oKP0;
 
+        // The previous job's W^T and U^T stores read the T buffer and its Kp^T buffer: the
+        // publisher waits for those reads here, ahead of the barrier after the hand-off
+        // (before which no thread of this stage writes either buffer), so that the wait
+        // overlaps the wait for the front stage, and then returns the Kp^T buffer to it.
+        if (ptid == kPublisher && jo > 0) {
+            bulk_wait_read();
+            mbar_arrive(&bars[B_HEMPTY0 + (b ^ 1)]);
+        }
         // The previous job is published while this stage would wait for the front stage;
         // when the front stage is already done with this job, the publisher does it during
         // the diagonal solve instead (its warp is idle there). Either way it waits on
@@ -901,10 +909,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
             bulk_store(slot + Slot::oWT, sm + Prod::oT, 16384);
             bulk_store(slot + Slot::oU, sm + oKP, 16384);
             bulk_commit();
-            bulk_wait_read();
-            mbar_arrive(&bars[B_HEMPTY0 + b]);  // the Kp^T buffer of slot b is free again
         }
-        bar_named(2, 256);  // the T buffer is free again
         prev_u = u;
         prev_c = c;
         it = nx;
