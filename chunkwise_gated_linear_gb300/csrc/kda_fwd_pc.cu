@@ -9,17 +9,19 @@
 //
 //   producer CTA, one chunk job after another, two stages working on consecutive jobs:
 //     front (warps 0-7)   TMA Q, K, G; gamma = chunk-local cumulative log2 gate;
-//                         Qp = scale Q e^gamma, Kp = K e^gamma, Km = K e^-gamma,
-//                         Kbar = Km e^gamma_n (transposed, bf16);
+//                         Qp = scale Q e^gamma, Kp = K e^gamma, Km = K e^-gamma
+//                         (transposed, bf16);
 //                         Gram D_G = [Qp; Kp] Km^T -> Aqk (lower), L = diag(beta) M (strict)
 //     back  (warps 8-15)  T = (I + L)^-1 (16x16 diagonal blocks by substitution, the rest
 //                         on tf32 mma.sync); D_W = Kp^T (T diag beta)^T, D_U = V^T (T diag beta)^T
-//     -> the chunk's slot in a per-unit ring in global memory: W^T, Qp^T, Kbar^T, Aqk (bf16,
+//     -> the chunk's slot in a per-unit ring in global memory: W^T, Qp^T, Km^T, Aqk (bf16,
 //        in the consumer's 128-byte swizzled shared-memory image), U^T (bf16), e^gamma_n.
-//   consumer CTA (unit u), state S^T [d_v x d_k] fp32 in TMEM, thread = d_v row:
+//   consumer CTA (unit u), TMEM holds R [d_v x d_k] fp32 with S_c^T = R Diag(e^gamma_n of
+//   chunk c - 1), thread = d_v row (Kbar = Km Diag(e^gamma_n) is never formed):
 //     one bulk copy per chunk brings the slot into shared memory (double-buffered), then
-//     D_X = S^T [W^T | Qp^T];  S^T <- S^T Diag(e^gamma_n);  Vt^T = U^T - D_X[:, :64];
-//     O^T = D_X[:, 64:] + Vt^T Aqk^T;  S^T += Vt^T Kbar.
+//     D_X = S_c^T [W^T | Qp^T] (A: the bf16 copy of S_c^T);  R <- R Diag(e^gamma_n, c - 1);
+//     Vt^T = U^T - D_X[:, :64];  O^T = D_X[:, 64:] + Vt^T Aqk^T;  R += Vt^T Km;
+//     bf16 copy of S_{c+1}^T = R Diag(e^gamma_n, c).
 //
 // Hand-offs through global memory use per-slot sequence numbers: a producer publishes
 // chunk c of unit u by a release store of c + 1 into ready[u][c % R] after its writes;
@@ -50,7 +52,7 @@ constexpr int kThreads = 512;
 struct Slot {
     static constexpr int oWT = 0;       // W^T [d][tok] bf16     } adjacent: one N = 128
     static constexpr int oQP = 16384;   // Qp^T [d][tok] bf16    } MN-major B operand
-    static constexpr int oKB = 32768;   // Kbar^T [d][tok] bf16 (K-major B)
+    static constexpr int oKM = 32768;   // Km^T [d][tok] bf16 (K-major B)
     static constexpr int oAQ = 49152;   // Aqk [tok][tok'] bf16 (K-major B)
     static constexpr int oEG = 57344;   // e^gamma_n [128] fp32
     static constexpr int oU = 57856;    // U^T as bf16 token pairs: u32 [tok / 2][d_v]
@@ -68,13 +70,13 @@ struct Prod {
     static constexpr int oIMG = 65536;     // the front part of the slot image (Slot::oQP ..
                                            // Slot::oU); its Qp^T is also the Gram A operand
     static constexpr int oQP = oIMG;
-    static constexpr int oKB = oIMG + (Slot::oKB - Slot::oQP);
+    static constexpr int oKM = oIMG + (Slot::oKM - Slot::oQP);  // also the Gram's B operand
     static constexpr int oAQ = oIMG + (Slot::oAQ - Slot::oQP);
     static constexpr int oEG = oIMG + (Slot::oEG - Slot::oQP);
     static constexpr int oKP0 = 107520;    // Kp^T [d][tok], hand-off slots 0 / 1 (Gram A atom 1);
                                            // then U^T staging of the back stage
     static constexpr int oKP1 = 123904;
-    static constexpr int oKM = 140288;     // Km^T [d][tok]
+                                           // 140288 .. 156672: free
     static constexpr int oL = 156672;      // L fp32 [64][68] (front -> back)
     static constexpr int oT = 174080;      // T fp32 [64][68]; then W^T staging [d][tok] bf16
     static constexpr int oTB = 191488;     // T_beta [tok][tok'] bf16 (K-major B)
@@ -104,11 +106,14 @@ struct Common {
     static constexpr int oUnits = oFlag + 16;      // UnitInfo [kMaxUnits]
     static constexpr int oSeen = oUnits + 16 * kMaxUnits;  // producer: done[u] last observed
     static constexpr int oJobq = oSeen + 4 * kMaxUnits;    // producer: claimed jobs [4]
-    static constexpr int kEnd = oJobq + 16;
+    static constexpr int oEGc = oJobq + 16;                // consumer: e^gamma_n of chunks, [2][128] fp32
+                                                           // (16-byte aligned: read as float4)
+    static constexpr int kEnd = oEGc + 1024;
     static constexpr int kBytes = kEnd + 1024;      // + slack to align the base
 };
 
 static_assert(Common::kBytes <= 232448, "shared memory");
+static_assert(Common::oEGc % 16 == 0, "float4 reads of the e^gamma_n copies");
 
 // TMEM columns
 constexpr uint32_t tGram = 0, tW = 64, tU = 128, kTmemProd = 256;     // producer
@@ -549,8 +554,8 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     const int cc = ch ? c1 : c0;
-                    const float off = ch ? off1 : off0, eg = ch ? eg1 : eg0;
-                    float kp[8], km[8], qp[8], kb[8];
+                    const float off = ch ? off1 : off0;
+                    float kp[8], km[8], qp[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int r = 16 * qr + 8 * j + e;
@@ -566,13 +571,11 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
                         kp[e] = a.decay_only ? 0.f : kv * ep;
                         km[e] = kv * em;
                         qp[e] = qs * qv * ep;
-                        kb[e] = km[e] * eg;
                     }
                     const uint32_t sw = sw128(cc, tc);
                     *reinterpret_cast<uint4 *>(sm + Prod::oQP + sw) = pack8(qp);
                     *reinterpret_cast<uint4 *>(sm + oKP + sw) = pack8(kp);
                     *reinterpret_cast<uint4 *>(sm + Prod::oKM + sw) = pack8(km);
-                    *reinterpret_cast<uint4 *>(sm + Prod::oKB + sw) = pack8(kb);
                 }
             }
         }
@@ -634,7 +637,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         bar_named(1, 256);
         if (ptid == 0) mbar_arrive(&bars[B_HFULL0 + b]);
         if (ptid == kIssImg) {
-            // Qp^T, Kbar^T, Aqk, e^gamma_n -> the ring slot, one bulk store; once it is
+            // Qp^T, Km^T, Aqk, e^gamma_n -> the ring slot, one bulk store; once it is
             // written the image buffer is free and the back stage may publish the job
             bulk_store(slot_ptr(pc, u, c) + Slot::oQP, sm + Prod::oIMG, Slot::kFrontBytes);
             bulk_commit();
@@ -978,6 +981,9 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
     const int64_t sv = (int64_t)a.H_v * 128;
     bf16 *o = static_cast<bf16 *>(a.o);
     const uint32_t tSc = tS + 64 * grp, tSAc = tSA + 32 * grp;  // this thread's columns
+    // e^gamma_n of the chunks by parity: the slot buffer is released before the state's bf16
+    // copy (and the next chunk's rescale) would read it
+    float *egc = reinterpret_cast<float *>(sm + Common::oEGc);
 
     // S^T row dv, columns 64 grp .. +63 (from h0, or zero) -> TMEM fp32 and its bf16 copy
 #pragma unroll 1
@@ -1040,24 +1046,30 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
                        s > 0);
             commit(&bars[B_X]);
         }
-        // meanwhile the previous chunk's output leaves, and S^T <- S^T Diag(e^gamma_n)
-        // (column d of S^T scales by e^gamma_n[d])
+        // meanwhile the previous chunk's output leaves, this chunk's e^gamma_n is kept, and
+        // R <- R Diag(e^gamma_n of chunk c - 1) = S_c^T (column d scales by e^gamma_n[d])
         if (c > 0) write_o(c - 1);
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-            float v[32];
-            tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
-            const float *eg = EG + 64 * grp + 32 * pass;
-            uint32_t y0[16], y1[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                y0[e] = __float_as_uint(v[e] * eg[e]);
-                y1[e] = __float_as_uint(v[16 + e] * eg[16 + e]);
-            }
-            tmem_st16(tmem + lane_off + tSc + 32 * pass, y0);
-            tmem_st16(tmem + lane_off + tSc + 32 * pass + 16, y1);
+        if ((warp & 3) == 0) {
+            egc[(c & 1) * 128 + 64 * grp + lane] = EG[64 * grp + lane];
+            egc[(c & 1) * 128 + 64 * grp + 32 + lane] = EG[64 * grp + 32 + lane];
         }
-        tmem_st_wait();
+        if (c > 0) {
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
+                const float *eg = egc + ((c - 1) & 1) * 128 + 64 * grp + 32 * pass;
+                uint32_t y0[16], y1[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    y0[e] = __float_as_uint(v[e] * eg[e]);
+                    y1[e] = __float_as_uint(v[16 + e] * eg[16 + e]);
+                }
+                tmem_st16(tmem + lane_off + tSc + 32 * pass, y0);
+                tmem_st16(tmem + lane_off + tSc + 32 * pass + 16, y1);
+            }
+            tmem_st_wait();
+        }
 
         failed = !wait_bar(&bars[B_X], (uint32_t)(c & 1), x.flag, a, pc);
         if (bar_or(1, 256, failed)) { failed = true; break; }
@@ -1079,7 +1091,7 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         fence_before_sync();
         bar_named(1, 256);
 
-        // O^T += Vt^T Aqk^T;  S^T += Vt^T Kbar  (A: Vt^T bf16 in TMEM)
+        // O^T += Vt^T Aqk^T;  R += Vt^T Km  (A: Vt^T bf16 in TMEM)
         if (lead) {
             fence_after_sync();
             const uint32_t ido = idesc_bf16(128, 64, false, false, false);
@@ -1087,7 +1099,7 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 mma_ts(tmem + tX + 64, tmem + tV + 8 * s, dK(sbase + oB + Slot::oAQ, 8192, s), ido, 1);
-                mma_ts(tmem + tS, tmem + tV + 8 * s, dK(sbase + oB + Slot::oKB, 16384, s), ids, 1);
+                mma_ts(tmem + tS, tmem + tV + 8 * s, dK(sbase + oB + Slot::oKM, 16384, s), ids, 1);
             }
             commit(&bars[B_S2]);
         }
@@ -1096,14 +1108,25 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         fence_after_sync();
         if (lead) mbar_arrive(&bars[B_EMPTY0 + b]);  // buffer b consumed
 
-        // S^T -> bf16 operand for the next chunk
+        // S_{c+1}^T = R Diag(e^gamma_n) -> bf16 operand for the next chunk
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
+            // the factors first, so that their loads overlap the TMEM load's wait
+            float eg[32];
+            const float4 *eg4 = reinterpret_cast<const float4 *>(egc + (c & 1) * 128 + 64 * grp + 32 * pass);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 t4 = eg4[q];
+                eg[4 * q] = t4.x;
+                eg[4 * q + 1] = t4.y;
+                eg[4 * q + 2] = t4.z;
+                eg[4 * q + 3] = t4.w;
+            }
             float v[32];
             tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
             uint32_t p16[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) p16[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            for (int e = 0; e < 16; ++e) p16[e] = pack_bf16(v[2 * e] * eg[2 * e], v[2 * e + 1] * eg[2 * e + 1]);
             tmem_st16(tmem + lane_off + tSAc + 16 * pass, p16);
         }
         tmem_st_wait();
@@ -1118,13 +1141,16 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         write_o(nchunks - 1);
     }
     if (a.ht != nullptr) {
+        // S_N^T = R Diag(e^gamma_n of the last chunk) (R = h0^T when there is none)
         float *ht = a.ht + ((int64_t)n * a.H_v + h) * 128 * 128 + dv;
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
             float v[32];
             tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
+            const float *eg = egc + ((nchunks - 1) & 1) * 128 + 64 * grp + 32 * pass;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ht[(int64_t)(64 * grp + 32 * pass + e) * 128] = v[e];
+            for (int e = 0; e < 32; ++e)
+                ht[(int64_t)(64 * grp + 32 * pass + e) * 128] = nchunks > 0 ? v[e] * eg[e] : v[e];
         }
     }
 }
