@@ -474,34 +474,107 @@ __global__ void __launch_bounds__(kT, 2) bwd_prep_kernel(const BwdArgs a) {
     block_gemm<SPLIT>(64, K, 64, 1.f, Tsh, 65, 1, Kbeta, K, 1, S + L.wm, K, 1, false, stage);
 }
 
-// Copy n floats (a multiple of 4, both ends 16-byte aligned) global -> shared with cp.async,
-// all kT threads; `rows` rows of `cols` floats with the given global row stride.
-__device__ __forceinline__ void stage_rows(float *dst, const float *src, int rows, int cols, int64_t stride) {
+// Copy `rows` rows of `cols` floats (a multiple of 4; every row start 16-byte aligned)
+// global -> shared with cp.async, all kT threads; global row stride `stride`, shared row
+// stride `dstride`.
+__device__ __forceinline__ void stage_rows(float *dst, int dstride, const float *src, int rows, int cols,
+                                           int64_t stride) {
     const int per = cols / 4;
     for (int e = threadIdx.x; e < rows * per; e += kT) {
         const int r = e / per, c4 = e - r * per;
-        cp_async_16(dst + r * cols + 4 * c4, src + r * stride + 4 * c4, 16);
+        cp_async_16(dst + r * dstride + 4 * c4, src + r * stride + 4 * c4, 16);
     }
+}
+
+// The scans' operands stay in shared memory with padded rows, and their products read the
+// mma fragments from there directly (smem_gemm): no staging copy, no barrier per k step.
+// A fragment read touches 8 rows x 4 consecutive k (row stride = 4 mod 32 words: row_k)
+// when k runs along the rows, or 4 rows x 8 consecutive m or n (stride = 8 mod 32: row_m)
+// otherwise; either way 32 different banks.
+__host__ __device__ constexpr int row_k(int n) { return n + 4; }  // rows holding k
+__host__ __device__ constexpr int row_m(int n) { return n + 8; }  // rows holding m or n
+static_assert(row_k(64) % 32 == 4 && row_k(128) % 32 == 4, "k rows");
+static_assert(row_m(64) % 32 == 8 && row_m(128) % 32 == 8, "m rows");
+
+// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc) with A, B and C in shared
+// memory: A(m, k) = A[m * am + k * ak] and so on, M, N multiples of 64, K of 8, C apart
+// from A and B. The same mma.sync split and precision as block_gemm (SPLIT: 3xTF32, else
+// operands rounded to tf32); fragments are read in place. Called by all kT threads; ends
+// with a barrier.
+template <bool SPLIT>
+__device__ void smem_gemm(int M, int N, int K, float alpha, const float *A, int am, int ak, const float *B, int bk,
+                          int bn, float *C, int cm, int cn, bool acc) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int mb = (warp & 3) * 16, nb = (warp >> 2) * 16;
+    for (int m0 = 0; m0 < M; m0 += 64) {
+        for (int n0 = 0; n0 < N; n0 += 64) {
+            float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const float *Ab = A + (m0 + mb + g) * am + t * ak;
+            const float *Bb = B + t * bk + (n0 + nb + g) * bn;
+#pragma unroll 2
+            for (int k8 = 0; k8 < K; k8 += 8) {
+                const float *Af = Ab + k8 * ak;
+                const float a[4] = {Af[0], Af[8 * am], Af[4 * ak], Af[8 * am + 4 * ak]};
+                uint32_t ah[4], al[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (SPLIT) split_tf32(a[i], ah[i], al[i]);
+                    else ah[i] = to_tf32(a[i]);
+                }
+#pragma unroll
+                for (int f = 0; f < 2; ++f) {
+                    const float *Bf = Bb + k8 * bk + 8 * f * bn;
+                    const float b0 = Bf[0], b1 = Bf[4 * bk];
+                    if constexpr (SPLIT) {
+                        uint32_t bh0, bl0, bh1, bl1;
+                        split_tf32(b0, bh0, bl0);
+                        split_tf32(b1, bh1, bl1);
+                        mma_m16n8k8_tf32(c[f], al, bh0, bh1);
+                        mma_m16n8k8_tf32(c[f], ah, bl0, bl1);
+                        mma_m16n8k8_tf32(c[f], ah, bh0, bh1);
+                    } else {
+                        mma_m16n8k8_tf32(c[f], ah, to_tf32(b0), to_tf32(b1));
+                    }
+                }
+            }
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq)
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int j = (g + rr) & 3, f = j >> 1, qi = j & 1;
+                    const float v0 = qi ? c[0][2 * hq + 1] : c[0][2 * hq];
+                    const float v1 = qi ? c[1][2 * hq + 1] : c[1][2 * hq];
+                    const float v = f ? v1 : v0;
+                    const int m = m0 + mb + g + 8 * hq, n = n0 + nb + 8 * f + 2 * t + qi;
+                    float *p = C + m * cm + n * cn;
+                    *p = acc ? fmaf(alpha, v, *p) : alpha * v;
+                }
+        }
+    }
+    __syncthreads();
 }
 
 __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;\n" ::); }
 
 // ---- states: the forward scan, S slice [K][64 columns] in shared memory -----------------------
 // Per chunk the operands (W, Kb [64][K], U's 64 columns, e^Gn) are copied into shared memory,
-// so that the products read no global memory; two buffers, the next chunk's copy in flight
-// while the current chunk is computed.
+// two buffers, the next chunk's copy in flight while the current chunk is computed. Row
+// strides: S and U rs (m/n rows), W rw (k rows: W is A with k = d_k along its rows), Kb rkb
+// (Kb^T is A with m = d_k along the rows of Kb).
 size_t states_smem(int K) {
-    return sizeof(float) * ((size_t)K * 64 + 2 * ((size_t)K * 64 * 2 + 64 * 64 + K) + kStageFloats);
+    const size_t rs = row_m(64), rw = row_k(K), rkb = row_m(K);
+    return sizeof(float) * (K * rs + 2 * (64 * rw + 64 * rkb + 64 * rs + K));
 }
 
 template <bool SPLIT>
 __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
+    const int rs = row_m(64), rw = row_k(K), rkb = row_m(K);
     float *St = sm;                          // S [K][64]
-    float *buf = St + K * 64;                // two buffers of the chunk operands
-    const int bstride = K * 64 * 2 + 64 * 64 + K;
-    float *stage = buf + 2 * bstride;
+    float *buf = St + K * rs;                // two buffers of the chunk operands
+    const int bstride = 64 * rw + 64 * rkb + 64 * rs + K;
     const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const Lay L = make_lay(K, V);
     int64_t bos;
@@ -511,56 +584,61 @@ __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     // buffer b: W [64][K], Kb [64][K], U, then Vt [64][64], e^Gn [K]
     auto issue = [&](int c) {
         const float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
-        float *Ws = buf + (c & 1) * bstride, *Kbs = Ws + 64 * K, *Us = Kbs + 64 * K, *EGs = Us + 64 * 64;
-        stage_rows(Ws, S + L.wm, 64, K, K);
-        stage_rows(Kbs, S + L.kb, 64, K, K);
-        stage_rows(Us, S + L.u + j0, 64, 64, V);
-        stage_rows(EGs, S + L.eg, 1, K, K);
+        float *Ws = buf + (c & 1) * bstride, *Kbs = Ws + 64 * rw, *Us = Kbs + 64 * rkb, *EGs = Us + 64 * rs;
+        stage_rows(Ws, rw, S + L.wm, 64, K, K);
+        stage_rows(Kbs, rkb, S + L.kb, 64, K, K);
+        stage_rows(Us, rs, S + L.u + j0, 64, 64, V);
+        stage_rows(EGs, K, S + L.eg, 1, K, K);
         cp_async_commit();
     };
     if (nch > 0) issue(0);
     for (int e = tid; e < K * 64; e += kT) {
         const int i = e >> 6, j = e & 63;
-        St[e] = a.h0 ? a.h0[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
+        St[i * rs + j] = a.h0 ? a.h0[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
     }
     for (int c = 0; c < nch; ++c) {
         float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
-        float *Ws = buf + (c & 1) * bstride, *Kbs = Ws + 64 * K, *Us = Kbs + 64 * K, *EGs = Us + 64 * 64;
+        float *Ws = buf + (c & 1) * bstride, *Kbs = Ws + 64 * rw, *Us = Kbs + 64 * rkb, *EGs = Us + 64 * rs;
         cp_async_wait_all();
         __syncthreads();
         if (c + 1 < nch) issue(c + 1);  // into the buffer chunk c - 1 used
-        for (int e = tid; e < K * 64; e += kT) S[L.se + (int64_t)(e >> 6) * V + j0 + (e & 63)] = St[e];
+        for (int e = tid; e < K * 64; e += kT)
+            S[L.se + (int64_t)(e >> 6) * V + j0 + (e & 63)] = St[(e >> 6) * rs + (e & 63)];
         // Vt = U - W S (in U's place), stored for the gradient kernel
-        block_gemm<SPLIT>(64, 64, K, -1.f, Ws, K, 1, St, 64, 1, Us, 64, 1, true, stage);
-        for (int e = tid; e < 64 * 64; e += kT) S[L.vt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = Us[e];
+        smem_gemm<SPLIT>(64, 64, K, -1.f, Ws, rw, 1, St, rs, 1, Us, rs, 1, true);
+        for (int e = tid; e < 64 * 64; e += kT)
+            S[L.vt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = Us[(e >> 6) * rs + (e & 63)];
         // S <- diag(EG) S + Kb^T Vt
-        for (int e = tid; e < K * 64; e += kT) St[e] *= EGs[e >> 6];
+        for (int e = tid; e < K * 64; e += kT) St[(e >> 6) * rs + (e & 63)] *= EGs[e >> 6];
         __syncthreads();
-        block_gemm<SPLIT>(K, 64, 64, 1.f, Kbs, 1, K, Us, 64, 1, St, 64, 1, true, stage);
+        smem_gemm<SPLIT>(K, 64, 64, 1.f, Kbs, 1, rkb, Us, rs, 1, St, rs, 1, true);
     }
 }
 
 // ---- adjoint: the reverse scan, dS slice [K][64 columns] in shared memory -------------------
 // The chunk's operands are copied into shared memory in two sets: A, Kb, e^Gn and dO for the
 // first products, Qp and W for the second. Each set's buffer is refilled with the next chunk's
-// set as soon as the current chunk is done with it (dO, used by both, has two buffers).
+// set as soon as the current chunk is done with it (dO, used by both, has two buffers). Row
+// strides: dS, A, dO, dVt rs; Kb rkb (k rows); Qp, W rq (Qp^T and W^T are A with m = d_k
+// along their rows).
 size_t adjoint_smem(int K) {
-    return sizeof(float) * ((size_t)K * 64 * 4 + 4 * 64 * 64 + 2 * K + kStageFloats);
+    const size_t rs = row_m(64), rkb = row_k(K), rq = row_m(K);
+    return sizeof(float) * (K * rs + 64 * rkb + 2 * 64 * rq + 4 * 64 * rs + 2 * K);
 }
 
 template <bool SPLIT>
 __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int K = a.d_k, V = a.d_v, tid = threadIdx.x;
-    float *dS = sm;               // dS [K][64]
-    float *Kbs = dS + K * 64;     // Kb [64][K]
-    float *Qps = Kbs + 64 * K;    // Qp [64][K]
-    float *Ws = Qps + 64 * K;     // W [64][K]
-    float *As = Ws + 64 * K;      // A [64][64]
-    float *dOb = As + 64 * 64;    // dO's 64 columns [64][64], two buffers
-    float *dVs = dOb + 2 * 64 * 64;  // dVt [64][64]
-    float *EGb = dVs + 64 * 64;   // e^Gn [K], two buffers
-    float *stage = EGb + 2 * K;
+    const int rs = row_m(64), rkb = row_k(K), rq = row_m(K);
+    float *dS = sm;                  // dS [K][64]
+    float *Kbs = dS + K * rs;        // Kb [64][K]
+    float *Qps = Kbs + 64 * rkb;     // Qp [64][K]
+    float *Ws = Qps + 64 * rq;       // W [64][K]
+    float *As = Ws + 64 * rq;        // A [64][64]
+    float *dOb = As + 64 * rs;       // dO's 64 columns [64][64], two buffers
+    float *dVs = dOb + 2 * 64 * rs;  // dVt [64][64]
+    float *EGb = dVs + 64 * rs;      // e^Gn [K], two buffers
     const int j0 = blockIdx.x * 64, h = blockIdx.y, n = blockIdx.z;
     const Lay L = make_lay(K, V);
     int64_t bos;
@@ -570,16 +648,16 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     auto slot = [&](int c) { return a.scratch + slot_of(a, bos, n, c, h) * L.total; };
     auto issue_first = [&](int c) {
         const float *S = slot(c);
-        stage_rows(Kbs, S + L.kb, 64, K, K);
-        stage_rows(As, S + L.a, 64, 64, 64);
-        stage_rows(dOb + (c & 1) * 4096, S + L.dof + j0, 64, 64, V);
-        stage_rows(EGb + (c & 1) * K, S + L.eg, 1, K, K);
+        stage_rows(Kbs, rkb, S + L.kb, 64, K, K);
+        stage_rows(As, rs, S + L.a, 64, 64, 64);
+        stage_rows(dOb + (c & 1) * 64 * rs, rs, S + L.dof + j0, 64, 64, V);
+        stage_rows(EGb + (c & 1) * K, K, S + L.eg, 1, K, K);
         cp_async_commit();
     };
     auto issue_second = [&](int c) {
         const float *S = slot(c);
-        stage_rows(Qps, S + L.qp, 64, K, K);
-        stage_rows(Ws, S + L.wm, 64, K, K);
+        stage_rows(Qps, rq, S + L.qp, 64, K, K);
+        stage_rows(Ws, rq, S + L.wm, 64, K, K);
         cp_async_commit();
     };
     if (nch > 0) {
@@ -588,18 +666,19 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     }
     for (int e = tid; e < K * 64; e += kT) {
         const int i = e >> 6, j = e & 63;
-        dS[e] = a.dht ? a.dht[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
+        dS[i * rs + j] = a.dht ? a.dht[(((int64_t)n * a.H_v + h) * K + i) * V + j0 + j] : 0.f;
     }
     for (int c = nch - 1; c >= 0; --c) {
         float *S = slot(c);
-        float *dOs = dOb + (c & 1) * 4096, *EGs = EGb + (c & 1) * K;
+        float *dOs = dOb + (c & 1) * 64 * rs, *EGs = EGb + (c & 1) * K;
         // the groups in flight are this chunk's two sets, oldest first
         cp_async_wait_one();
         __syncthreads();
-        for (int e = tid; e < K * 64; e += kT) S[L.dsx + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dS[e];
+        for (int e = tid; e < K * 64; e += kT)
+            S[L.dsx + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dS[(e >> 6) * rs + (e & 63)];
         // dVt = A^T dO + Kb dS', stored for the gradient kernel
-        block_gemm<SPLIT>(64, 64, 64, 1.f, As, 1, 64, dOs, 64, 1, dVs, 64, 1, false, stage);
-        block_gemm<SPLIT>(64, 64, K, 1.f, Kbs, K, 1, dS, 64, 1, dVs, 64, 1, true, stage);
+        smem_gemm<SPLIT>(64, 64, 64, 1.f, As, 1, rs, dOs, rs, 1, dVs, rs, 1, false);
+        smem_gemm<SPLIT>(64, 64, K, 1.f, Kbs, rkb, 1, dS, rs, 1, dVs, rs, 1, true);
         // A and Kb are consumed: the previous chunk's first set (its dO into the other buffer)
         if (c > 0) {
             issue_first(c - 1);
@@ -607,17 +686,18 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
         } else {
             cp_async_wait_all();
         }
-        for (int e = tid; e < 64 * 64; e += kT) S[L.dvt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dVs[e];
+        for (int e = tid; e < 64 * 64; e += kT)
+            S[L.dvt + (int64_t)(e >> 6) * V + j0 + (e & 63)] = dVs[(e >> 6) * rs + (e & 63)];
         // dS <- diag(EG) dS' + Qp^T dO - W^T dVt
-        for (int e = tid; e < K * 64; e += kT) dS[e] *= EGs[e >> 6];
+        for (int e = tid; e < K * 64; e += kT) dS[(e >> 6) * rs + (e & 63)] *= EGs[e >> 6];
         __syncthreads();
-        block_gemm<SPLIT>(K, 64, 64, 1.f, Qps, 1, K, dOs, 64, 1, dS, 64, 1, true, stage);
-        block_gemm<SPLIT>(K, 64, 64, -1.f, Ws, 1, K, dVs, 64, 1, dS, 64, 1, true, stage);
+        smem_gemm<SPLIT>(K, 64, 64, 1.f, Qps, 1, rq, dOs, rs, 1, dS, rs, 1, true);
+        smem_gemm<SPLIT>(K, 64, 64, -1.f, Ws, 1, rq, dVs, rs, 1, dS, rs, 1, true);
         if (c > 0) issue_second(c - 1);  // Qp and W are consumed
     }
     if (a.dh0 != nullptr)
         for (int e = tid; e < K * 64; e += kT)
-            a.dh0[(((int64_t)n * a.H_v + h) * K + (e >> 6)) * V + j0 + (e & 63)] = dS[e];
+            a.dh0[(((int64_t)n * a.H_v + h) * K + (e >> 6)) * V + j0 + (e & 63)] = dS[(e >> 6) * rs + (e & 63)];
 }
 
 // ---- grads: every gradient of one chunk ---------------------------------------------------------
