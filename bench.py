@@ -334,7 +334,7 @@ def run_ours(args, world, rank, local, pg):
     cu = torch.from_numpy(x.cu_seqlens.astype(np.int32)).to(dev) if x.varlen else None
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
-    north_star = args.entry == "chunk" and x.dtype == "bf16" and x.gate == "channel" and not fe_on
+    plain_call = args.entry == "chunk" and x.dtype == "bf16" and x.gate == "channel" and not fe_on
 
     def make_call(Ds):
         """One library call on the device buffers Ds, on `stream`."""
@@ -348,12 +348,12 @@ def run_ours(args, world, rank, local, pg):
         fe = kda.kda_frontend(1, 1 if x.beta is not None else 0, ptr("A_log"), ptr("dt_bias")) if fe_on else None
 
         def call():
-            # kda_chunk_fwd (the spec symbol) when the workload fits its argument list,
-            # else the struct entry points of the same ABI
+            # kda_chunk_fwd (the plain argument-list entry point) when the workload fits its
+            # argument list, else the struct entry points of the same ABI
             if fe_on:
                 fn = lib.kda_recurrent_fwd_fused if args.entry == "recurrent" else lib.kda_chunk_fwd_fused
                 st = fn(ctypes.byref(params), ctypes.byref(fe), sh)
-            elif north_star:
+            elif plain_call:
                 st = lib.kda_chunk_fwd(ptr("q"), ptr("k"), ptr("v"), ptr("g"), ptr("beta"), ptr("h0"), ptr("o"),
                                        ptr("ht"), B, T, x.H_k, x.H_v, x.d_k, x.d_v, 64, x.scale,
                                        None if cu is None else cu.data_ptr(), sh)
