@@ -21,6 +21,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -43,12 +44,13 @@ def metric_name(entry: str, workload: str) -> str:
     return f"{what} tokens/s on {workload}"
 
 # DRAM traffic per launch of the forward kernel, from an ncu capture of this workload
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of the sources of the
-# kernel it was taken on; any change to them makes the figure stale (reported as null).
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by a hash of the code of the kernel
+# it was taken on (comments ignored); any change to the code makes the figure stale
+# (reported as null).
 MEASURED_TRAFFIC = {
     # profiles/kda_fwd_pc_b2_t8192_h32_d128.md: 504.5 MB on the same 64 units over half the
     # tokens (B=2, T=4096), scaled by 2 to this workload
-    ("kda_b2_t8192_h32_d128_bf16", "7dd12545e7b41260"): 1_009_000_000,
+    ("kda_b2_t8192_h32_d128_bf16", "be6633b5bbca160c"): 1_009_000_000,
 }
 
 # The translation unit of each forward kernel and the headers it includes.
@@ -61,12 +63,22 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and with whitespace collapsed (string and character
+    literals kept as they are), so that edits to comments leave the hash unchanged."""
+    tok = re.compile(r'"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|//[^\n]*|/\*.*?\*/', re.S)
+    text = tok.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str = "kda_fwd_pc_kernel") -> str:
+    """Hash of the code (comments and layout ignored) of a kernel's translation unit and
+    the headers it includes."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "chunkwise_gated_linear_gb300", "csrc", name), "rb") as f:
+        with open(os.path.join(ROOT, "chunkwise_gated_linear_gb300", "csrc", name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,7 +18,8 @@
 //        in the consumer's 128-byte swizzled shared-memory image), U^T (bf16), e^gamma_n.
 //   consumer CTA (unit u), TMEM holds R [d_v x d_k] fp32 with S_c^T = R Diag(e^gamma_n of
 //   chunk c - 1), thread = d_v row (Kbar = Km Diag(e^gamma_n) is never formed):
-//     one bulk copy per chunk brings the slot into shared memory (double-buffered), then
+//     bulk copies bring each slot into shared memory (three buffers, up to three chunks
+//     ahead of the serial step), then
 //     D_X = S_c^T [W^T | Qp^T] (A: the bf16 copy of S_c^T);  R <- R Diag(e^gamma_n, c - 1);
 //     Vt^T = U^T - D_X[:, :64];  O^T = D_X[:, 64:] + Vt^T Aqk^T;  R += Vt^T Km;
 //     bf16 copy of S_{c+1}^T = R Diag(e^gamma_n, c).
@@ -26,8 +27,8 @@
 // Hand-offs through global memory use per-slot sequence numbers: a producer publishes
 // chunk c of unit u by a release store of c + 1 into ready[u][c % R] after its writes;
 // the consumer releases the slot by storing c + 1 into done[u] once the bulk copy has
-// landed. Producers take jobs in (chunk, unit) order, so the oldest unfinished job
-// never waits on a later one. The launch is cooperative (every CTA resident). Every
+// landed. Producers take jobs in (chunk, unit) order (claimed from a global counter when
+// the units have equal lengths), so the oldest unfinished job never waits on a later one. The launch is cooperative (every CTA resident). Every
 // wait is bounded (about one second) and watches a global abort word, so a failure
 // anywhere ends all CTAs with KDA_DEVICE_ERR_TIMEOUT.
 #include <algorithm>
