@@ -81,3 +81,15 @@ def test_workload_accounting_and_dispatch():
     assert bench.forward_kernel(x, 120) == "kda_fwd_tc_kernel"  # more than half the SMs
     y = workload_inputs("kda_b1_t256_h1_d64_f32")
     assert bench.forward_kernel(y, 152) == "kda_fwd_f32_kernel"
+
+
+def test_kernel_hash_ignores_comments_and_layout_only():
+    """The measured-traffic key follows the code: comments and whitespace do not change it,
+    string and character literals and code do."""
+    code = 'int f(int a) {\n    return a + 1;  // one\n}\n/* block\n comment */ const char *s = "x // y";\n'
+    same = 'int f(int a) { return a + 1; }\n// other comment\nconst char *s = "x // y";'
+    assert bench._code_only(code) == bench._code_only(same)
+    assert bench._code_only(code) != bench._code_only(code.replace("a + 1", "a + 2"))
+    assert bench._code_only(code) != bench._code_only(code.replace('"x // y"', '"x /* y"'))
+    assert "'/'" in bench._code_only("char c = '/'; // slash")
+    assert len(bench.kernel_source_hash("kda_fwd_pc_kernel")) == 16
