@@ -9,8 +9,8 @@
 //
 //   producer CTA, one chunk job after another, two stages working on consecutive jobs:
 //     front (warps 0-7)   TMA Q, K, G; gamma = chunk-local cumulative log2 gate;
-//                         Qp = scale Q e^gamma, Kp = K e^gamma, Km = K e^-gamma
-//                         (transposed, bf16);
+//                         Qp = Q e^gamma, Kp = K e^gamma, Km = K e^-gamma
+//                         (transposed, bf16; the scale is applied to the output);
 //                         Gram D_G = [Qp; Kp] Km^T -> Aqk (lower), L = diag(beta) M (strict)
 //     back  (warps 8-15)  T = (I + L)^-1 (16x16 diagonal blocks by substitution, the rest
 //                         on tf32 mma.sync); D_W = Kp^T (T diag beta)^T, D_U = V^T (T diag beta)^T
@@ -89,7 +89,7 @@ struct Prod {
     static constexpr int oGh1 = 217088;
     static constexpr int oTot = 217344;    // [4][128] fp32 partial gate sums
     static constexpr int oPS = 219392;     // solve scratch, 8 warps x 16x8 fp32
-    static constexpr int oRN = oPS + 4096; // front-end: scale / |q_t| [64], 1 / |k_t| [64]
+    static constexpr int oRN = oPS + 4096; // front-end: 1 / |q_t| [64], 1 / |k_t| [64]
     static constexpr int kEnd = oRN + 512;
 };
 static_assert(Prod::oEG + 512 <= Prod::oKP0, "image overlaps");
@@ -182,53 +182,106 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_done() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// Product of two bf16 pairs, rounded to the nearest bf16 pair.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t x, uint32_t y) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(y));
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(y), "r"(sel));
+    return d;
+}
+// x[e] holds (channel ch, channel ch + 1) of token 8 tc + e; rows ra and rb (ch and ch + 1,
+// in either order) of a [d][tok] 128-byte swizzled tile receive the eight tokens as 16 bytes
+// each: selector 0x5410 gathers the low halves of a token pair, 0x7632 the high halves.
+__device__ __forceinline__ void store_pairs_t(unsigned char *tile, const uint32_t (&x)[8], int ra, int rb, int tc,
+                                              uint32_t sel_a, uint32_t sel_b) {
+    uint4 A, B;
+    A.x = prmt(x[0], x[1], sel_a);
+    A.y = prmt(x[2], x[3], sel_a);
+    A.z = prmt(x[4], x[5], sel_a);
+    A.w = prmt(x[6], x[7], sel_a);
+    B.x = prmt(x[0], x[1], sel_b);
+    B.y = prmt(x[2], x[3], sel_b);
+    B.z = prmt(x[4], x[5], sel_b);
+    B.w = prmt(x[6], x[7], sel_b);
+    *reinterpret_cast<uint4 *>(tile + sw128(ra, tc)) = A;
+    *reinterpret_cast<uint4 *>(tile + sw128(rb, tc)) = B;
+}
+
 // Raise the abort word (once) and the device error bit.
-__device__ __forceinline__ void raise_abort(const FwdArgs &a, const PcArgs &pc, volatile int *cta_flag) {
+__device__ __forceinline__ void raise_abort_w(int *abort_w, unsigned int *err, volatile int *cta_flag) {
     *cta_flag = 1;
-    if (atomicExch(pc.abort, 1) == 0) atomicOr(a.err, kDeviceErrTimeout);
+    if (atomicExch(abort_w, 1) == 0) atomicOr(err, kDeviceErrTimeout);
+}
+// mbarrier phase test that lets the hardware suspend the thread until the phase completes
+// (or about `hint_ns` nanoseconds have passed), so that waiting threads take no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// The waits below keep their slow paths out of line: one copy of each loop serves every
+// call site, which keeps the kernel's hot code small.
+__device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *cta_flag, int *abort_w,
+                                           unsigned int *err) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (*cta_flag) return false;
+        if (*(volatile int *)abort_w) {
+            *cta_flag = 1;
+            return false;
+        }
+        if (clock64() - t0 > kWaitCycles) {
+            raise_abort_w(abort_w, err, cta_flag);
+            return false;
+        }
+    }
+    return true;
 }
 // Bounded wait on an mbarrier phase of this CTA; gives up when this CTA or any other is
 // aborting.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *cta_flag, const FwdArgs &a,
                                          const PcArgs &pc) {
     if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    int spins = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if (*cta_flag) return false;
-        if ((++spins & 63) == 0 && *(volatile int *)pc.abort) {
-            *cta_flag = 1;
-            return false;
-        }
-        if (clock64() - t0 > kWaitCycles) {
-            raise_abort(a, pc, cta_flag);
-            return false;
-        }
-    }
-    return true;
+    return wait_bar_slow(bar, parity, cta_flag, pc.abort, a.err);
 }
-// Bounded wait until the global word *p reaches at least `target` (acquire); the value
-// read last goes to *seen.
-__device__ __forceinline__ bool wait_geq(const int *p, int target, volatile int *cta_flag, const FwdArgs &a,
-                                         const PcArgs &pc, int *seen = nullptr) {
-    int v = ld_acquire(p);
-    if (seen) *seen = v;
-    if (v >= target) return true;
+__device__ __noinline__ bool wait_geq_slow(const int *p, int target, volatile int *cta_flag, int *abort_w,
+                                           unsigned int *err, int *seen) {
     const long long t0 = clock64();
+    int v;
     while ((v = ld_acquire(p)) < target) {
         if (*cta_flag) return false;
-        if (*(volatile int *)pc.abort) {
+        if (*(volatile int *)abort_w) {
             *cta_flag = 1;
             return false;
         }
         if (clock64() - t0 > kWaitCycles) {
-            raise_abort(a, pc, cta_flag);
+            raise_abort_w(abort_w, err, cta_flag);
             return false;
         }
         __nanosleep(64);
     }
     if (seen) *seen = v;
     return true;
+}
+// Bounded wait until the global word *p reaches at least `target` (acquire); the value
+// read last goes to *seen.
+__device__ __forceinline__ bool wait_geq(const int *p, int target, volatile int *cta_flag, const FwdArgs &a,
+                                         const PcArgs &pc, int *seen = nullptr) {
+    const int v = ld_acquire(p);
+    if (seen) *seen = v;
+    if (v >= target) return true;
+    return wait_geq_slow(p, target, cta_flag, pc.abort, a.err, seen);
 }
 
 // Per-CTA context shared by the roles.
@@ -246,21 +299,27 @@ struct Ctx {
 };
 
 // Bounded wait until the shared-memory counter *p reaches at least `target`.
-__device__ __forceinline__ bool wait_count(const volatile int *p, int target, volatile int *cta_flag,
-                                           const FwdArgs &a, const PcArgs &pc) {
+__device__ __noinline__ bool wait_count_slow(const volatile int *p, int target, volatile int *cta_flag, int *abort_w,
+                                             unsigned int *err) {
     const long long t0 = clock64();
     while (*p < target) {
         if (*cta_flag) return false;
-        if (*(volatile int *)pc.abort) {
+        if (*(volatile int *)abort_w) {
             *cta_flag = 1;
             return false;
         }
         if (clock64() - t0 > kWaitCycles) {
-            raise_abort(a, pc, cta_flag);
+            raise_abort_w(abort_w, err, cta_flag);
             return false;
         }
+        __nanosleep(32);
     }
     return true;
+}
+__device__ __forceinline__ bool wait_count(const volatile int *p, int target, volatile int *cta_flag,
+                                           const FwdArgs &a, const PcArgs &pc) {
+    if (*p >= target) return true;
+    return wait_count_slow(p, target, cta_flag, pc.abort, a.err);
 }
 
 // The jobs of producer p: the (chunk c, unit u) pairs with c < nch[u], ordered by c then
@@ -408,9 +467,9 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
                     if constexpr (GATE_HEAD) {
                         bias0 = a.fe_dt_bias[h];
                     } else {
-                        const int cb = 64 * (pw & 1) + lane;
+                        const int cb = 64 * (pw & 1) + 2 * lane;
                         bias0 = a.fe_dt_bias[h * 128 + cb];
-                        bias1 = a.fe_dt_bias[h * 128 + cb + 32];
+                        bias1 = a.fe_dt_bias[h * 128 + cb + 1];
                     }
                 }
             }
@@ -438,9 +497,10 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         }
 
         // ---- gate pass ---------------------------------------------------------------------
-        // warp pw: rows 16 (pw >> 1) .. +15, channels c0 = 64 (pw & 1) + lane and c0 + 32.
+        // thread: rows 16 qr .. 16 qr + 15 (qr = pw >> 1) of the channel pair c0, c0 + 1,
+        // c0 = 64 (pw & 1) + 2 lane; gl0 / gl1 hold the two channels' running log2 sums.
         const int qr = pw >> 1;
-        const int c0 = 64 * (pw & 1) + lane, c1 = c0 + 32;
+        const int c0 = 64 * (pw & 1) + 2 * lane;
         float gl0[16], gl1[16];
         bool gate_done = false;
         if constexpr (!GATE_HEAD && FE) {
@@ -450,8 +510,9 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int r = 16 * qr + e;
-                    const float v0 = nAl * softplus_fast(G[r * 128 + c0] + bias0);
-                    const float v1 = nAl * softplus_fast(G[r * 128 + c1] + bias1);
+                    const float2 gv = *reinterpret_cast<const float2 *>(G + r * 128 + c0);
+                    const float v0 = nAl * softplus_fast(gv.x + bias0);
+                    const float v1 = nAl * softplus_fast(gv.y + bias1);
                     gl0[e] = r < nvalid ? v0 : 0.f;
                     gl1[e] = r < nvalid ? v1 : 0.f;
                 }
@@ -460,8 +521,6 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
                     gl0[e] += gl0[e - 1];
                     gl1[e] += gl1[e - 1];
                 }
-                Tot[qr * 128 + c0] = gl0[15];
-                Tot[qr * 128 + c1] = gl1[15];
                 gate_done = true;
             }
         }
@@ -471,19 +530,18 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             for (int e = 0; e < 16; ++e) {
                 const int r = 16 * qr + e;
                 if constexpr (!GATE_HEAD) {
-                    acc0 += G[r * 128 + c0] * kLog2e;
-                    acc1 += G[r * 128 + c1] * kLog2e;
+                    const float2 gv = *reinterpret_cast<const float2 *>(G + r * 128 + c0);
+                    acc0 += gv.x * kLog2e;
+                    acc1 += gv.y * kLog2e;
                 } else {
-                    const float gr = Gh[r] * kLog2e;
-                    acc0 += gr;
-                    acc1 += gr;
+                    acc0 += Gh[r] * kLog2e;
+                    acc1 = acc0;
                 }
                 gl0[e] = acc0;
                 gl1[e] = acc1;
             }
-            Tot[qr * 128 + c0] = acc0;
-            Tot[qr * 128 + c1] = acc1;
         }
+        *reinterpret_cast<float2 *>(Tot + qr * 128 + c0) = make_float2(gl0[15], gl1[15]);
         // G (and the per-head gates) are consumed: request the next job's right away
         bar_named(1, 256);
         if (have_next) stage_g(nx, jo + 1);
@@ -514,7 +572,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         }
         if constexpr (FE) {
             if (a.fe_qk_l2norm) {
-                qk_row_norms(sm + Prod::oRQ, sm + Prod::oRK, reinterpret_cast<float *>(sm + Prod::oRN), pw, lane, a.scale);
+                qk_row_norms(sm + Prod::oRQ, sm + Prod::oRK, reinterpret_cast<float *>(sm + Prod::oRN), pw, lane, 1.f);
                 bar_named(1, 256);
             }
         }
@@ -522,62 +580,60 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             float off0 = 0.f, off1 = 0.f, gn0 = 0.f, gn1 = 0.f;
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
-                const float t0 = Tot[qq * 128 + c0], t1 = Tot[qq * 128 + c1];
+                const float2 t = *reinterpret_cast<const float2 *>(Tot + qq * 128 + c0);
                 if (qq < qr) {
-                    off0 += t0;
-                    off1 += t1;
+                    off0 += t.x;
+                    off1 += t.y;
                 }
-                gn0 += t0;
-                gn1 += t1;
+                gn0 += t.x;
+                gn1 += t.y;
             }
-            const float eg0 = ex2(gn0), eg1 = ex2(gn1);
-            if (qr == 0) {
-                EG[c0] = eg0;
-                EG[c1] = eg1;
-            }
+            if (qr == 0) *reinterpret_cast<float2 *>(EG + c0) = make_float2(ex2(gn0), ex2(gn1));
+            // The products are taken on bf16 pairs of the two channels of one token (the factor
+            // e^{+-gamma} rounded to bf16 first), then each 2 x 2 block of (token, channel) is
+            // transposed by byte permutes into the [d][tok] rows. Lanes whose (lane >> 2) is odd
+            // store the odd channel's row first, so that each 16-byte store spans all eight
+            // swizzle phases of its rows.
+            const bool odd_first = (lane >> 2) & 1;
+            const uint32_t sel_a = odd_first ? 0x7632u : 0x5410u, sel_b = odd_first ? 0x5410u : 0x7632u;
+            const int ra = c0 + (odd_first ? 1 : 0), rb = c0 + (odd_first ? 0 : 1);
+            const float *RN = reinterpret_cast<const float *>(sm + Prod::oRN);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int tc = 2 * qr + j;  // 16-byte chunk (8 tokens) of a 64-token row
-                // front-end: the factors of these 8 rows (q: scale / |q|, k: 1 / |k|)
-                float fq[8], fk[8];
-                if constexpr (FE) {
-                    const bool nrm = a.fe_qk_l2norm != 0;
-                    const float4 *RN4 = reinterpret_cast<const float4 *>(sm + Prod::oRN) + 4 * qr + 2 * j;
-                    const float4 q0 = nrm ? RN4[0] : make_float4(a.scale, a.scale, a.scale, a.scale);
-                    const float4 q1 = nrm ? RN4[1] : q0;
-                    const float4 k0 = nrm ? RN4[16] : make_float4(1.f, 1.f, 1.f, 1.f);
-                    const float4 k1 = nrm ? RN4[17] : k0;
-                    fq[0] = q0.x; fq[1] = q0.y; fq[2] = q0.z; fq[3] = q0.w;
-                    fq[4] = q1.x; fq[5] = q1.y; fq[6] = q1.z; fq[7] = q1.w;
-                    fk[0] = k0.x; fk[1] = k0.y; fk[2] = k0.z; fk[3] = k0.w;
-                    fk[4] = k1.x; fk[5] = k1.y; fk[6] = k1.z; fk[7] = k1.w;
-                }
+                uint32_t qp2[8], kp2[8], km2[8];
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    const int cc = ch ? c1 : c0;
-                    const float off = ch ? off1 : off0;
-                    float kp[8], km[8], qp[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int r = 16 * qr + 8 * j + e;
-                        const float gm = off + (ch ? gl1[8 * j + e] : gl0[8 * j + e]);
-                        const float ep = ex2(gm), em = ex2(-gm);
-                        float kv = __bfloat162float(RK[r * 128 + cc]);
-                        const float qv = __bfloat162float(RQ[r * 128 + cc]);
-                        float qs = a.scale;
-                        if constexpr (FE) {
-                            qs = fq[e];
-                            kv *= fk[e];
-                        }
-                        kp[e] = a.decay_only ? 0.f : kv * ep;
-                        km[e] = kv * em;
-                        qp[e] = qs * qv * ep;
+                for (int e = 0; e < 8; ++e) {
+                    const int r = 16 * qr + 8 * j + e;
+                    const float gm0 = off0 + gl0[8 * j + e];
+                    const float ep0 = ex2(gm0), em0 = ex2(-gm0);
+                    float ep1 = ep0, em1 = em0;
+                    if constexpr (!GATE_HEAD) {
+                        const float gm1 = off1 + gl1[8 * j + e];
+                        ep1 = ex2(gm1);
+                        em1 = ex2(-gm1);
                     }
-                    const uint32_t sw = sw128(cc, tc);
-                    *reinterpret_cast<uint4 *>(sm + Prod::oQP + sw) = pack8(qp);
-                    *reinterpret_cast<uint4 *>(sm + oKP + sw) = pack8(kp);
-                    *reinterpret_cast<uint4 *>(sm + Prod::oKM + sw) = pack8(km);
+                    const uint32_t q2 = *reinterpret_cast<const uint32_t *>(RQ + r * 128 + c0);
+                    const uint32_t k2 = *reinterpret_cast<const uint32_t *>(RK + r * 128 + c0);
+                    uint32_t epq, epk, emk;
+                    if constexpr (FE) {
+                        // front-end: the row factors 1 / |q_r| and 1 / |k_r| (or 1)
+                        const bool nrm = a.fe_qk_l2norm != 0;
+                        const float fq = nrm ? RN[r] : 1.f, fk = nrm ? RN[64 + r] : 1.f;
+                        epq = pack_bf16(ep0 * fq, ep1 * fq);
+                        epk = pack_bf16(ep0 * fk, ep1 * fk);
+                        emk = pack_bf16(em0 * fk, em1 * fk);
+                    } else {
+                        epq = epk = pack_bf16(ep0, ep1);
+                        emk = pack_bf16(em0, em1);
+                    }
+                    qp2[e] = mul_bf16x2(q2, epq);
+                    kp2[e] = a.decay_only ? 0u : mul_bf16x2(k2, epk);
+                    km2[e] = mul_bf16x2(k2, emk);
                 }
+                store_pairs_t(sm + Prod::oQP, qp2, ra, rb, tc, sel_a, sel_b);
+                store_pairs_t(sm + oKP, kp2, ra, rb, tc, sel_a, sel_b);
+                store_pairs_t(sm + Prod::oKM, km2, ra, rb, tc, sel_a, sel_b);
             }
         }
         fence_proxy_async();
@@ -1021,7 +1077,7 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         bf16 *op = o + (bos + row0o + 32 * grp) * sv + (int64_t)h * 128 + dv;
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-            if (32 * grp + e < nvalido) op[(int64_t)e * sv] = __float2bfloat16_rn(v[e]);
+            if (32 * grp + e < nvalido) op[(int64_t)e * sv] = __float2bfloat16_rn(v[e] * a.scale);
     };
 
     bool failed = false;
