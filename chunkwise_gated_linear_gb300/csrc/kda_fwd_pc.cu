@@ -132,7 +132,8 @@ enum {
     // consumer
     B_FULL0, B_FULL1, B_FULL2,     // slot image in buffer 0 / 1 / 2 landed
     B_EMPTY0, B_EMPTY1, B_EMPTY2,  // buffer 0 / 1 / 2 consumed by the serial step
-    B_X, B_S2,               // serial products
+    B_X, B_R, B_O,           // consumer products: D_X, the state update, the output
+    B_XFREE0, B_XFREE1,      // the output half of D_X buffer 0 / 1 has been read out
     B_CZ,
     kNumBars
 };
@@ -981,23 +982,24 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
 }
 
 // ---------------------------------------------------------------------------------------
-// consumer, loader (warps 4-7): slot images of unit u into the three shared buffers, each
-// as four bulk copies from four warps (so that they overlap); up to three in flight. A
+// consumer, loader (warps 4-6): slot images of unit u into the three shared buffers, each
+// as three bulk copies from three warps (so that they overlap); up to three in flight. A
 // ring slot is released when its buffer comes round again. Returns, for thread 128, the
 // copies that may still be in flight: bit b for buffer b, bit 4 + b its phase parity.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &pc, const Ctx &x, int u, int nch) {
     uint64_t *bars = x.bars;
     const int lt = threadIdx.x - 128, lw = lt >> 5, lane = lt & 31;
-    constexpr uint32_t kPart = Slot::kBytes / 4;
-    static_assert(Slot::kBytes % 64 == 0, "four 16-byte aligned parts");
+    static_assert(Slot::kBytes % 16 == 0, "16-byte parts");
+    constexpr uint32_t kPart = ((Slot::kBytes / 16 + 2) / 3) * 16;  // parts 0, 1; part 2 is the rest
+    const uint32_t off = lw * kPart, bytes = lw < 2 ? kPart : Slot::kBytes - 2 * kPart;
     int pend = 0;
     bool failed = false;
     for (int c = 0; c < nch; ++c) {
         const int b = c % Cons::kBufs, k = c / Cons::kBufs;  // buffer and its use count
         if (lt == 0 && !failed) {
-            // buffer b held chunk c - 3 until the serial step released it; that copy has
-            // long landed, so the ring slot of chunk c - 3 is free for the producers
+            // buffer b held chunk c - 3 until its output left; that copy has long landed, so
+            // the ring slot of chunk c - 3 is free for the producers
             if (c >= Cons::kBufs) {
                 failed = !wait_bar(&bars[B_EMPTY0 + b], (uint32_t)((k - 1) & 1), x.flag, a, pc);
                 if (!failed) st_release(&pc.done[u], c - Cons::kBufs + 1);
@@ -1005,17 +1007,30 @@ __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &p
             if (!failed) failed = !wait_geq(&pc.ready[u * pc.R + c % pc.R], c + 1, x.flag, a, pc);
             if (!failed) mbar_arrive_expect_tx(&bars[B_FULL0 + b], Slot::kBytes);
         }
-        if (bar_or(2, 128, failed)) {
+        if (bar_or(2, 96, failed)) {
             failed = true;
             break;
         }
         if (lane == 0) {
             fence_proxy_async_global();  // the producers' generic writes, before the async-proxy read
-            bulk_load(x.sm + b * Slot::kStride + lw * kPart, slot_ptr(pc, u, c) + lw * kPart, kPart, &bars[B_FULL0 + b]);
+            bulk_load(x.sm + b * Slot::kStride + off, slot_ptr(pc, u, c) + off, bytes, &bars[B_FULL0 + b]);
         }
         pend = (pend & ~(0x11 << b)) | ((1 | ((k & 1) << 4)) << b);
     }
     return lt == 0 ? pend : 0;
+}
+
+// ---------------------------------------------------------------------------------------
+// consumer: the MMAs of the serial step are issued by warp 7 (lane 0), which waits for the
+// element warps at named barrier kBarIss; the element warps arrive there without waiting
+// (bar.arrive), once when the bf16 copy of the state S_c^T is in TMEM and once when
+// Vt^T is. Every exit of the element warps on a failure arrives once more, so that the
+// issuer never waits for arrivals that will not come.
+// ---------------------------------------------------------------------------------------
+constexpr int kBarIss = 1, kIssCount = 288;  // warps 0-3, 8-11 arrive; warp 7 waits
+
+__device__ __forceinline__ void bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1025,18 +1040,14 @@ __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &p
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &pc, const Ctx &x, int u) {
     unsigned char *sm = x.sm;
-    const uint32_t sbase = x.sbase, tmem = x.tmem;
+    const uint32_t tmem = x.tmem;
     uint64_t *bars = x.bars;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = warp >> 3;                 // column half
-    const int dv = 32 * (warp & 3) + lane;     // row of S^T and of O^T
-    const bool lead = threadIdx.x == 0;        // issues the MMAs
+    const int dv = 32 * (warp & 3) + lane;     // row of S^T
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const int n = u / a.H_v, h = u % a.H_v;
-    const int len = x.units[u].len, nchunks = x.units[u].nch;
-    const int64_t bos = x.units[u].bos;
-    const int64_t sv = (int64_t)a.H_v * 128;
-    bf16 *o = static_cast<bf16 *>(a.o);
+    const int nchunks = x.units[u].nch;
     const uint32_t tSc = tS + 64 * grp, tSAc = tSA + 32 * grp;  // this thread's columns
     // e^gamma_n of the chunks by parity: the slot buffer is released before the state's bf16
     // copy (and the next chunk's rescale) would read it
@@ -1064,26 +1075,10 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
     }
     tmem_st_wait();
     fence_before_sync();
-    bar_named(1, 256);
-
-    // O^T of chunk cc, row dv, tokens 32 grp .. +31 -> o[token][dv] (valid tokens only;
-    // a warp writes 64 contiguous bytes per token). Runs while the next chunk's first MMA
-    // does.
-    auto write_o = [&](int cc) {
-        const int row0o = cc * kChunk;
-        const int nvalido = min(kChunk, len - row0o);
-        float v[32];
-        tmem_ld32(tmem + lane_off + ((cc & 1) ? tX1 : tX0) + 64 + 32 * grp, v);
-        bf16 *op = o + (bos + row0o + 32 * grp) * sv + (int64_t)h * 128 + dv;
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-            if (32 * grp + e < nvalido) op[(int64_t)e * sv] = __float2bfloat16_rn(v[e] * a.scale);
-    };
+    if (nchunks > 0) bar_arrive(kBarIss, kIssCount);  // S_0^T is in TMEM
 
     bool failed = false;
     for (int c = 0; c < nchunks; ++c) {
-        const int row0 = c * kChunk;
-        const int nvalid = min(kChunk, len - row0);
         const int b = c % Cons::kBufs;  // slot buffer; the TMEM buffers go by c & 1
         const uint32_t oB = b * Slot::kStride;
         const float *EG = reinterpret_cast<const float *>(sm + oB + Slot::oEG);
@@ -1091,26 +1086,15 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         const uint32_t tX = (c & 1) ? tX1 : tX0;
 
         failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c / Cons::kBufs) & 1), x.flag, a, pc);
-        if (bar_or(1, 256, failed)) { failed = true; break; }
-        fence_after_sync();
-
-        // D_X = S^T [W^T | Qp^T]  (A: S^T bf16 in TMEM; B: the W^T and Qp^T tiles, MN-major)
-        if (lead) {
-            const uint32_t id = idesc_bf16(128, 128, false, true, false);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_ts(tmem + tX, tmem + tSA + 8 * s, dMN(sbase + oB + Slot::oWT, Slot::oQP - Slot::oWT, s), id,
-                       s > 0);
-            commit(&bars[B_X]);
-        }
-        // meanwhile the previous chunk's output leaves, this chunk's e^gamma_n is kept, and
+        if (bar_or(4, 256, failed)) { failed = true; break; }
+        // while D_X runs: this chunk's e^gamma_n is kept, and
         // R <- R Diag(e^gamma_n of chunk c - 1) = S_c^T (column d scales by e^gamma_n[d])
-        if (c > 0) write_o(c - 1);
         if ((warp & 3) == 0) {
             egc[(c & 1) * 128 + 64 * grp + lane] = EG[64 * grp + lane];
             egc[(c & 1) * 128 + 64 * grp + 32 + lane] = EG[64 * grp + 32 + lane];
         }
         if (c > 0) {
+            fence_after_sync();
 #pragma unroll 1
             for (int pass = 0; pass < 2; ++pass) {
                 float v[32];
@@ -1129,7 +1113,7 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         }
 
         failed = !wait_bar(&bars[B_X], (uint32_t)(c & 1), x.flag, a, pc);
-        if (bar_or(1, 256, failed)) { failed = true; break; }
+        if (bar_or(4, 256, failed)) { failed = true; break; }
         fence_after_sync();
         // Vt^T = U^T - S^T W^T for tokens 32 grp .. +31 -> bf16 token pairs at tV
         {
@@ -1146,25 +1130,11 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         }
         tmem_st_wait();
         fence_before_sync();
-        bar_named(1, 256);
+        bar_arrive(kBarIss, kIssCount);  // Vt^T (and the rescaled R) are in TMEM
 
-        // O^T += Vt^T Aqk^T;  R += Vt^T Km  (A: Vt^T bf16 in TMEM)
-        if (lead) {
-            fence_after_sync();
-            const uint32_t ido = idesc_bf16(128, 64, false, false, false);
-            const uint32_t ids = idesc_bf16(128, 128, false, false, false);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                mma_ts(tmem + tX + 64, tmem + tV + 8 * s, dK(sbase + oB + Slot::oAQ, 8192, s), ido, 1);
-                mma_ts(tmem + tS, tmem + tV + 8 * s, dK(sbase + oB + Slot::oKM, 16384, s), ids, 1);
-            }
-            commit(&bars[B_S2]);
-        }
-        failed = !wait_bar(&bars[B_S2], (uint32_t)(c & 1), x.flag, a, pc);
-        if (bar_or(1, 256, failed)) { failed = true; break; }
+        failed = !wait_bar(&bars[B_R], (uint32_t)(c & 1), x.flag, a, pc);
+        if (bar_or(4, 256, failed)) { failed = true; break; }
         fence_after_sync();
-        if (lead) mbar_arrive(&bars[B_EMPTY0 + b]);  // buffer b consumed
-
         // S_{c+1}^T = R Diag(e^gamma_n) -> bf16 operand for the next chunk
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
@@ -1188,17 +1158,16 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         }
         tmem_st_wait();
         fence_before_sync();
+        if (c + 1 < nchunks) bar_arrive(kBarIss, kIssCount);  // S_{c+1}^T is in TMEM
     }
     if (failed) {
         *x.flag = 1;
+        bar_arrive(kBarIss, kIssCount);  // the issuer may be waiting for this warp group
         return;
-    }
-    if (nchunks > 0) {
-        fence_after_sync();
-        write_o(nchunks - 1);
     }
     if (a.ht != nullptr) {
         // S_N^T = R Diag(e^gamma_n of the last chunk) (R = h0^T when there is none)
+        fence_after_sync();
         float *ht = a.ht + ((int64_t)n * a.H_v + h) * 128 * 128 + dv;
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
@@ -1210,6 +1179,128 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
                 ht[(int64_t)(64 * grp + 32 * pass + e) * 128] = nchunks > 0 ? v[e] * eg[e] : v[e];
         }
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// consumer, MMA issuer (warp 7; lane 0 issues): per chunk c, once its slot image has landed,
+// the output half of its D_X buffer has been read out (chunk c - 2) and S_c^T is in TMEM:
+//   D_X = S_c^T [W^T | Qp^T]   (A: S_c^T bf16 in TMEM; B: the W^T and Qp^T tiles, MN-major)
+// then, once Vt^T is in TMEM:
+//   R += Vt^T Km  (commit B_R: the next state's copy may start),
+//   O^T = D_X[:, 64:] + Vt^T Aqk^T  (commit B_O: the output may leave).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void consumer_issuer(const FwdArgs &a, const PcArgs &pc, const Ctx &x, int u) {
+    uint64_t *bars = x.bars;
+    const uint32_t tmem = x.tmem, sbase = x.sbase;
+    const bool lead = (threadIdx.x & 31) == 0;
+    const int nchunks = x.units[u].nch;
+    bool failed = false;
+    for (int c = 0; c < nchunks; ++c) {
+        const int b = c % Cons::kBufs;
+        const uint32_t oB = b * Slot::kStride;
+        const uint32_t tX = (c & 1) ? tX1 : tX0;
+        if (lead) {
+            failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c / Cons::kBufs) & 1), x.flag, a, pc);
+            if (!failed && c >= 2)
+                failed = !wait_bar(&bars[B_XFREE0 + (c & 1)], (uint32_t)(((c >> 1) - 1) & 1), x.flag, a, pc);
+        }
+        if (__shfl_sync(0xffffffffu, (int)failed, 0)) { failed = true; break; }
+        bar_named(kBarIss, kIssCount);  // S_c^T is in TMEM
+        if (__shfl_sync(0xffffffffu, *x.flag, 0)) { failed = true; break; }
+        if (lead) {
+            fence_after_sync();
+            const uint32_t id = idesc_bf16(128, 128, false, true, false);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_ts(tmem + tX, tmem + tSA + 8 * s, dMN(sbase + oB + Slot::oWT, Slot::oQP - Slot::oWT, s), id,
+                       s > 0);
+            commit(&bars[B_X]);
+        }
+        __syncwarp();
+        bar_named(kBarIss, kIssCount);  // Vt^T (and the rescaled R) are in TMEM
+        if (__shfl_sync(0xffffffffu, *x.flag, 0)) { failed = true; break; }
+        if (lead) {
+            fence_after_sync();
+            const uint32_t ido = idesc_bf16(128, 64, false, false, false);
+            const uint32_t ids = idesc_bf16(128, 128, false, false, false);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_ts(tmem + tS, tmem + tV + 8 * s, dK(sbase + oB + Slot::oKM, 16384, s), ids, 1);
+            commit(&bars[B_R]);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_ts(tmem + tX + 64, tmem + tV + 8 * s, dK(sbase + oB + Slot::oAQ, 8192, s), ido, 1);
+            commit(&bars[B_O]);
+        }
+        __syncwarp();
+    }
+    if (failed) *x.flag = 1;
+}
+
+// TMA 2-D store shared -> global (bulk async-group of the issuing thread).
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------------------
+// consumer, epilogue (warps 12-15): O^T of each chunk, scaled and rounded, leaves through the
+// slot buffer of that chunk, whose W^T area (all its MMAs are complete) holds the [tok][d_v]
+// tile for one TMA store; the buffer goes back to the loader once the store has read it. A
+// chunk shorter than 64 tokens is written by plain stores of its valid rows.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void consumer_epilogue(const FwdArgs &a, const TcMaps &maps, const PcArgs &pc,
+                                                  const Ctx &x, int u) {
+    unsigned char *sm = x.sm;
+    uint64_t *bars = x.bars;
+    const int et = threadIdx.x - 384, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int dv = 32 * (warp & 3) + lane;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int h = u % a.H_v;
+    const int len = x.units[u].len, nchunks = x.units[u].nch;
+    const int64_t bos = x.units[u].bos;
+    const int64_t sv = (int64_t)a.H_v * 128;
+    bf16 *o = static_cast<bf16 *>(a.o);
+    bool failed = false;
+    for (int c = 0; c < nchunks; ++c) {
+        const int b = c % Cons::kBufs;
+        unsigned char *stage = sm + b * Slot::kStride + Slot::oWT;  // [64 tok][128 d_v] bf16
+        const int nvalid = min(kChunk, len - c * kChunk);
+        const uint32_t tO = ((c & 1) ? tX1 : tX0) + 64;
+        failed = !wait_bar(&bars[B_O], (uint32_t)(c & 1), x.flag, a, pc);
+        if (bar_or(3, 128, failed)) { failed = true; break; }
+        fence_after_sync();
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+            float v[32];
+            tmem_ld32(x.tmem + lane_off + tO + 32 * hh, v);
+            if (nvalid == kChunk) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    *reinterpret_cast<bf16 *>(stage + (32 * hh + e) * 256 + dv * 2) = __float2bfloat16_rn(v[e] * a.scale);
+            } else {
+                bf16 *op = o + (bos + (int64_t)c * kChunk + 32 * hh) * sv + (int64_t)h * 128 + dv;
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (32 * hh + e < nvalid) op[(int64_t)e * sv] = __float2bfloat16_rn(v[e] * a.scale);
+            }
+        }
+        fence_before_sync();
+        fence_proxy_async();
+        bar_named(3, 128);
+        if (et == 0) {
+            mbar_arrive(&bars[B_XFREE0 + (c & 1)]);  // the issuer may reuse this D_X buffer
+            if (nvalid == kChunk) {
+                tma_store_2d(&maps.o, h * 128, (int)(bos + (int64_t)c * kChunk), stage);
+                bulk_commit();
+                bulk_wait_read();  // the tile has been read: the buffer may be refilled
+            }
+            mbar_arrive(&bars[B_EMPTY0 + b]);
+        }
+    }
+    if (et == 0) bulk_wait_done();
+    if (failed) *x.flag = 1;
 }
 
 template <bool GATE_HEAD, bool FE>
@@ -1294,8 +1385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == 0) atomicOr(a.err, kDeviceErrSeqlens);  // the unit is skipped, as in every kernel
         } else if (warp < 4 || (warp >= 8 && warp < 12)) {
             consumer_serial(a, pc, x, u);
-        } else if (warp < 8) {
+        } else if (warp < 7) {
             pend_load = consumer_loader(a, pc, x, u, units[u].nch);
+        } else if (warp == 7) {
+            consumer_issuer(a, pc, x, u);
+        } else {
+            consumer_epilogue(a, maps, pc, x, u);
         }
     } else if (tid < 256) {
         pend_front = producer_front<GATE_HEAD, FE>(a, maps, pc, x);
@@ -1307,7 +1402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__syncthreads_or(*flag != 0)) {
         // drain: every MMA and copy this CTA issued must land before TMEM is freed and the
         // CTA exits (bounded waits)
-        const bool issuer = tid == 0 || (!consumer && tid == 256);
+        const bool issuer = consumer ? tid == 224 : (tid == 0 || tid == 256);
         if (issuer) {
             fence_after_sync();
             uint64_t *z = &bars[consumer ? B_CZ : (tid == 0 ? B_PZ0 : B_PZ1)];
@@ -1392,7 +1487,7 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
 
     TcMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if (!encode_tile_maps(&maps, a, GATE_HEAD)) return cudaErrorInvalidValue;
+    if (!encode_tile_maps(&maps, a, GATE_HEAD) || !encode_o_map(&maps, a)) return cudaErrorInvalidValue;
 
     // ring depth: 8 slots per unit at least, deeper for fewer units (about 38 MB, well
     // inside L2), so that producers taking jobs in order rarely wait for a slow consumer
@@ -1472,7 +1567,7 @@ cudaError_t launch_pc_static(const FwdArgs &a, cudaStream_t stream) {
 
     TcMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if (!encode_tile_maps(&maps, a, GATE_HEAD)) return cudaErrorInvalidValue;
+    if (!encode_tile_maps(&maps, a, GATE_HEAD) || !encode_o_map(&maps, a)) return cudaErrorInvalidValue;
 
     unsigned char *base = nullptr;
     e = static_scratch(dev, &base);

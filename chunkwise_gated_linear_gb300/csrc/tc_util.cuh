@@ -23,6 +23,7 @@ constexpr long long kWaitCycles = 1ll << 31;  // bounded waits: about one second
 // v [tokens][H_v*128] bf16 (box 64 x 64, 128-byte swizzle), g [tokens][H_v*128] fp32 (box 128 x 64).
 struct TcMaps {
     CUtensorMap q, k, v, g;
+    CUtensorMap o;  // o [tokens][H_v*128] bf16 (box 128 x 64), written by the persistent kernel only
 };
 
 __device__ __forceinline__ uint32_t tf32(float x) {
@@ -213,6 +214,14 @@ inline bool encode_tile_maps(TcMaps *maps, const FwdArgs &a, bool gate_per_head)
         ok = encode_map(&maps->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.g, (uint64_t)a.H_v * 128, rows, 4, 128,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     return ok;
+}
+
+// The output map of the persistent kernel (box 128 x 64, no swizzle: 256-byte rows).
+inline bool encode_o_map(TcMaps *maps, const FwdArgs &a) {
+    const uint64_t rows = a.cu_seqlens ? (uint64_t)a.T : (uint64_t)a.N * (uint64_t)a.T;
+    if (rows == 0) return true;
+    return encode_map(&maps->o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.o, (uint64_t)a.H_v * 128, rows, 2, 128,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace tcu
