@@ -58,7 +58,8 @@ int prepare(const kda_fwd_params &p, kda::FwdArgs &a) {
     if (p.T != 0 && (p.q == nullptr || p.k == nullptr || p.v == nullptr || p.g == nullptr || p.o == nullptr))
         return KDA_ERR_INVALID_ARG;
     if (p.B < 1 || p.T < 0 || p.H_k < 1 || p.H_v < 1 || p.H_v % p.H_k != 0) return KDA_ERR_INVALID_ARG;
-    if ((p.flags & ~(KDA_FLAG_ONE_CTA_PER_UNIT | KDA_FLAG_UNFUSED_FRONTEND)) != 0) return KDA_ERR_INVALID_ARG;
+    if ((p.flags & ~(KDA_FLAG_ONE_CTA_PER_UNIT | KDA_FLAG_UNFUSED_FRONTEND | KDA_FLAG_DEBUG_SHORT_WAITS)) != 0)
+        return KDA_ERR_INVALID_ARG;
     if (p.dtype != KDA_DTYPE_BF16 && p.dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (p.gate_mode != KDA_GATE_PER_CHANNEL && p.gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_UNSUPPORTED;
     if ((p.d_k != 64 && p.d_k != 128) || (p.d_v != 64 && p.d_v != 128) || p.C != kda::kChunk)
@@ -91,6 +92,7 @@ int prepare(const kda_fwd_params &p, kda::FwdArgs &a) {
     a.scale = p.scale;
     a.gate_per_head = p.gate_mode == KDA_GATE_PER_HEAD ? 1 : 0;
     a.decay_only = p.beta == nullptr ? 1 : 0;
+    a.wait_cycles = (p.flags & KDA_FLAG_DEBUG_SHORT_WAITS) ? 1024 : kda::kDefaultWaitCycles;
     return KDA_OK;
 }
 
@@ -116,7 +118,8 @@ cudaError_t dispatch(const kda_fwd_params &p, const kda::FwdArgs &a, cudaStream_
         // few units: the persistent producer/consumer kernel, else one CTA per unit
         bool launched = false;
         cudaError_t e = cudaSuccess;
-        if (!(p.flags & KDA_FLAG_ONE_CTA_PER_UNIT)) e = kda::launch_fwd_pc(a, stream, &launched);
+        if (!(p.flags & (KDA_FLAG_ONE_CTA_PER_UNIT | KDA_FLAG_DEBUG_SHORT_WAITS)))
+            e = kda::launch_fwd_pc(a, stream, &launched);
         if (e == cudaSuccess && !launched) e = kda::launch_fwd_tc(a, stream);
         return e;
     }
@@ -206,15 +209,12 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
     kda::FwdArgs a;
     const int st = prepare(p, a);
     if (st != KDA_OK) return st;
-    // only the persistent kernel's shapes, within the static scratch (checked on the host
-    // before any CUDA call)
+    // only the persistent kernel's shapes, within the static scratch (unit count and head
+    // sizes checked on the host before any CUDA call)
     if (d_k != 128 || d_v != 128 || (int64_t)a.N * a.H_v > kda::pc_static_max_units()) return KDA_ERR_UNSUPPORTED;
     cudaError_t e = device_error_ptr(&a.err);
     if (e == cudaSuccess) e = kda::launch_fwd_pc_static(a, stream);
-    if (e == cudaErrorNotSupported) {
-        cudaGetLastError();
-        return KDA_ERR_UNSUPPORTED;
-    }
+    if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;  // from host-side checks only
     if (e != cudaSuccess) {
         t_last_cuda_error = e;
         return KDA_ERR_CUDA;

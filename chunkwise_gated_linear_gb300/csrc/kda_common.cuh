@@ -9,6 +9,7 @@
 namespace kda {
 
 constexpr int kChunk = 64;  // tokens per chunk (the only chunk length supported)
+constexpr long long kDefaultWaitCycles = 1ll << 31;  // bounded waits inside kernels: about one second
 
 // Device error bits, the same values as KDA_DEVICE_ERR_* in kda.h.
 constexpr unsigned int kDeviceErrSeqlens = 1u;
@@ -29,6 +30,7 @@ struct FwdArgs {
     int gate_per_head;
     int decay_only;             // beta == nullptr: S <- Diag(a_t) S + k_t v_t^T (no erase)
     unsigned int *err;          // device error word of the current device (KDA_DEVICE_ERR_*)
+    long long wait_cycles;      // limit of the one-CTA-per-unit kernel's bounded waits (SM cycles)
     // Fused front-end, read only by the kernels that apply it in their staging:
     int fe_qk_l2norm;           // q, k divided per (token, key head) by sqrt(sum of squares + 1e-6)
     int fe_beta_sigmoid;        // beta holds logits b: sigmoid(b) is used

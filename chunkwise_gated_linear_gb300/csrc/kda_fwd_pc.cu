@@ -1432,10 +1432,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// Stream-ordered scratch (the ring and flags here, the front-end's prepared tensors) from a
-// pool owned by the library, one per device, that keeps its memory between calls.
+// Stream-ordered scratch (the ring and flags here, the front-end's prepared tensors, the
+// backward's factors) from a pool owned by the library, one per device. The pool keeps up
+// to 64 MiB reserved between calls and releases the rest when the device, a stream or an
+// event of it is synchronised.
 namespace {
 constexpr int kMaxDevices = 64;
+constexpr uint64_t kPoolKeepBytes = 64ull << 20;
 std::mutex g_pool_mu;
 cudaMemPool_t g_pool[kMaxDevices] = {};
 }  // namespace
@@ -1452,7 +1455,9 @@ cudaError_t scratch_pool(int dev, cudaMemPool_t *out) {
         cudaMemPool_t pool = nullptr;
         cudaError_t e = cudaMemPoolCreate(&pool, &props);
         if (e != cudaSuccess) return e;
-        uint64_t keep = UINT64_MAX;
+        // keep up to kPoolKeepBytes reserved between calls (the forward's ring fits), and give
+        // anything above it back at the next synchronisation, such as the backward's scratch
+        uint64_t keep = kPoolKeepBytes;
         e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
         if (e != cudaSuccess) {
             cudaMemPoolDestroy(pool);
@@ -1600,11 +1605,14 @@ cudaError_t launch_fwd_pc(const FwdArgs &a, cudaStream_t stream, bool *launched)
     return a.gate_per_head ? launch_pc<true, false>(a, stream, launched) : launch_pc<false, false>(a, stream, launched);
 }
 
-// The same kernel with its scratch in g_static_scratch (nothing allocated). Returns
-// cudaErrorNotSupported, with nothing launched, when the call has more than kStaticUnits
-// units, more units than half the SMs, or the device cannot launch it cooperatively.
+// The same kernel with its scratch in g_static_scratch (nothing allocated), per-channel
+// gates only. Returns cudaErrorNotSupported, with nothing launched, when the call has more
+// than kStaticUnits units, more units than half the SMs, per-head gates, or the device
+// cannot launch it cooperatively.
 cudaError_t launch_fwd_pc_static(const FwdArgs &a, cudaStream_t stream) {
-    return a.gate_per_head ? launch_pc_static<true>(a, stream) : launch_pc_static<false>(a, stream);
+    // the entry point that uses it always passes per-channel gates
+    if (a.gate_per_head) return cudaErrorNotSupported;
+    return launch_pc_static<false>(a, stream);
 }
 
 int pc_static_max_units() { return kStaticUnits; }

@@ -97,6 +97,7 @@ enum {
     BAR_S2,      // serial products O^T, S^T done
     BAR_Z0,      // drains after a timeout (one per MMA-issuing thread)
     BAR_Z1,
+    BAR_NEVER,   // test aid: a phase that nothing completes (see FwdArgs::wait_cycles)
     kNumBars
 };
 
@@ -106,12 +107,13 @@ __device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 2, 256;" :::
 
 // Bounded wait on an mbarrier phase; gives up early when the CTA is aborting. On its own
 // timeout it marks the CTA as aborting. Returns false when the phase did not complete.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             return false;
         }
@@ -250,9 +252,9 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
                 Gh[ptid - 64] = negA * softplus_fast(Gh[ptid - 64] + bias0);
             }
         }
-        if constexpr (!GATE_HEAD) failed = !wait_bar(&bars[BAR_LG], (uint32_t)(p & 1), u.abort_flag);
+        if constexpr (!GATE_HEAD) failed = !wait_bar(&bars[BAR_LG], (uint32_t)(p & 1), u.abort_flag, a.wait_cycles);
         if (!failed && p >= 2)
-            failed = !wait_bar(&bars[b ? BAR_FREE1 : BAR_FREE0], (uint32_t)(((p >> 1) - 1) & 1), u.abort_flag);
+            failed = !wait_bar(&bars[b ? BAR_FREE1 : BAR_FREE0], (uint32_t)(((p >> 1) - 1) & 1), u.abort_flag, a.wait_cycles);
         if (bar_or(2, 256, failed)) { failed = true; break; }
         pend_g = -1;
         if (!GATE_HEAD && nz > 0) {
@@ -311,7 +313,7 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
                 Tot[qr * 128 + c0] = acc0;
                 Tot[qr * 128 + c1] = acc1;
             }
-            failed = !wait_bar(&bars[BAR_LQK], (uint32_t)(p & 1), u.abort_flag);
+            failed = !wait_bar(&bars[BAR_LQK], (uint32_t)(p & 1), u.abort_flag, a.wait_cycles);
             if (bar_or(2, 256, failed)) { failed = true; break; }
             pend_qk = -1;
             if (nz > 0) {
@@ -406,7 +408,7 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
                     s > 0);
             commit(&bars[BAR_G]);
         }
-        failed = !wait_bar(&bars[BAR_G], (uint32_t)(p & 1), u.abort_flag);
+        failed = !wait_bar(&bars[BAR_G], (uint32_t)(p & 1), u.abort_flag, a.wait_cycles);
         if (bar_or(2, 256, failed)) { failed = true; break; }
         fence_after_sync();
         {
@@ -519,7 +521,7 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
         fence_proxy_async();
         bar_prep();
         if (p + 1 < nchunks) stage_g(p + 1);  // G, L, T and beta are consumed
-        failed = !wait_bar(&bars[BAR_LV], (uint32_t)(p & 1), u.abort_flag);
+        failed = !wait_bar(&bars[BAR_LV], (uint32_t)(p & 1), u.abort_flag, a.wait_cycles);
         if (bar_or(2, 256, failed)) { failed = true; break; }
         pend_v = -1;
         if (nz > 0) {
@@ -546,8 +548,8 @@ __device__ __forceinline__ int prep_role(const FwdArgs &a, const TcMaps &maps, c
             commit(&bars[BAR_W]);
         }
         // W^T is single-buffered: the serial product of chunk p - 1 must have read it
-        failed = !wait_bar(&bars[BAR_W], (uint32_t)(p & 1), u.abort_flag);
-        if (!failed && p >= 1) failed = !wait_bar(&bars[BAR_WT], (uint32_t)((p - 1) & 1), u.abort_flag);
+        failed = !wait_bar(&bars[BAR_W], (uint32_t)(p & 1), u.abort_flag, a.wait_cycles);
+        if (!failed && p >= 1) failed = !wait_bar(&bars[BAR_WT], (uint32_t)((p - 1) & 1), u.abort_flag, a.wait_cycles);
         if (bar_or(2, 256, failed)) { failed = true; break; }
         if (p + 1 < nchunks) stage_v(p + 1);  // the U MMA has read V
         fence_after_sync();
@@ -614,7 +616,13 @@ __device__ __forceinline__ void serial_role(const FwdArgs &a, const Unit &u) {
     bar_serial();
 
     bool failed = false;
-    for (int c = 0; c < nchunks; ++c) {
+    if (a.wait_cycles < kDefaultWaitCycles) {
+        // test aid (shortened waits): first wait on a phase that nothing completes, so that
+        // the call takes the failure path every time
+        failed = !wait_bar(&u.bars[BAR_NEVER], 0u, u.abort_flag, a.wait_cycles);
+        failed = bar_or(1, 128, failed);
+    }
+    for (int c = 0; c < nchunks && !failed; ++c) {
         const int row0 = c * kChunk;
         const int nvalid = min(kChunk, len - row0);
         const int b = c & 1;
@@ -624,7 +632,7 @@ __device__ __forceinline__ void serial_role(const FwdArgs &a, const Unit &u) {
         const float *EG = reinterpret_cast<const float *>(sm + (b ? Lay::oEG1 : Lay::oEG0));
         const uint32_t tU = b ? tU1 : tU0;
 
-        failed = !wait_bar(&bars[b ? BAR_FULL1 : BAR_FULL0], (uint32_t)((c >> 1) & 1), u.abort_flag);
+        failed = !wait_bar(&bars[b ? BAR_FULL1 : BAR_FULL0], (uint32_t)((c >> 1) & 1), u.abort_flag, a.wait_cycles);
         if (bar_or(1, 128, failed)) { failed = true; break; }
         fence_after_sync();
 
@@ -653,7 +661,7 @@ __device__ __forceinline__ void serial_role(const FwdArgs &a, const Unit &u) {
         }
         tmem_st_wait();
 
-        failed = !wait_bar(&bars[BAR_X], (uint32_t)(c & 1), u.abort_flag);
+        failed = !wait_bar(&bars[BAR_X], (uint32_t)(c & 1), u.abort_flag, a.wait_cycles);
         if (bar_or(1, 128, failed)) { failed = true; break; }
         fence_after_sync();
         if (dv == 0) mbar_arrive(&bars[BAR_WT]);  // W^T is no longer needed
@@ -684,7 +692,7 @@ __device__ __forceinline__ void serial_role(const FwdArgs &a, const Unit &u) {
             }
             commit(&bars[BAR_S2]);
         }
-        failed = !wait_bar(&bars[BAR_S2], (uint32_t)(c & 1), u.abort_flag);
+        failed = !wait_bar(&bars[BAR_S2], (uint32_t)(c & 1), u.abort_flag, a.wait_cycles);
         if (bar_or(1, 128, failed)) { failed = true; break; }
         fence_after_sync();
         if (dv == 0) mbar_arrive(&bars[b ? BAR_FREE1 : BAR_FREE0]);  // hand-off slot b consumed

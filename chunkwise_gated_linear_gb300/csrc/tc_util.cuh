@@ -17,7 +17,7 @@ namespace tcu {
 using namespace tc5;
 
 constexpr int LDF = 68;                       // fp32 row stride of the 64 x 64 L and T tiles
-constexpr long long kWaitCycles = 1ll << 31;  // bounded waits: about one second
+constexpr long long kWaitCycles = kDefaultWaitCycles;  // bounded waits: about one second
 
 // Tensor maps of the per-chunk tiles (TMA): q, k [tokens][H_k*128] bf16 (box 128 x 64),
 // v [tokens][H_v*128] bf16 (box 64 x 64, 128-byte swizzle), g [tokens][H_v*128] fp32 (box 128 x 64).

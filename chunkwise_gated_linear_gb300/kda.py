@@ -26,6 +26,7 @@ KDA_GATE_PER_CHANNEL = 0
 KDA_GATE_PER_HEAD = 1
 KDA_FLAG_ONE_CTA_PER_UNIT = 1
 KDA_FLAG_UNFUSED_FRONTEND = 2
+KDA_FLAG_DEBUG_SHORT_WAITS = 4
 KDA_DEVICE_ERR_SEQLENS = 1
 KDA_DEVICE_ERR_TIMEOUT = 2
 

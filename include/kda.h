@@ -130,7 +130,10 @@ typedef struct kda_fwd_params {
  * runs a persistent kernel that occupies every SM: the chunk-local factors of all units
  * are built in parallel on the SMs the units leave free and handed to one SM per unit
  * that runs the serial state step. It allocates about 220 KiB per unit of stream-ordered
- * scratch from a memory pool the library owns (kept between calls). KDA_FLAG_ONE_CTA_PER_UNIT
+ * scratch from a memory pool the library owns (one per device). The pool keeps up to
+ * 64 MiB reserved between calls, enough for this scratch, and returns anything above that
+ * (the backward's scratch, for instance) to the device when the device, a stream or an
+ * event is next synchronised. KDA_FLAG_ONE_CTA_PER_UNIT
  * selects the kernel with one CTA per unit instead, which allocates nothing and leaves
  * the other SMs free for concurrent work. Both give the same result up to rounding.
  */
@@ -139,6 +142,14 @@ typedef struct kda_fwd_params {
  * pass into scratch even where the selected kernel can apply it itself (for comparison;
  * the result agrees up to rounding). Ignored by the other entry points. */
 #define KDA_FLAG_UNFUSED_FRONTEND 2
+/* Test aid for the failure path: the one-CTA-per-unit kernel is used (as with
+ * KDA_FLAG_ONE_CTA_PER_UNIT, bf16 with d_k = d_v = 128), its waits give up after about 1,000
+ * SM cycles instead of about one second, and its serial warps first wait on a barrier phase
+ * that nothing completes, so that the wait runs out; the kernel then drains its copies and
+ * tensor-core work, frees its tensor memory, leaves its outputs undefined and raises
+ * KDA_DEVICE_ERR_TIMEOUT. Read by kda_chunk_fwd_ex and kda_chunk_fwd_fused; the recurrent
+ * entry points accept and ignore it. */
+#define KDA_FLAG_DEBUG_SHORT_WAITS 4
 
 /*
  * kda_chunk_fwd_ex — the general entry point: dtype and gate mode chosen by the struct.
@@ -152,13 +163,20 @@ int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream);
  * persistent kernel with its scratch (the ring of chunk slots and its flags) in one
  * fixed array of device memory inside the library: 9,568,256 + 1,024 bytes, room for 16
  * (sequence, value head) units. The pages have no counterpart: it exists for callers
- * that must not allocate (nothing is allocated, on the device or the host).
+ * that must not allocate (nothing is allocated, on the device or the host) — for example a
+ * process that hands all device memory to its own allocator at start-up, where an
+ * allocation inside the library could fail in the middle of a run, or one that must keep
+ * its peak device memory fixed and known in advance.
  *
  * Supported: bf16, d_k = d_v = 128, C = 64, at most 16 units (B * H_v, or N * H_v with
  * cu_seqlens) and at most half as many units as the device has SMs; anything else returns
- * KDA_ERR_UNSUPPORTED with nothing launched (the unit and size checks are made on the host
- * before any CUDA call). Each call first zeroes the flag words of the array with
- * cudaMemsetAsync on `stream`; the slots need no clearing.
+ * KDA_ERR_UNSUPPORTED with nothing launched. The unit-count and head-size checks are made
+ * on the host before any CUDA call; the checks of the SM count and of cooperative launch
+ * follow cudaGetDevice and cudaDeviceGetAttribute. Each call first zeroes the flag words of
+ * the array with cudaMemsetAsync on `stream`; the slots need no clearing. The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) and the device error
+ * word, and later calls reuse both: they assume the device's primary context is not reset
+ * (cudaDeviceReset) while the library stays loaded.
  *
  * The array is shared by every call of this entry point on a device: calls that overlap
  * in time (on any stream, from any thread) race on it and give wrong results. The caller
@@ -253,7 +271,8 @@ int kda_recurrent_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cud
  * Outputs are fully overwritten. Scratch: about 540 KB per (64-token chunk, value head)
  * at d = 128 (the chunk factors, entry states and their adjoints), plus fp32 accumulators
  * of dq and dk for bf16 outputs, all stream-ordered from the library's pool and freed on
- * the same stream. Errors as kda_chunk_fwd_ex (flags must be 0).
+ * the same stream; the pool gives it back to the device at the next synchronisation (it
+ * keeps at most 64 MiB between calls). Errors as kda_chunk_fwd_ex (flags must be 0).
  */
 typedef struct kda_bwd_params {
     const void *q, *k, *v;

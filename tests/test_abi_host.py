@@ -74,7 +74,7 @@ def test_ex_rejects_unknown_modes_and_flags():
     p = kda.kda_fwd_params(A, A, A, A, A, None, A, None, 1, 64, 1, 1, 128, 128, 64, 1.0, None,
                            kda.KDA_DTYPE_BF16, kda.KDA_GATE_PER_CHANNEL, 8)
     assert kda.kda_chunk_fwd_ex(p, 0) == kda.KDA_ERR_INVALID_ARG
-    p.flags = kda.KDA_FLAG_ONE_CTA_PER_UNIT | kda.KDA_FLAG_UNFUSED_FRONTEND | 4
+    p.flags = kda.KDA_FLAG_ONE_CTA_PER_UNIT | kda.KDA_FLAG_UNFUSED_FRONTEND | kda.KDA_FLAG_DEBUG_SHORT_WAITS | 16
     assert kda.kda_chunk_fwd_ex(p, 0) == kda.KDA_ERR_INVALID_ARG
     p.flags = 0
     p.dtype = 7
