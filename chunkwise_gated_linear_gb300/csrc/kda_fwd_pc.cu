@@ -115,6 +115,7 @@ struct Common {
 
 static_assert(Common::kBytes <= 232448, "shared memory");
 static_assert(Common::oEGc % 16 == 0, "float4 reads of the e^gamma_n copies");
+static_assert(Slot::kBytes % 128 == 0 && Slot::kStride % 128 == 0, "slots are whole 128-byte lines");
 
 // TMEM columns
 constexpr uint32_t tGram = 0, tW = 64, tU = 128, kTmemProd = 256;     // producer
@@ -697,6 +698,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         if (ptid == kIssImg) {
             // Qp^T, Km^T, Aqk, e^gamma_n -> the ring slot, one bulk store; once it is
             // written the image buffer is free and the back stage may publish the job
+            fence_proxy_async_global();  // after the slot was seen free (and dropped from L2)
             bulk_store(slot_ptr(pc, u, c) + Slot::oQP, sm + Prod::oIMG, Slot::kFrontBytes);
             bulk_commit();
         }
@@ -967,6 +969,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         fence_before_sync();
         bar_named(2, 256);
         if (ptid == kPublisher) {
+            fence_proxy_async_global();  // after the slot was seen free (and dropped from L2)
             bulk_store(slot + Slot::oWT, sm + Prod::oT, 16384);
             bulk_store(slot + Slot::oU, sm + oKP, 16384);
             bulk_commit();
@@ -1236,6 +1239,11 @@ __device__ __forceinline__ void consumer_issuer(const FwdArgs &a, const PcArgs &
     if (failed) *x.flag = 1;
 }
 
+// Drop a 128-byte line from L2 without writing it back (its contents become undefined).
+__device__ __forceinline__ void discard_l2(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // TMA 2-D store shared -> global (bulk async-group of the issuing thread).
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, const void *src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -1285,6 +1293,14 @@ __device__ __forceinline__ void consumer_epilogue(const FwdArgs &a, const TcMaps
                 for (int e = 0; e < 32; ++e)
                     if (32 * hh + e < nvalid) op[(int64_t)e * sv] = __float2bfloat16_rn(v[e] * a.scale);
             }
+        }
+        // The ring slot of this chunk was copied into shared memory long ago (its copy is
+        // complete: B_O follows the MMAs that read it). Its lines are dropped from L2
+        // without being written back to DRAM: the producer that reuses the slot
+        // overwrites every byte, and only after this CTA releases it (B_EMPTY, then done[u]).
+        {
+            const unsigned char *slot = slot_ptr(pc, u, c);
+            for (int i = et; i < Slot::kBytes / 128; i += 128) discard_l2(slot + (size_t)i * 128);
         }
         fence_before_sync();
         fence_proxy_async();
