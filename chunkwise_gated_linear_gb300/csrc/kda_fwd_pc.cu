@@ -133,7 +133,9 @@ enum {
     // consumer
     B_FULL0, B_FULL1, B_FULL2,     // slot image in buffer 0 / 1 / 2 landed
     B_EMPTY0, B_EMPTY1, B_EMPTY2,  // buffer 0 / 1 / 2 consumed by the serial step
-    B_X, B_R, B_O,           // consumer products: D_X, the state update, the output
+    B_X, B_R,                // consumer products: D_X, the state update
+    B_O0, B_O1,              // the output of D_X buffer 0 / 1 is complete (one barrier per
+                             // buffer: each completes again only after the epilogue freed it)
     B_XFREE0, B_XFREE1,      // the output half of D_X buffer 0 / 1 has been read out
     B_CZ,
     kNumBars
@@ -1190,7 +1192,7 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
 //   D_X = S_c^T [W^T | Qp^T]   (A: S_c^T bf16 in TMEM; B: the W^T and Qp^T tiles, MN-major)
 // then, once Vt^T is in TMEM:
 //   R += Vt^T Km  (commit B_R: the next state's copy may start),
-//   O^T = D_X[:, 64:] + Vt^T Aqk^T  (commit B_O: the output may leave).
+//   O^T = D_X[:, 64:] + Vt^T Aqk^T  (commit B_O0 / B_O1 by D_X buffer: the output may leave).
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void consumer_issuer(const FwdArgs &a, const PcArgs &pc, const Ctx &x, int u) {
     uint64_t *bars = x.bars;
@@ -1232,7 +1234,7 @@ __device__ __forceinline__ void consumer_issuer(const FwdArgs &a, const PcArgs &
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_ts(tmem + tX + 64, tmem + tV + 8 * s, dK(sbase + oB + Slot::oAQ, 8192, s), ido, 1);
-            commit(&bars[B_O]);
+            commit(&bars[B_O0 + (c & 1)]);
         }
         __syncwarp();
     }
@@ -1276,7 +1278,7 @@ __device__ __forceinline__ void consumer_epilogue(const FwdArgs &a, const TcMaps
         unsigned char *stage = sm + b * Slot::kStride + Slot::oWT;  // [64 tok][128 d_v] bf16
         const int nvalid = min(kChunk, len - c * kChunk);
         const uint32_t tO = ((c & 1) ? tX1 : tX0) + 64;
-        failed = !wait_bar(&bars[B_O], (uint32_t)(c & 1), x.flag, a, pc);
+        failed = !wait_bar(&bars[B_O0 + (c & 1)], (uint32_t)((c >> 1) & 1), x.flag, a, pc);
         if (bar_or(3, 128, failed)) { failed = true; break; }
         fence_after_sync();
 #pragma unroll 1
@@ -1295,7 +1297,7 @@ __device__ __forceinline__ void consumer_epilogue(const FwdArgs &a, const TcMaps
             }
         }
         // The ring slot of this chunk was copied into shared memory long ago (its copy is
-        // complete: B_O follows the MMAs that read it). Its lines are dropped from L2
+        // complete: B_O0 / B_O1 follow the MMAs that read it). Its lines are dropped from L2
         // without being written back to DRAM: the producer that reuses the slot
         // overwrites every byte, and only after this CTA releases it (B_EMPTY, then done[u]).
         {

@@ -53,3 +53,27 @@ def test_workload_parity(name):
         got_o.append(o[s:e, h]); want_o.append(ou); got_h.append(ht[n, h]); want_h.append(hu)
     assert rel_l2(np.concatenate(got_o), np.concatenate(want_o)) <= tol
     assert rel_l2(np.stack(got_h), np.stack(want_h)) <= tol
+
+
+def test_long_sequences_repeat_without_stalls():
+    """Grouped heads, 32 units x 512 chunks: the persistent kernel's roles run hundreds of
+    laps of their barriers. Twenty calls in a row must neither raise the device error (a
+    bounded wait that ran out) nor differ by a bit from the first call."""
+    import torch
+
+    from chunkwise_gated_linear_gb300 import chunk_kda_fwd, kda
+
+    B, T, H, HK, D = 1, 32768, 32, 16, 128
+    gen = torch.Generator(device="cuda").manual_seed(21)
+    q = torch.nn.functional.normalize(torch.randn(B, T, HK, D, device="cuda", generator=gen), dim=-1).bfloat16()
+    k = torch.nn.functional.normalize(torch.randn(B, T, HK, D, device="cuda", generator=gen), dim=-1).bfloat16()
+    v = torch.randn(B, T, H, D, device="cuda", generator=gen).bfloat16()
+    g = torch.log(torch.empty(B, T, H, D, device="cuda").uniform_(0.9, 0.999, generator=gen))
+    beta = torch.rand(B, T, H, device="cuda", generator=gen)
+    stream = torch.cuda.current_stream().cuda_stream
+    kda.kda_get_device_error(stream)
+    o0, h0 = chunk_kda_fwd(q, k, v, g, beta)
+    for _ in range(20):
+        o, h = chunk_kda_fwd(q, k, v, g, beta)
+        assert kda.kda_get_device_error(stream) == 0
+        assert torch.equal(o, o0) and torch.equal(h, h0)
