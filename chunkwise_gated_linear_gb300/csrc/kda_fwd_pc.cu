@@ -16,13 +16,14 @@
 //                         on tf32 mma.sync); D_W = Kp^T (T diag beta)^T, D_U = V^T (T diag beta)^T
 //     -> the chunk's slot in a per-unit ring in global memory: W^T, Qp^T, Km^T, Aqk (bf16,
 //        in the consumer's 128-byte swizzled shared-memory image), U^T (bf16), e^gamma_n.
-//   consumer CTA (unit u), TMEM holds R [d_v x d_k] fp32 with S_c^T = R Diag(e^gamma_n of
-//   chunk c - 1), thread = d_v row (Kbar = Km Diag(e^gamma_n) is never formed):
+//   consumer CTA (unit u), TMEM holds R [d_v x d_k] fp32 = S_c^T, thread = d_v row (Kbar =
+//   Km Diag(e^gamma_n) is never formed: S_{c+1}^T = (S_c^T + Vt^T Km) Diag(e^gamma_n)):
 //     bulk copies bring each slot into shared memory (three buffers, up to three chunks
 //     ahead of the serial step), then
-//     D_X = S_c^T [W^T | Qp^T] (A: the bf16 copy of S_c^T);  R <- R Diag(e^gamma_n, c - 1);
+//     D_X = S_c^T [W^T | Qp^T] (A: the bf16 copy of S_c^T);
 //     Vt^T = U^T - D_X[:, :64];  O^T = D_X[:, 64:] + Vt^T Aqk^T;  R += Vt^T Km;
-//     bf16 copy of S_{c+1}^T = R Diag(e^gamma_n, c).
+//     R <- R Diag(e^gamma_n) = S_{c+1}^T, with its bf16 copy for the next chunk.
+//   The MMAs are issued by one warp, the output leaves through an epilogue warp group.
 //
 // Hand-offs through global memory use per-slot sequence numbers: a producer publishes
 // chunk c of unit u by a release store of c + 1 into ready[u][c % R] after its writes;
@@ -1092,29 +1093,11 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
 
         failed = !wait_bar(&bars[B_FULL0 + b], (uint32_t)((c / Cons::kBufs) & 1), x.flag, a, pc);
         if (bar_or(4, 256, failed)) { failed = true; break; }
-        // while D_X runs: this chunk's e^gamma_n is kept, and
-        // R <- R Diag(e^gamma_n of chunk c - 1) = S_c^T (column d scales by e^gamma_n[d])
+        // this chunk's e^gamma_n is kept (the slot buffer may be released before the copy
+        // pass below reads it)
         if ((warp & 3) == 0) {
             egc[(c & 1) * 128 + 64 * grp + lane] = EG[64 * grp + lane];
             egc[(c & 1) * 128 + 64 * grp + 32 + lane] = EG[64 * grp + 32 + lane];
-        }
-        if (c > 0) {
-            fence_after_sync();
-#pragma unroll 1
-            for (int pass = 0; pass < 2; ++pass) {
-                float v[32];
-                tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
-                const float *eg = egc + ((c - 1) & 1) * 128 + 64 * grp + 32 * pass;
-                uint32_t y0[16], y1[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    y0[e] = __float_as_uint(v[e] * eg[e]);
-                    y1[e] = __float_as_uint(v[16 + e] * eg[16 + e]);
-                }
-                tmem_st16(tmem + lane_off + tSc + 32 * pass, y0);
-                tmem_st16(tmem + lane_off + tSc + 32 * pass + 16, y1);
-            }
-            tmem_st_wait();
         }
 
         failed = !wait_bar(&bars[B_X], (uint32_t)(c & 1), x.flag, a, pc);
@@ -1140,7 +1123,8 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         failed = !wait_bar(&bars[B_R], (uint32_t)(c & 1), x.flag, a, pc);
         if (bar_or(4, 256, failed)) { failed = true; break; }
         fence_after_sync();
-        // S_{c+1}^T = R Diag(e^gamma_n) -> bf16 operand for the next chunk
+        // S_{c+1}^T = R Diag(e^gamma_n): back into R (fp32) and as the bf16 operand of the
+        // next chunk
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
             // the factors first, so that their loads overlap the TMEM load's wait
@@ -1156,10 +1140,22 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
             }
             float v[32];
             tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
-            uint32_t p16[16];
+            uint32_t p16[16], y0[16], y1[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) p16[e] = pack_bf16(v[2 * e] * eg[2 * e], v[2 * e + 1] * eg[2 * e + 1]);
+            for (int e = 0; e < 16; ++e) {
+                const float s0 = v[2 * e] * eg[2 * e], s1 = v[2 * e + 1] * eg[2 * e + 1];
+                p16[e] = pack_bf16(s0, s1);
+                if (e < 8) {
+                    y0[2 * e] = __float_as_uint(s0);
+                    y0[2 * e + 1] = __float_as_uint(s1);
+                } else {
+                    y1[2 * e - 16] = __float_as_uint(s0);
+                    y1[2 * e - 15] = __float_as_uint(s1);
+                }
+            }
             tmem_st16(tmem + lane_off + tSAc + 16 * pass, p16);
+            tmem_st16(tmem + lane_off + tSc + 32 * pass, y0);
+            tmem_st16(tmem + lane_off + tSc + 32 * pass + 16, y1);
         }
         tmem_st_wait();
         fence_before_sync();
@@ -1171,17 +1167,15 @@ __device__ __forceinline__ void consumer_serial(const FwdArgs &a, const PcArgs &
         return;
     }
     if (a.ht != nullptr) {
-        // S_N^T = R Diag(e^gamma_n of the last chunk) (R = h0^T when there is none)
+        // S_N^T = R (h0^T when there is no chunk)
         fence_after_sync();
         float *ht = a.ht + ((int64_t)n * a.H_v + h) * 128 * 128 + dv;
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
             float v[32];
             tmem_ld32(tmem + lane_off + tSc + 32 * pass, v);
-            const float *eg = egc + ((nchunks - 1) & 1) * 128 + 64 * grp + 32 * pass;
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-                ht[(int64_t)(64 * grp + 32 * pass + e) * 128] = nchunks > 0 ? v[e] * eg[e] : v[e];
+            for (int e = 0; e < 32; ++e) ht[(int64_t)(64 * grp + 32 * pass + e) * 128] = v[e];
         }
     }
 }
