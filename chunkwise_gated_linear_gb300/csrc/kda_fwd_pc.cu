@@ -148,10 +148,15 @@ struct UnitInfo {
 };
 
 // Ring and flags in global memory; ready/done/abort start at zero for every launch.
+// Each unit's flags have a 128-byte line of their own: a unit's ready words are polled by its
+// consumer, its done word by the producers waiting for one of its slots, and lines shared by
+// several units would concentrate that polling on a few L2 slices.
+constexpr int kFlagLine = 32;  // ints
+
 struct PcArgs {
     unsigned char *ring;   // [U][R] slots of Slot::kStride bytes
-    int *ready;            // [U][R]: c + 1 once chunk c is in slot c % R
-    int *done;             // [U]: chunks whose slot image has been copied out
+    int *ready;            // [U][kFlagLine], R used: c + 1 once chunk c is in slot c % R
+    int *done;             // [U][kFlagLine], 1 used: chunks whose slot image has been copied out
     int *abort;            // set by any CTA that gave up
     int *jobs;             // equal-length units: the next job not yet claimed by a producer
     int U, P;              // units (= consumer CTAs), producer CTAs
@@ -221,6 +226,16 @@ __device__ __forceinline__ void raise_abort_w(int *abort_w, unsigned int *err, v
     *cta_flag = 1;
     if (atomicExch(abort_w, 1) == 0) atomicOr(err, kDeviceErrTimeout);
 }
+// Whether another CTA has raised the abort word, read at most once every kAbortPollCycles
+// of a wait: the word sits in one L2 line that every waiting thread of the grid would
+// otherwise load every few tens of nanoseconds, and that load stream slows every other
+// access served by the same L2 slice (the ring flags among them).
+constexpr long long kAbortPollCycles = 8192;
+__device__ __forceinline__ bool abort_due(long long now, long long &tpoll, int *abort_w) {
+    if (now - tpoll < kAbortPollCycles) return false;
+    tpoll = now;
+    return *(volatile int *)abort_w != 0;
+}
 // mbarrier phase test that lets the hardware suspend the thread until the phase completes
 // (or about `hint_ns` nanoseconds have passed), so that waiting threads take no issue slots.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
@@ -240,13 +255,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 __device__ __noinline__ bool wait_bar_slow(uint64_t *bar, uint32_t parity, volatile int *cta_flag, int *abort_w,
                                            unsigned int *err) {
     const long long t0 = clock64();
+    long long tpoll = t0;
     while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
         if (*cta_flag) return false;
-        if (*(volatile int *)abort_w) {
+        const long long now = clock64();
+        if (abort_due(now, tpoll, abort_w)) {
             *cta_flag = 1;
             return false;
         }
-        if (clock64() - t0 > kWaitCycles) {
+        if (now - t0 > kWaitCycles) {
             raise_abort_w(abort_w, err, cta_flag);
             return false;
         }
@@ -263,18 +280,23 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
 __device__ __noinline__ bool wait_geq_slow(const int *p, int target, volatile int *cta_flag, int *abort_w,
                                            unsigned int *err, int *seen) {
     const long long t0 = clock64();
+    long long tpoll = t0;
+    unsigned nap = 64u;
     int v;
     while ((v = ld_acquire(p)) < target) {
         if (*cta_flag) return false;
-        if (*(volatile int *)abort_w) {
+        const long long now = clock64();
+        if (abort_due(now, tpoll, abort_w)) {
             *cta_flag = 1;
             return false;
         }
-        if (clock64() - t0 > kWaitCycles) {
+        if (now - t0 > kWaitCycles) {
             raise_abort_w(abort_w, err, cta_flag);
             return false;
         }
-        __nanosleep(64);
+        // back off (64 ns doubling to 512 ns): a long wait polls its line less often
+        __nanosleep(nap);
+        nap = nap < 512u ? 2u * nap : nap;
     }
     if (seen) *seen = v;
     return true;
@@ -307,13 +329,15 @@ struct Ctx {
 __device__ __noinline__ bool wait_count_slow(const volatile int *p, int target, volatile int *cta_flag, int *abort_w,
                                              unsigned int *err) {
     const long long t0 = clock64();
+    long long tpoll = t0;
     while (*p < target) {
         if (*cta_flag) return false;
-        if (*(volatile int *)abort_w) {
+        const long long now = clock64();
+        if (abort_due(now, tpoll, abort_w)) {
             *cta_flag = 1;
             return false;
         }
-        if (clock64() - t0 > kWaitCycles) {
+        if (now - t0 > kWaitCycles) {
             raise_abort_w(abort_w, err, cta_flag);
             return false;
         }
@@ -561,7 +585,7 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
         // grows, so a value this CTA has already acquired that is large enough saves the
         // round trip to L2
         if (!failed && ptid == 0 && c >= pc.R && x.seen[u] < c - pc.R + 1)
-            failed = !wait_geq(&pc.done[u], c - pc.R + 1, x.flag, a, pc, &x.seen[u]);
+            failed = !wait_geq(&pc.done[u * kFlagLine], c - pc.R + 1, x.flag, a, pc, &x.seen[u]);
         // hand-off slot b (Kp^T) is free once the back stage has multiplied job jo - 2
         if (!failed && jo >= 2)
             failed = !wait_bar(&bars[B_HEMPTY0 + b], (uint32_t)(((jo >> 1) - 1) & 1), x.flag, a, pc);
@@ -753,7 +777,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         bulk_wait_done();
         if (!wait_count(x.stored, pjo + 1, x.flag, a, pc)) return false;
         fence_proxy_async_global();
-        st_release(&pc.ready[pu * pc.R + pcn % pc.R], pcn + 1);
+        st_release(&pc.ready[pu * kFlagLine + pcn % pc.R], pcn + 1);
         return true;
     };
 
@@ -1008,9 +1032,9 @@ __device__ __forceinline__ int consumer_loader(const FwdArgs &a, const PcArgs &p
             // the ring slot of chunk c - 3 is free for the producers
             if (c >= Cons::kBufs) {
                 failed = !wait_bar(&bars[B_EMPTY0 + b], (uint32_t)((k - 1) & 1), x.flag, a, pc);
-                if (!failed) st_release(&pc.done[u], c - Cons::kBufs + 1);
+                if (!failed) st_release(&pc.done[u * kFlagLine], c - Cons::kBufs + 1);
             }
-            if (!failed) failed = !wait_geq(&pc.ready[u * pc.R + c % pc.R], c + 1, x.flag, a, pc);
+            if (!failed) failed = !wait_geq(&pc.ready[u * kFlagLine + c % pc.R], c + 1, x.flag, a, pc);
             if (!failed) mbar_arrive_expect_tx(&bars[B_FULL0 + b], Slot::kBytes);
         }
         if (bar_or(2, 96, failed)) {
@@ -1450,6 +1474,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // event of it is synchronised.
 namespace {
 constexpr int kMaxDevices = 64;
+// Flag words of a launch: ready [U][kFlagLine], done [U][kFlagLine], the abort word and the
+// job counter, each on a 128-byte line of its own (R <= kFlagLine).
+struct FlagLayout {
+    size_t done, abort, jobs, bytes;  // offsets in ints from the ready array; total bytes
+};
+constexpr FlagLayout flag_layout(size_t U) {
+    return FlagLayout{U * kFlagLine, 2 * U * kFlagLine, 2 * U * kFlagLine + kFlagLine,
+                      (2 * U * kFlagLine + 2 * kFlagLine) * sizeof(int)};
+}
+inline void set_flags(PcArgs &pc, int *base, const FlagLayout &f) {
+    pc.ready = base;
+    pc.done = base + f.done;
+    pc.abort = base + f.abort;
+    pc.jobs = base + f.jobs;
+}
+
 constexpr uint64_t kPoolKeepBytes = 64ull << 20;
 std::mutex g_pool_mu;
 cudaMemPool_t g_pool[kMaxDevices] = {};
@@ -1509,9 +1549,10 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     // ring depth: 8 slots per unit at least, deeper for fewer units (about 38 MB, well
     // inside L2), so that producers taking jobs in order rarely wait for a slow consumer
     const int R = (int)std::max<int64_t>(kRing, std::min<int64_t>(4 * kRing, 512 / U));
+    static_assert(4 * kRing <= kFlagLine, "a unit's ready words fit its flag line");
     const size_t ring_bytes = (size_t)U * R * Slot::kStride;
-    const size_t flag_words = (size_t)U * R + (size_t)U + 2;  // ready, done, abort, jobs
-    const size_t flag_bytes = (flag_words * sizeof(int) + 255) & ~(size_t)255;
+    const FlagLayout fl = flag_layout((size_t)U);
+    const size_t flag_bytes = (fl.bytes + 255) & ~(size_t)255;
     cudaMemPool_t pool = nullptr;
     e = scratch_pool(dev, &pool);
     if (e != cudaSuccess) return e;
@@ -1520,10 +1561,7 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
     if (e != cudaSuccess) return e;
     PcArgs pc;
     pc.ring = static_cast<unsigned char *>(buf);
-    pc.ready = reinterpret_cast<int *>(pc.ring + ring_bytes);
-    pc.done = pc.ready + (size_t)U * R;
-    pc.abort = pc.done + U;
-    pc.jobs = pc.abort + 1;
+    set_flags(pc, reinterpret_cast<int *>(pc.ring + ring_bytes), fl);
     pc.U = (int)U;
     pc.P = sms - (int)U;
     pc.R = R;
@@ -1543,8 +1581,8 @@ cudaError_t launch_pc(const FwdArgs &a, cudaStream_t stream, bool *launched) {
 // not overlap (on any stream or thread): they share this one array.
 constexpr int kStaticUnits = 16;
 constexpr size_t kStaticRingBytes = (size_t)kStaticUnits * kRing * Slot::kStride;      // 9,568,256 B
-constexpr size_t kStaticFlagBytes = 1024;  // >= (kStaticUnits * (kRing + 1) + 2) ints
-static_assert((kStaticUnits * (kRing + 1) + 2) * sizeof(int) <= kStaticFlagBytes, "flag room");
+constexpr size_t kStaticFlagBytes = 4352;
+static_assert(flag_layout((size_t)kStaticUnits).bytes <= kStaticFlagBytes, "flag room");
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticRingBytes + kStaticFlagBytes];
 
 std::mutex g_static_mu;
@@ -1591,10 +1629,7 @@ cudaError_t launch_pc_static(const FwdArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     PcArgs pc;
     pc.ring = base;
-    pc.ready = reinterpret_cast<int *>(base + kStaticRingBytes);
-    pc.done = pc.ready + (size_t)U * kRing;
-    pc.abort = pc.done + U;
-    pc.jobs = pc.abort + 1;
+    set_flags(pc, reinterpret_cast<int *>(base + kStaticRingBytes), flag_layout((size_t)U));
     pc.U = (int)U;
     pc.P = sms - (int)U;
     pc.R = kRing;

@@ -161,7 +161,7 @@ int kda_chunk_fwd_ex(const kda_fwd_params *p, cudaStream_t stream);
 /*
  * kda_chunk_fwd_noalloc — the arguments and result of kda_chunk_fwd, computed by the
  * persistent kernel with its scratch (the ring of chunk slots and its flags) in one
- * fixed array of device memory inside the library: 9,568,256 + 1,024 bytes, room for 16
+ * fixed array of device memory inside the library: 9,568,256 + 4,352 bytes, room for 16
  * (sequence, value head) units. The pages have no counterpart: it exists for callers
  * that must not allocate (nothing is allocated, on the device or the host) — for example a
  * process that hands all device memory to its own allocator at start-up, where an
