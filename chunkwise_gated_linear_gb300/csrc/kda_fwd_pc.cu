@@ -78,22 +78,25 @@ struct Prod {
     static constexpr int oKP0 = 107520;    // Kp^T [d][tok], hand-off slots 0 / 1 (Gram A atom 1);
                                            // then U^T staging of the back stage
     static constexpr int oKP1 = 123904;
-                                           // 140288 .. 156672: free
-    static constexpr int oL = 156672;      // L fp32 [64][68] (front -> back)
-    static constexpr int oT = 174080;      // T fp32 [64][68]; then W^T staging [d][tok] bf16
-    static constexpr int oTB = 191488;     // T_beta [tok][tok'] bf16 (K-major B)
-    static constexpr int oRV = 199680;     // raw V [2 atoms (d_v)][64 tok][128 B]
-    static constexpr int oBF0 = 216064;    // beta as loaded, job parity 0 / 1
-    static constexpr int oBF1 = 216320;
-    static constexpr int oBH = 216576;     // beta handed to the back stage
-    static constexpr int oGh0 = 216832;    // per-head gates, job parity 0 / 1
-    static constexpr int oGh1 = 217088;
-    static constexpr int oTot = 217344;    // [4][128] fp32 partial gate sums
-    static constexpr int oPS = 219392;     // solve scratch, 8 warps x 16x8 fp32
+    static constexpr int oL1 = 140288;     // L fp32 [64][68] (front -> back), job parity 1
+    static constexpr int oL0 = 157696;     // the same, job parity 0
+    static constexpr int oT = 175104;      // T fp32 [64][68]; then W^T staging [d][tok] bf16
+    static constexpr int oTB = 192512;     // T_beta [tok][tok'] bf16 (K-major B)
+    static constexpr int oRV = 200704;     // raw V [2 atoms (d_v)][64 tok][128 B]
+    static constexpr int oBF0 = 217088;    // beta as loaded, job parity 0 / 1
+    static constexpr int oBF1 = 217344;
+    static constexpr int oBH0 = 217600;    // beta handed to the back stage, job parity 0 / 1
+    static constexpr int oBH1 = 217856;
+    static constexpr int oGh0 = 218112;    // per-head gates, job parity 0 / 1
+    static constexpr int oGh1 = 218368;
+    static constexpr int oTot = 218624;    // [4][128] fp32 partial gate sums
+    static constexpr int oPS = 220672;     // solve scratch, 8 warps x 16x8 fp32
     static constexpr int oRN = oPS + 4096; // front-end: 1 / |q_t| [64], 1 / |k_t| [64]
     static constexpr int kEnd = oRN + 512;
 };
 static_assert(Prod::oEG + 512 <= Prod::oKP0, "image overlaps");
+static_assert(Prod::oL1 + 64 * 68 * 4 <= Prod::oL0 && Prod::oL0 + 64 * 68 * 4 <= Prod::oT, "L buffers overlap");
+static_assert(Prod::oTB % 1024 == 0 && Prod::oRV % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 // Consumer shared memory.
 struct Cons {
     static constexpr int kBufs = 3;        // slot images in flight: loads have up to two
@@ -129,7 +132,7 @@ enum {
     B_GRAM, B_WMMA,          // MMA completion: Gram, WY
     B_HFULL0, B_HFULL1,      // front -> back hand-off slot 0 / 1 written
     B_HEMPTY0, B_HEMPTY1,    // back -> front: the Kp^T buffer of hand-off slot 0 / 1 is free
-    B_LFREE,                 // back -> front: L and beta consumed by the solve
+    B_LFREE0, B_LFREE1,      // back -> front: L and beta of job parity 0 / 1 consumed by the solve
     B_PZ0, B_PZ1,            // drains after a failure (one per MMA-issuing thread)
     // consumer
     B_FULL0, B_FULL1, B_FULL2,     // slot image in buffer 0 / 1 / 2 landed
@@ -401,7 +404,6 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
     float *G = reinterpret_cast<float *>(sm + Prod::oG);
     float *Tot = reinterpret_cast<float *>(sm + Prod::oTot);
     float *EG = reinterpret_cast<float *>(sm + Prod::oEG);
-    float *L = reinterpret_cast<float *>(sm + Prod::oL);
     const int64_t sg = GATE_HEAD ? (int64_t)a.H_v : (int64_t)a.H_v * 128;
     uint32_t pend = 0;
 
@@ -680,12 +682,15 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
             commit(&bars[B_GRAM]);
         }
         failed = !wait_bar(&bars[B_GRAM], (uint32_t)(jo & 1), x.flag, a, pc);
-        // L and beta of the back stage's current job are consumed once its solve is done
-        if (!failed && jo >= 1) failed = !wait_bar(&bars[B_LFREE], (uint32_t)((jo - 1) & 1), x.flag, a, pc);
+        // L and beta go to the buffer of this job's parity, which job jo - 2 used: its
+        // solve is long done unless the back stage is two jobs behind
+        if (!failed && jo >= 2)
+            failed = !wait_bar(&bars[B_LFREE0 + b], (uint32_t)(((jo >> 1) - 1) & 1), x.flag, a, pc);
         if (bar_or(1, 256, failed)) { failed = true; break; }
         fence_after_sync();
         {
             // each warp half reads 32 of the 64 columns of its lane's row
+            float *Lw = reinterpret_cast<float *>(sm + (b ? Prod::oL1 : Prod::oL0));
             const int row = 32 * (pw & 3) + lane;
             float v[32];
             tmem_ld32(x.tmem + lane_off + tGram + half, v);
@@ -713,10 +718,10 @@ __device__ __forceinline__ uint32_t producer_front(const FwdArgs &a, const TcMap
                     y.y = col + 1 < r ? br * v[e + 1] : 0.f;
                     y.z = col + 2 < r ? br * v[e + 2] : 0.f;
                     y.w = col + 3 < r ? br * v[e + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(L + r * LDF + col) = y;
+                    *reinterpret_cast<float4 *>(Lw + r * LDF + col) = y;
                 }
             }
-            if (ptid < 64) reinterpret_cast<float *>(sm + Prod::oBH)[ptid] = Bf[ptid];
+            if (ptid < 64) reinterpret_cast<float *>(sm + (b ? Prod::oBH1 : Prod::oBH0))[ptid] = Bf[ptid];
         }
         fence_proxy_async();
         fence_before_sync();
@@ -754,8 +759,6 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
     const uint32_t half = (uint32_t)(pw >> 2) * 32u;                // column half of a 64-wide readback
     constexpr int kPublisher = 224;  // lane 0 of the last warp: stores and publishes the slot
     float *Tm = reinterpret_cast<float *>(sm + Prod::oT);
-    const float *L = reinterpret_cast<const float *>(sm + Prod::oL);
-    const float *Bs = reinterpret_cast<const float *>(sm + Prod::oBH);
     int pend_v = -1;
     auto stage_v = [&](const JobIt &j, int jo) {
         if (ptid == 0 || ptid == 32) {  // the two d_v halves from two warps
@@ -796,6 +799,8 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         bool have_next = x.uniform ? false : next_job(nx, x, pc);  // equal lengths: after the hand-off
         unsigned char *slot = slot_ptr(pc, u, c);
         const uint32_t oKP = b ? Prod::oKP1 : Prod::oKP0;
+        const float *L = reinterpret_cast<const float *>(sm + (b ? Prod::oL1 : Prod::oL0));
+        const float *Bs = reinterpret_cast<const float *>(sm + (b ? Prod::oBH1 : Prod::oBH0));
 
         // The previous job's W^T and U^T stores read the T buffer and its Kp^T buffer: the
         // publisher waits for those reads here, ahead of the barrier after the hand-off
@@ -943,7 +948,7 @@ __device__ __forceinline__ int producer_back(const FwdArgs &a, const TcMaps &map
         failed = !wait_bar(&bars[B_LV], (uint32_t)(jo & 1), x.flag, a, pc);
         if (bar_or(2, 256, failed)) { failed = true; break; }
         pend_v = -1;
-        if (ptid == 0) mbar_arrive(&bars[B_LFREE]);  // L and beta are consumed
+        if (ptid == 0) mbar_arrive(&bars[B_LFREE0 + b]);  // L and beta of this parity are consumed
         if (nz > 0) {
             for (int i = ptid; i < nz * 16; i += 256) {
                 const int r = nvalid + (i >> 4), c16 = i & 15;
