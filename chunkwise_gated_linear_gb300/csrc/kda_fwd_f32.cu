@@ -22,10 +22,13 @@ namespace {
 
 template <int DK>
 struct F32Layout {
+    // Km and W rows are DK + 1 floats apart: the Gram reads Km by row across the lanes of
+    // a warp, which would otherwise put all 32 lanes on one shared-memory bank
+    static constexpr int LDK = DK + 1;
     static constexpr int oQ = 0;                        // [64][DK]  raw Q, then Qp
     static constexpr int oK = oQ + 64 * DK * 4;         // [64][DK]  raw K, then Kp
-    static constexpr int oKm = oK + 64 * DK * 4;        // [64][DK]  Km, then W
-    static constexpr int oG = oKm + 64 * DK * 4;        // [64][DK]  gamma, then Kbar
+    static constexpr int oKm = oK + 64 * DK * 4;        // [64][LDK] Km, then W
+    static constexpr int oG = oKm + 64 * LDK * 4;       // [64][DK]  gamma, then Kbar
     static constexpr int oV = oG + 64 * DK * 4;         // [64][64]  V, then U, then Vt
     static constexpr int oS = oV + 64 * 64 * 4;         // [DK][64]  state slice
     static constexpr int oA = oS + DK * 64 * 4;         // [64][64]  Aqk (masked)
@@ -40,6 +43,7 @@ struct F32Layout {
 template <int DK, bool GATE_HEAD>
 __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
     using Lay = F32Layout<DK>;
+    constexpr int LDK = Lay::LDK;
     extern __shared__ __align__(128) unsigned char smem[];
     float *Q = reinterpret_cast<float *>(smem + Lay::oQ);
     float *K = reinterpret_cast<float *>(smem + Lay::oK);
@@ -116,13 +120,13 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
                 acc += (GATE_HEAD ? Gh[r] : Gs[r * DK + c]) * kLog2e;
                 const float ep = exp2f(acc), em = exp2f(-acc);
                 const float kv = K[r * DK + c];
-                Km[r * DK + c] = kv * em;
+                Km[r * LDK + c] = kv * em;
                 K[r * DK + c] = a.decay_only ? 0.f : kv * ep;
                 Q[r * DK + c] = a.scale * Q[r * DK + c] * ep;
             }
             const float eg = exp2f(acc);
             Eg[c] = eg;
-            for (int r = 0; r < 64; ++r) Gs[r * DK + c] = Km[r * DK + c] * eg;  // Kbar
+            for (int r = 0; r < 64; ++r) Gs[r * DK + c] = Km[r * LDK + c] * eg;  // Kbar
         }
         __syncthreads();
 
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
             float m = 0.f, aq = 0.f;
             if (c <= r) {
                 for (int d = 0; d < DK; ++d) {
-                    const float km = Km[c * DK + d];
+                    const float km = Km[c * LDK + d];
                     m += K[r * DK + d] * km;
                     aq += Q[r * DK + d] * km;
                 }
@@ -142,19 +146,59 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
         }
         __syncthreads();
 
-        // T = (I + L)^-1, one column per thread, then T_beta = T diag(beta)
+        // T = (I + L)^-1 as a block lower-triangular inverse of 16 x 16 blocks, all in fp32:
+        // the diagonal blocks D_k by forward substitution (one column per thread), then
+        //   T_{k+1,k} = -D_{k+1} L_{k+1,k} D_k   (k = 0, 2)
+        //   T_BA = -T_BB L_BA T_AA                (32 x 32 blocks A = rows 0-31, B = 32-63)
+        // with the intermediate products kept in T's unused upper triangle; then
+        // T_beta = T diag(beta) on the lower triangle
         if (tid < 64) {
-            const int j = tid;
-            for (int r = 0; r < 64; ++r) {
-                float s = 0.f;
-                if (r == j) s = 1.f;
-                if (r > j) {
-                    for (int m = j; m < r; ++m) s -= L[r * 64 + m] * T[m * 64 + j];
-                }
-                T[r * 64 + j] = s;
+            const int b0 = 16 * (tid >> 4), j = tid & 15;
+            float v[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float s = (r == j) ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) s -= L[(b0 + r) * 64 + b0 + m] * v[m];
+                v[r] = s;
             }
-            const float bj = Bs[j];
-            for (int r = 0; r < 64; ++r) T[r * 64 + j] *= bj;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) T[(b0 + r) * 64 + b0 + j] = v[r];
+        }
+        __syncthreads();
+        for (int e = tid; e < 512; e += 256) {  // P_k = L_{k+1,k} D_k -> upper block (k, k+1)
+            const int k = 2 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
+            const int lo = 16 * k, hi = lo + 16;
+            float s = 0.f;
+            for (int m = c; m < 16; ++m) s += L[(hi + r) * 64 + lo + m] * T[(lo + m) * 64 + lo + c];
+            T[(lo + r) * 64 + hi + c] = s;
+        }
+        __syncthreads();
+        for (int e = tid; e < 512; e += 256) {  // T_{k+1,k} = -D_{k+1} P_k
+            const int k = 2 * (e >> 8), r = (e >> 4) & 15, c = e & 15;
+            const int lo = 16 * k, hi = lo + 16;
+            float s = 0.f;
+            for (int m = 0; m <= r; ++m) s += T[(hi + r) * 64 + hi + m] * T[(lo + m) * 64 + hi + c];
+            T[(hi + r) * 64 + lo + c] = -s;
+        }
+        __syncthreads();
+        for (int e = tid; e < 1024; e += 256) {  // Y = L_BA T_AA -> upper block rows 0-31, cols 32-63
+            const int r = e >> 5, c = e & 31;
+            float s = 0.f;
+            for (int m = c; m < 32; ++m) s += L[(32 + r) * 64 + m] * T[m * 64 + c];
+            T[r * 64 + 32 + c] = s;
+        }
+        __syncthreads();
+        for (int e = tid; e < 1024; e += 256) {  // T_BA = -T_BB Y
+            const int r = e >> 5, c = e & 31;
+            float s = 0.f;
+            for (int m = 0; m <= r; ++m) s += T[(32 + r) * 64 + 32 + m] * T[m * 64 + 32 + c];
+            T[(32 + r) * 64 + c] = -s;
+        }
+        __syncthreads();
+        for (int e = tid; e < 64 * 64; e += 256) {
+            const int r = e >> 6, j = e & 63;
+            if (j <= r) T[e] *= Bs[j];
         }
         __syncthreads();
 
@@ -163,7 +207,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
             const int r = i / DK, d = i % DK;
             float s = 0.f;
             for (int m = 0; m <= r; ++m) s += T[r * 64 + m] * K[m * DK + d];
-            Km[i] = s;
+            Km[r * LDK + d] = s;
         }
         float u[16];
 #pragma unroll
@@ -182,7 +226,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_f32_kernel(const FwdArgs a) {
         for (int i = tid; i < 64 * 64; i += 256) {
             const int r = i >> 6, c = i & 63;
             float s = V[i];
-            for (int d = 0; d < DK; ++d) s -= Km[r * DK + d] * S[d * 64 + c];
+            for (int d = 0; d < DK; ++d) s -= Km[r * LDK + d] * S[d * 64 + c];
             V[i] = s;
         }
         __syncthreads();
