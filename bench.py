@@ -50,9 +50,9 @@ def metric_name(entry: str, workload: str) -> str:
 # it was taken on (comments ignored); any change to the code makes the figure stale
 # (reported as null).
 MEASURED_TRAFFIC = {
-    # profiles/kda_fwd_pc_b2_t8192_h32_d128.md: 397.2 MB on the same 64 units over half the
+    # profiles/kda_fwd_pc_b2_t8192_h32_d128.md: 397.7 MB on the same 64 units over half the
     # tokens (B=2, T=4096), scaled by 2 to this workload
-    ("kda_b2_t8192_h32_d128_bf16", "bb185430c799a975"): 794_400_000,
+    ("kda_b2_t8192_h32_d128_bf16", "8e9d471b383ffba9"): 795_367_936,
 }
 
 # The translation unit of each forward kernel and the headers it includes.
