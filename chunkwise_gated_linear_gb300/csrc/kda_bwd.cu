@@ -23,21 +23,23 @@
 //
 // Five kernels, all on stream-ordered scratch from the library's pool:
 //   prep     (chunk, unit) parallel: gamma, Qp, Kp, Km, Kb, EG, M, A, T, W, U, V, dO
-//   states   (unit, 64 columns of d_v): the forward state scan, storing S and Vt per chunk
+//   states   (unit, 64 columns of d_v): the forward state scan, storing S and Vt per chunk;
+//            for bf16 inputs with d_k = d_v = 128 on tcgen05 (tf32, the state in TMEM)
 //   adjoint  (unit, 64 columns of d_v): the reverse scan of dS, storing dS' and dVt per
 //            chunk, and dh0
 //   grads    (chunk, unit) parallel: every gradient above; dq and dk written directly when
 //            each key head has one value head, else added atomically into fp32
 //            accumulators (value heads that share a key head add into the same rows)
 //   finish   the accumulators to the output dtype (grouped heads, bf16 outputs)
-// Every contraction goes through one CTA-wide GEMM on tf32 tensor cores (block_gemm: 64 x 64
-// output tiles, 32-deep k steps staged in shared memory, fp32 accumulation).
+// The other contractions go through one CTA-wide GEMM on tf32 tensor cores (block_gemm:
+// 64 x 64 output tiles, 32-deep k steps staged in shared memory, fp32 accumulation).
 #include <algorithm>
 #include <cstdint>
 #include <type_traits>
 
 #include "kda_bwd.h"
 #include "kda_common.cuh"
+#include "tc_util.cuh"
 
 namespace kda {
 
@@ -615,6 +617,262 @@ __global__ void __launch_bounds__(kT) bwd_states_kernel(const BwdArgs a) {
     }
 }
 
+// ---- states on tcgen05 (bf16 inputs, d_k = d_v = 128) ---------------------------------------
+// One CTA per (sequence, value head, 64 columns of d_v) carries R = S^T [64 v][d_k] through
+// the chunks in TMEM (fp32, an M = 64 accumulator: row r in lane 32 (r / 16) + r % 16, 128
+// columns). Per chunk c:
+//   D1 = R W^T          tf32 MMA, A = R read from TMEM, B = W [t][d] (K-major), which TMA
+//                       loads with the 128-byte swizzle
+//   element warps:      Vt^T = U^T - D1 into TMEM (the next product's A operand) and to the
+//                       scratch; the entry state S_c to the scratch; R <- R diag(e^Gn)
+//   R += Vt^T Kb        A = Vt^T from TMEM, B = Kb^T [d][t] (K-major), which the staging
+//                       warps transpose from the scratch into shared memory
+// Roles: warps 0-3 and 8-11 the element passes (lane quarter warp % 4, its 16 rows in lanes
+// 0-15; column half warp / 8), warp 4 lane 0 the loads and MMAs, warps 5-7 and 12-15 the
+// transposition of Kb. The loads, Kb^T, U and e^Gn alternate between two buffers by chunk
+// parity. Every wait is bounded; a timeout raises the device error word and ends the CTA's
+// roles, which then wait for their MMAs and copies in flight before TMEM is freed.
+struct StTc {
+    static constexpr int oW = 0;         // W [64 t][128 d]: 4 K-major atoms (32 d) of 64 x 128 B
+    static constexpr int oKbT = 32768;   // Kb^T [128 d][64 t]: 2 K-major atoms (32 t) of 128 x 128 B
+    static constexpr int oU = 65536;     // U [64 t][64 v] fp32, row-major (this CTA's columns)
+    static constexpr int oEG = 98304;    // e^Gn [128]
+    static constexpr int kBuf = 99328;   // one buffer (1024-byte multiple)
+    static constexpr int oBar = 2 * kBuf;
+    static constexpr int kBytes = oBar + 128 + 1024;  // + barriers, + alignment slack
+};
+constexpr uint32_t kStR = 0, kStD = 128, kStV = 192, kStCols = 256;  // TMEM columns
+enum { SB_LD0 = 0, SB_LD1, SB_KB0, SB_KB1, SB_D1, SB_UP0, SB_UP1, SB_EL, SB_Z, kStBars };
+
+__device__ bool st_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, unsigned int *err) {
+    if (tc5::mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!tc5::mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kDefaultWaitCycles) {
+            *abort_flag = 1;
+            atomicOr(err, kDeviceErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kT, 1) bwd_states_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap wmap,
+                                                               const __grid_constant__ CUtensorMap umap) {
+    using namespace tc5;
+    using tcu::mbar_arrive;
+    using tcu::tmem_ld32;
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char *sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + StTc::oBar);
+    __shared__ uint32_t tslot;
+    __shared__ int abort_w;
+    volatile int *abort_flag = &abort_w;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j0 = 64 * blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    constexpr int K = 128, V = 128;
+    const Lay L = make_lay(K, V);
+    int64_t bos;
+    int len;
+    if (!bounds(a, n, bos, len)) return;
+    const int nch = (len + 63) / 64;
+    if (tid == 0) {
+        for (int i = 0; i < kStBars; ++i) mbar_init(&bars[i], i == SB_EL ? 8 : 1);
+        abort_w = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tslot, kStCols);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tslot;
+    const bool elem = warp < 4 || (warp >= 8 && warp < 12);
+    const int q = warp & 3, hh = warp >> 3;  // element warps: lane quarter, column half
+    const bool row_lane = lane < 16;         // lanes 0-15 of a quarter hold rows 16 q + lane
+    const int v = j0 + 16 * q + (lane & 15);  // this lane's d_v column
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    // R = h0^T (or zero)
+    if (elem) {
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+            uint32_t r0[16], r1[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int d0 = 64 * hh + 32 * p + j, d1 = d0 + 16;
+                const float *h0 = a.h0 ? a.h0 + (((int64_t)n * a.H_v + h) * K) * V + v : nullptr;
+                r0[j] = __float_as_uint(h0 ? h0[(int64_t)d0 * V] : 0.f);
+                r1[j] = __float_as_uint(h0 ? h0[(int64_t)d1 * V] : 0.f);
+            }
+            tmem_st16(tmem + lane_off + kStR + 64 * hh + 32 * p, r0);
+            tmem_st16(tmem + lane_off + kStR + 64 * hh + 32 * p + 16, r1);
+        }
+        tmem_st_wait();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    if (warp == 4) {
+        // ---- loads and MMAs (lane 0) ----
+        if (lane == 0) {
+            auto load = [&](int c) {
+                const int b = c & 1;
+                unsigned char *B = sm + b * StTc::kBuf;
+                const int64_t slot = slot_of(a, bos, n, c, h);
+                const float *S = a.scratch + slot * L.total;
+                mbar_arrive_expect_tx(&bars[SB_LD0 + b], 32768 + 16384 + 512);
+#pragma unroll
+                for (int at = 0; at < 4; ++at) tma_load_3d(B + StTc::oW + at * 8192, &wmap, &bars[SB_LD0 + b], 32 * at, 0, (int)slot);
+                tma_load_3d(B + StTc::oU, &umap, &bars[SB_LD0 + b], j0, 0, (int)slot);
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                 smem_u32(B + StTc::oEG)), "l"(S + L.eg), "r"(512), "r"(smem_u32(&bars[SB_LD0 + b]))
+                             : "memory");
+            };
+            const uint32_t id1 = idesc_tf32(64, 64), id2 = idesc_tf32(64, 128);
+            bool ok = true;
+            int issued[2] = {-1, -1}, waited[2] = {-1, -1};  // latest chunk loaded / waited per buffer
+            if (nch > 0) {
+                load(0);
+                issued[0] = 0;
+            }
+            for (int c = 0; c < nch && ok; ++c) {
+                const int b = c & 1;
+                const uint32_t sB = smem_u32(sm + b * StTc::kBuf);
+                // R = S_c^T (the previous update is complete); buffer (c + 1) & 1 is free
+                if (c > 0) ok = st_wait(&bars[SB_UP0 + ((c - 1) & 1)], (uint32_t)(((c - 1) >> 1) & 1), abort_flag, a.err);
+                if (ok && c + 1 < nch) {
+                    load(c + 1);
+                    issued[(c + 1) & 1] = c + 1;
+                }
+                if (ok) ok = st_wait(&bars[SB_LD0 + b], (uint32_t)((c >> 1) & 1), abort_flag, a.err);
+                if (ok) waited[b] = c;
+                if (!ok) break;
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32_ts(tmem + kStD, tmem + kStR + 8 * s,
+                                desc_sw128(sB + StTc::oW + (s >> 2) * 8192 + (s & 3) * 32, 0, 1024), id1, s > 0);
+                commit(&bars[SB_D1]);
+                ok = st_wait(&bars[SB_EL], (uint32_t)(c & 1), abort_flag, a.err);
+                if (ok) ok = st_wait(&bars[SB_KB0 + b], (uint32_t)((c >> 1) & 1), abort_flag, a.err);
+                if (!ok) break;
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32_ts(tmem + kStR, tmem + kStV + 8 * s,
+                                desc_sw128(sB + StTc::oKbT + (s >> 2) * 16384 + (s & 3) * 32, 0, 1024), id2, 1);
+                commit(&bars[SB_UP0 + b]);
+            }
+            // every MMA and load of this CTA lands before TMEM is freed
+            commit(&bars[SB_Z]);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&bars[SB_Z], 0) && clock64() - t0 < kDefaultWaitCycles) {}
+            for (int bb = 0; bb < 2; ++bb) {
+                if (issued[bb] > waited[bb]) {
+                    const long long t1 = clock64();
+                    while (!mbar_try_wait(&bars[SB_LD0 + bb], (uint32_t)((issued[bb] >> 1) & 1)) &&
+                           clock64() - t1 < kDefaultWaitCycles) {}
+                }
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (elem) {
+        // ---- element passes ----
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            const unsigned char *B = sm + b * StTc::kBuf;
+            float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
+            if (!st_wait(&bars[SB_D1], (uint32_t)(c & 1), abort_flag, a.err)) break;
+            if (!st_wait(&bars[SB_LD0 + b], (uint32_t)((c >> 1) & 1), abort_flag, a.err)) break;
+            fence_after_sync();
+            {
+                // Vt^T = U^T - D1 for tokens 32 hh .. 32 hh + 31
+                float d1[32];
+                tmem_ld32(tmem + lane_off + kStD + 32 * hh, d1);
+                const float *U = reinterpret_cast<const float *>(B + StTc::oU);
+                uint32_t w0[16], w1[16];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * hh + j;
+                    const float vt = U[t * 64 + (v - j0)] - d1[j];
+                    if (row_lane) S[L.vt + (int64_t)t * V + v] = vt;
+                    if (j < 16) w0[j] = __float_as_uint(vt); else w1[j - 16] = __float_as_uint(vt);
+                }
+                tmem_st16(tmem + lane_off + kStV + 32 * hh, w0);
+                tmem_st16(tmem + lane_off + kStV + 32 * hh + 16, w1);
+            }
+            {
+                // the entry state S_c to the scratch, then R <- R diag(e^Gn), channels 64 hh .. + 63
+                const float *EG = reinterpret_cast<const float *>(B + StTc::oEG);
+#pragma unroll 1
+                for (int p = 0; p < 2; ++p) {
+                    const int d0 = 64 * hh + 32 * p;
+                    float r[32];
+                    tmem_ld32(tmem + lane_off + kStR + d0, r);
+                    uint32_t y0[16], y1[16];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (row_lane) S[L.se + (int64_t)(d0 + j) * V + v] = r[j];
+                        const float y = r[j] * EG[d0 + j];
+                        if (j < 16) y0[j] = __float_as_uint(y); else y1[j - 16] = __float_as_uint(y);
+                    }
+                    tmem_st16(tmem + lane_off + kStR + d0, y0);
+                    tmem_st16(tmem + lane_off + kStR + d0 + 16, y1);
+                }
+            }
+            tmem_st_wait();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[SB_EL]);
+        }
+    } else {
+        // ---- Kb^T staging: warps 5-7 and 12-15 (224 threads) ----
+        const int tt = (warp < 8 ? warp - 5 : warp - 9) * 32 + lane;
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            unsigned char *KbT = sm + b * StTc::kBuf + StTc::oKbT;
+            const float4 *Kb = reinterpret_cast<const float4 *>(a.scratch + slot_of(a, bos, n, c, h) * L.total + L.kb);
+            float4 r[10];
+#pragma unroll
+            for (int i = 0; i < 10; ++i) {
+                const int e = tt + 224 * i;  // t = e % 64, 4 d = 4 (e / 64)
+                if (e < 2048) r[i] = __ldg(Kb + (e & 63) * 32 + (e >> 6));
+            }
+            // the buffer's previous Kb^T (chunk c - 2) has been read by its update
+            if (c >= 2 && !st_wait(&bars[SB_UP0 + b], (uint32_t)(((c >> 1) - 1) & 1), abort_flag, a.err)) break;
+#pragma unroll
+            for (int i = 0; i < 10; ++i) {
+                const int e = tt + 224 * i;
+                if (e < 2048) {
+                    const int t = e & 63, d = 4 * (e >> 6);
+                    unsigned char *atom = KbT + (t >> 5) * 16384;
+                    const int k = t & 31;
+                    const float x[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int row = d + j;
+                        *reinterpret_cast<uint32_t *>(atom + row * 128 + (((k >> 2) ^ (row & 7)) << 4) + (k & 3) * 4) =
+                            tcu::tf32(x[j]);
+                    }
+                }
+            }
+            fence_proxy_async();
+            asm volatile("bar.sync 3, 224;" ::: "memory");
+            if (tt == 0) mbar_arrive(&bars[SB_KB0 + b]);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tmem, kStCols);
+    }
+}
+
 // ---- adjoint: the reverse scan, dS slice [K][64 columns] in shared memory -------------------
 // The chunk's operands are copied into shared memory in two sets: A, Kb, e^Gn and dO for the
 // first products, Qp and W for the second. Each set's buffer is refilled with the next chunk's
@@ -902,6 +1160,22 @@ size_t grads_smem(int K, int V) {
     return sizeof(float) * ((size_t)4 * 64 * K + (size_t)64 * KV + 2 * 4096 + 128 + 128 + 64 + kStageFloats);
 }
 
+// The tensor map of one [64][cols] fp32 factor of every slot (at `off` floats into the slot):
+// 3-D (column, token, slot), boxes of `box_cols` columns x 64 tokens, with the 128-byte
+// swizzle (K-major MMA operand tiles) or without (plain row-major tiles).
+bool encode_slot_map(CUtensorMap *m, const BwdArgs &a, const Lay &L, int64_t off, int cols, int box_cols, bool swizzle,
+                     int64_t nslots) {
+    auto enc = tcu::tensor_map_encoder();
+    if (enc == nullptr || nslots <= 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, 64, (cuuint64_t)nslots};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * sizeof(float), (cuuint64_t)L.total * sizeof(float)};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(a.scratch + off), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename T, bool GATE_HEAD>
 cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
     constexpr bool kSplit = std::is_same<T, float>::value;  // fp32-grade products for fp32 inputs
@@ -957,8 +1231,19 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
         bwd_prep_kernel<T, GATE_HEAD><<<gw, kT, psmem, stream>>>(a);
         e = cudaGetLastError();
         if (e == cudaSuccess) {
-            bwd_states_kernel<kSplit><<<dim3(V / 64, a.H_v, a.N), kT, ssmem, stream>>>(a);
-            e = cudaGetLastError();
+            CUtensorMap wmap, umap;
+            if (!kSplit && K == 128 && V == 128 && encode_slot_map(&wmap, a, L, L.wm, K, 32, true, windows * a.H_v) &&
+                encode_slot_map(&umap, a, L, L.u, V, 64, false, windows * a.H_v)) {
+                e = cudaFuncSetAttribute(bwd_states_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         StTc::kBytes);
+                if (e == cudaSuccess) {
+                    bwd_states_tc_kernel<<<dim3(2, a.H_v, a.N), kT, StTc::kBytes, stream>>>(a, wmap, umap);
+                    e = cudaGetLastError();
+                }
+            } else {
+                bwd_states_kernel<kSplit><<<dim3(V / 64, a.H_v, a.N), kT, ssmem, stream>>>(a);
+                e = cudaGetLastError();
+            }
         }
         if (e == cudaSuccess) {
             bwd_adjoint_kernel<kSplit><<<dim3(V / 64, a.H_v, a.N), kT, asmem, stream>>>(a);
