@@ -657,6 +657,15 @@ __device__ bool st_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag
     }
     return true;
 }
+// Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// st_wait by every lane of a warp, with one outcome for all of them (the warp-collective TMEM
+// accesses and __syncwarp that follow need the whole warp on the same branch).
+__device__ __forceinline__ bool st_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag, unsigned int *err) {
+    return __all_sync(0xffffffffu, st_wait(bar, parity, abort_flag, err));
+}
 
 __global__ void __launch_bounds__(kT, 1) bwd_states_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap wmap,
                                                                const __grid_constant__ CUtensorMap umap) {
@@ -786,8 +795,8 @@ __global__ void __launch_bounds__(kT, 1) bwd_states_tc_kernel(const BwdArgs a, c
             const int b = c & 1;
             const unsigned char *B = sm + b * StTc::kBuf;
             float *S = a.scratch + slot_of(a, bos, n, c, h) * L.total;
-            if (!st_wait(&bars[SB_D1], (uint32_t)(c & 1), abort_flag, a.err)) break;
-            if (!st_wait(&bars[SB_LD0 + b], (uint32_t)((c >> 1) & 1), abort_flag, a.err)) break;
+            if (!st_wait_warp(&bars[SB_D1], (uint32_t)(c & 1), abort_flag, a.err)) break;
+            if (!st_wait_warp(&bars[SB_LD0 + b], (uint32_t)((c >> 1) & 1), abort_flag, a.err)) break;
             fence_after_sync();
             {
                 // Vt^T = U^T - D1 for tokens 32 hh .. 32 hh + 31
@@ -836,6 +845,7 @@ __global__ void __launch_bounds__(kT, 1) bwd_states_tc_kernel(const BwdArgs a, c
             const int b = c & 1;
             unsigned char *KbT = sm + b * StTc::kBuf + StTc::oKbT;
             const float4 *Kb = reinterpret_cast<const float4 *>(a.scratch + slot_of(a, bos, n, c, h) * L.total + L.kb);
+            if (tt == 0 && c + 1 < nch) prefetch_l2(a.scratch + slot_of(a, bos, n, c + 1, h) * L.total + L.kb, 64 * K * 4);
             float4 r[10];
 #pragma unroll
             for (int i = 0; i < 10; ++i) {
@@ -843,7 +853,9 @@ __global__ void __launch_bounds__(kT, 1) bwd_states_tc_kernel(const BwdArgs a, c
                 if (e < 2048) r[i] = __ldg(Kb + (e & 63) * 32 + (e >> 6));
             }
             // the buffer's previous Kb^T (chunk c - 2) has been read by its update
-            if (c >= 2 && !st_wait(&bars[SB_UP0 + b], (uint32_t)(((c >> 1) - 1) & 1), abort_flag, a.err)) break;
+            // (all 224 threads take the same branch, so that none is left at the named barrier)
+            if (c >= 2 && tcu::bar_or(3, 224, !st_wait(&bars[SB_UP0 + b], (uint32_t)(((c >> 1) - 1) & 1), abort_flag, a.err)))
+                break;
 #pragma unroll
             for (int i = 0; i < 10; ++i) {
                 const int e = tt + 224 * i;
@@ -956,6 +968,353 @@ __global__ void __launch_bounds__(kT) bwd_adjoint_kernel(const BwdArgs a) {
     if (a.dh0 != nullptr)
         for (int e = tid; e < K * 64; e += kT)
             a.dh0[(((int64_t)n * a.H_v + h) * K + (e >> 6)) * V + j0 + (e & 63)] = dS[(e >> 6) * rs + (e & 63)];
+}
+
+// ---- adjoint on tcgen05 (bf16 inputs, d_k = d_v = 128) --------------------------------------
+// One CTA per (sequence, value head, 64 columns of d_v) carries Q = dS^T [64 v][d_k] backwards
+// through the chunks in TMEM (an M = 64 fp32 accumulator, 128 columns). Per chunk c, last
+// first:
+//   element warps:  dS' (= Q on entry) to the scratch; dO^T [v][t] into TMEM (an A operand)
+//   D2 = dO^T A^T^T + Q Kb^T = dVt^T [v][t]   (A^T as a K-major [s][t] tile, Kb by TMA)
+//   element warps:  dVt to the scratch, -dVt^T into TMEM, Q <- Q diag(e^Gn)
+//   Q += dO^T Qp - dVt^T W                     (Qp^T and W^T as K-major [d][t] tiles)
+// The transposed tiles are made by the staging warps from the scratch, as in the states scan.
+// Roles: warps 0-3 and 8-11 the element passes, warp 4 lane 0 the loads and MMAs, warps 5-7 and
+// 12-15 the transposition. Kb, dO, e^Gn and A^T alternate between two buffers; Qp^T and W^T
+// have one. Every wait is bounded, as in the states scan.
+struct AdTc {
+    static constexpr int oKb = 0;        // Kb [64 t][128 d]: 4 K-major atoms (32 d) of 64 x 128 B
+    static constexpr int oAT = 32768;    // A^T [64 s][64 t]: 2 K-major atoms (32 t) of 64 x 128 B
+    static constexpr int oDO = 49152;    // dO [64 t][64 v] fp32 row-major (this CTA's columns)
+    static constexpr int oEG = 65536;    // e^Gn [128]
+    static constexpr int kBuf = 66560;
+    static constexpr int oQpT = 2 * kBuf;          // Qp^T [128 d][64 t]: 2 atoms (32 t) of 128 x 128 B
+    static constexpr int oWT = oQpT + 32768;       // W^T likewise
+    static constexpr int oBar = oWT + 32768;
+    static constexpr int kBytes = oBar + 128 + 1024;
+};
+constexpr uint32_t kAdQ = 0, kAdD = 128, kAdO = 192, kAdN = 256, kAdCols = 512;  // TMEM columns
+enum { AB_LD0 = 0, AB_LD1, AB_AT0, AB_AT1, AB_QW, AB_PRE, AB_D0, AB_D1, AB_EL, AB_UP, AB_Z, kAdBars };
+
+// Transposed K-major tile: element (row, k) of a tile of 32-column atoms `atom_bytes` apart.
+__device__ __forceinline__ void st_kmajor(unsigned char *tile, int atom_bytes, int row, int k, float x) {
+    unsigned char *atom = tile + (k >> 5) * atom_bytes;
+    const int kk = k & 31;
+    *reinterpret_cast<uint32_t *>(atom + row * 128 + (((kk >> 2) ^ (row & 7)) << 4) + (kk & 3) * 4) = tcu::tf32(x);
+}
+
+__global__ void __launch_bounds__(kT, 1) bwd_adjoint_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap kbmap,
+                                                                const __grid_constant__ CUtensorMap domap) {
+    using namespace tc5;
+    using tcu::mbar_arrive;
+    using tcu::tmem_ld32;
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char *sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + AdTc::oBar);
+    __shared__ uint32_t tslot;
+    __shared__ int abort_w;
+    volatile int *abort_flag = &abort_w;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j0 = 64 * blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    constexpr int K = 128, V = 128;
+    const Lay L = make_lay(K, V);
+    int64_t bos;
+    int len;
+    if (!bounds(a, n, bos, len)) return;
+    const int nch = (len + 63) / 64;
+    if (tid == 0) {
+        for (int i = 0; i < kAdBars; ++i) mbar_init(&bars[i], (i == AB_PRE || i == AB_EL) ? 8 : 1);
+        abort_w = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tslot, kAdCols);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tslot;
+    const bool elem = warp < 4 || (warp >= 8 && warp < 12);
+    const int q = warp & 3, hh = warp >> 3;
+    const bool row_lane = lane < 16;
+    const int v = j0 + 16 * q + (lane & 15);
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    auto slot = [&](int c) { return a.scratch + slot_of(a, bos, n, c, h) * L.total; };
+    // Q = dht^T (or zero)
+    if (elem) {
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+            uint32_t r0[16], r1[16];
+            const float *dht = a.dht ? a.dht + (((int64_t)n * a.H_v + h) * K) * V + v : nullptr;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int d0 = 64 * hh + 32 * p + j;
+                r0[j] = __float_as_uint(dht ? dht[(int64_t)d0 * V] : 0.f);
+                r1[j] = __float_as_uint(dht ? dht[(int64_t)(d0 + 16) * V] : 0.f);
+            }
+            tmem_st16(tmem + lane_off + kAdQ + 64 * hh + 32 * p, r0);
+            tmem_st16(tmem + lane_off + kAdQ + 64 * hh + 32 * p + 16, r1);
+        }
+        tmem_st_wait();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // iteration i works on chunk nch - 1 - i, in buffer i & 1
+            auto load = [&](int i) {
+                const int b = i & 1, c = nch - 1 - i;
+                unsigned char *B = sm + b * AdTc::kBuf;
+                const int64_t sl = slot_of(a, bos, n, c, h);
+                mbar_arrive_expect_tx(&bars[AB_LD0 + b], 32768 + 16384 + 512);
+#pragma unroll
+                for (int at = 0; at < 4; ++at) tma_load_3d(B + AdTc::oKb + at * 8192, &kbmap, &bars[AB_LD0 + b], 32 * at, 0, (int)sl);
+                tma_load_3d(B + AdTc::oDO, &domap, &bars[AB_LD0 + b], j0, 0, (int)sl);
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                 smem_u32(B + AdTc::oEG)), "l"(a.scratch + sl * L.total + L.eg), "r"(512),
+                             "r"(smem_u32(&bars[AB_LD0 + b]))
+                             : "memory");
+            };
+            const uint32_t id64 = idesc_tf32(64, 64), id128 = idesc_tf32(64, 128);
+            const uint32_t sQW = smem_u32(sm + AdTc::oQpT), sWT = smem_u32(sm + AdTc::oWT);
+            bool ok = true;
+            int issued[2] = {-1, -1}, waited[2] = {-1, -1};
+            if (nch > 0) {
+                load(0);
+                issued[0] = 0;
+            }
+            for (int i = 0; i < nch && ok; ++i) {
+                const int b = i & 1;
+                const uint32_t sB = smem_u32(sm + b * AdTc::kBuf);
+                if (i > 0) ok = st_wait(&bars[AB_UP], (uint32_t)((i - 1) & 1), abort_flag, a.err);
+                if (ok && i + 1 < nch) {
+                    load(i + 1);
+                    issued[(i + 1) & 1] = i + 1;
+                }
+                if (ok) ok = st_wait(&bars[AB_LD0 + b], (uint32_t)((i >> 1) & 1), abort_flag, a.err);
+                if (ok) waited[b] = i;
+                if (ok) ok = st_wait(&bars[AB_PRE], (uint32_t)(i & 1), abort_flag, a.err);
+                if (ok) ok = st_wait(&bars[AB_AT0 + b], (uint32_t)((i >> 1) & 1), abort_flag, a.err);
+                if (!ok) break;
+                fence_after_sync();
+                // dVt^T = dO^T (A^T)^T + Q Kb^T
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32_ts(tmem + kAdD, tmem + kAdO + 8 * s,
+                                desc_sw128(sB + AdTc::oAT + (s >> 2) * 8192 + (s & 3) * 32, 0, 1024), id64, s > 0);
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32_ts(tmem + kAdD, tmem + kAdQ + 8 * s,
+                                desc_sw128(sB + AdTc::oKb + (s >> 2) * 8192 + (s & 3) * 32, 0, 1024), id64, 1);
+                commit(&bars[AB_D0 + b]);
+                ok = st_wait(&bars[AB_EL], (uint32_t)(i & 1), abort_flag, a.err);
+                if (ok) ok = st_wait(&bars[AB_QW], (uint32_t)(i & 1), abort_flag, a.err);
+                if (!ok) break;
+                fence_after_sync();
+                // Q += dO^T Qp - dVt^T W
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32_ts(tmem + kAdQ, tmem + kAdO + 8 * s, desc_sw128(sQW + (s >> 2) * 16384 + (s & 3) * 32, 0, 1024),
+                                id128, 1);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32_ts(tmem + kAdQ, tmem + kAdN + 8 * s, desc_sw128(sWT + (s >> 2) * 16384 + (s & 3) * 32, 0, 1024),
+                                id128, 1);
+                commit(&bars[AB_UP]);
+            }
+            commit(&bars[AB_Z]);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&bars[AB_Z], 0) && clock64() - t0 < kDefaultWaitCycles) {}
+            for (int bb = 0; bb < 2; ++bb) {
+                if (issued[bb] > waited[bb]) {
+                    const long long t1 = clock64();
+                    while (!mbar_try_wait(&bars[AB_LD0 + bb], (uint32_t)((issued[bb] >> 1) & 1)) &&
+                           clock64() - t1 < kDefaultWaitCycles) {}
+                }
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (elem) {
+        bool ok = true;
+        for (int i = 0; i < nch && ok; ++i) {
+            const int b = i & 1, c = nch - 1 - i;
+            const unsigned char *B = sm + b * AdTc::kBuf;
+            float *S = slot(c);
+            if (i > 0 && !(ok = st_wait_warp(&bars[AB_UP], (uint32_t)((i - 1) & 1), abort_flag, a.err))) break;
+            if (!(ok = st_wait_warp(&bars[AB_LD0 + b], (uint32_t)((i >> 1) & 1), abort_flag, a.err))) break;
+            fence_after_sync();
+            {
+                // dO^T [v][t] for tokens 32 hh .. + 31 into TMEM
+                const float *dO = reinterpret_cast<const float *>(B + AdTc::oDO);
+                uint32_t w0[16], w1[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    w0[j] = __float_as_uint(dO[(32 * hh + j) * 64 + (v - j0)]);
+                    w1[j] = __float_as_uint(dO[(32 * hh + 16 + j) * 64 + (v - j0)]);
+                }
+                tmem_st16(tmem + lane_off + kAdO + 32 * hh, w0);
+                tmem_st16(tmem + lane_off + kAdO + 32 * hh + 16, w1);
+                tmem_st_wait();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[AB_PRE]);
+            }
+            // dS' of this chunk (Q on entry) to the scratch, channels 64 hh .. + 63
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                const int d0 = 64 * hh + 32 * p;
+                float r[32];
+                tmem_ld32(tmem + lane_off + kAdQ + d0, r);
+                if (row_lane) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) S[L.dsx + (int64_t)(d0 + j) * V + v] = r[j];
+                }
+            }
+            if (!(ok = st_wait_warp(&bars[AB_D0 + b], (uint32_t)((i >> 1) & 1), abort_flag, a.err))) break;
+            fence_after_sync();
+            {
+                // dVt to the scratch, -dVt^T into TMEM (tokens 32 hh .. + 31)
+                float d2[32];
+                tmem_ld32(tmem + lane_off + kAdD + 32 * hh, d2);
+                uint32_t w0[16], w1[16];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (row_lane) S[L.dvt + (int64_t)(32 * hh + j) * V + v] = d2[j];
+                    if (j < 16) w0[j] = __float_as_uint(-d2[j]); else w1[j - 16] = __float_as_uint(-d2[j]);
+                }
+                tmem_st16(tmem + lane_off + kAdN + 32 * hh, w0);
+                tmem_st16(tmem + lane_off + kAdN + 32 * hh + 16, w1);
+            }
+            {
+                // Q <- Q diag(e^Gn)
+                const float *EG = reinterpret_cast<const float *>(B + AdTc::oEG);
+#pragma unroll 1
+                for (int p = 0; p < 2; ++p) {
+                    const int d0 = 64 * hh + 32 * p;
+                    float r[32];
+                    tmem_ld32(tmem + lane_off + kAdQ + d0, r);
+                    uint32_t y0[16], y1[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        y0[j] = __float_as_uint(r[j] * EG[d0 + j]);
+                        y1[j] = __float_as_uint(r[16 + j] * EG[d0 + 16 + j]);
+                    }
+                    tmem_st16(tmem + lane_off + kAdQ + d0, y0);
+                    tmem_st16(tmem + lane_off + kAdQ + d0 + 16, y1);
+                }
+            }
+            tmem_st_wait();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[AB_EL]);
+        }
+        // dh0 = Q after the first chunk (dht when there is none)
+        if (ok && nch > 0) ok = st_wait_warp(&bars[AB_UP], (uint32_t)((nch - 1) & 1), abort_flag, a.err);
+        if (ok && a.dh0 != nullptr) {
+            fence_after_sync();
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                const int d0 = 64 * hh + 32 * p;
+                float r[32];
+                tmem_ld32(tmem + lane_off + kAdQ + d0, r);
+                if (row_lane) {
+                    float *dh0 = a.dh0 + (((int64_t)n * a.H_v + h) * K) * V + v;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dh0[(int64_t)(d0 + j) * V] = r[j];
+                }
+            }
+        }
+    } else {
+        // ---- transposition: warps 5-7 and 12-15 (224 threads) ----
+        const int tt = (warp < 8 ? warp - 5 : warp - 9) * 32 + lane;
+        for (int i = 0; i < nch; ++i) {
+            const int b = i & 1, c = nch - 1 - i;
+            const float *S = slot(c);
+            if (tt == 0 && c > 0) {
+                // the next chunk's A, Qp and W into L2 while this one is staged
+                const float *Sn = slot(c - 1);
+                prefetch_l2(Sn + L.a, 64 * 64 * 4);
+                prefetch_l2(Sn + L.qp, 64 * K * 4);
+                prefetch_l2(Sn + L.wm, 64 * K * 4);
+            }
+            // A^T: element (s, t) = A[t][s]; A [64 t][64 s] as 1024 float4, t = e % 64, 4 s = 4 (e / 64)
+            {
+                float4 r[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) {
+                    const int e = tt + 224 * k;
+                    if (e < 1024) r[k] = __ldg(reinterpret_cast<const float4 *>(S + L.a) + (e & 63) * 16 + (e >> 6));
+                }
+                // the buffer's A^T (iteration i - 2) has been read by its D2
+                // (all 224 threads take the same branch, so that none is left at the named barrier)
+                if (i >= 2 && tcu::bar_or(3, 224, !st_wait(&bars[AB_D0 + b], (uint32_t)(((i >> 1) - 1) & 1), abort_flag, a.err)))
+                    break;
+                unsigned char *AT = sm + b * AdTc::kBuf + AdTc::oAT;
+#pragma unroll
+                for (int k = 0; k < 5; ++k) {
+                    const int e = tt + 224 * k;
+                    if (e < 1024) {
+                        const int t = e & 63, s0 = 4 * (e >> 6);
+                        st_kmajor(AT, 8192, s0, t, r[k].x);
+                        st_kmajor(AT, 8192, s0 + 1, t, r[k].y);
+                        st_kmajor(AT, 8192, s0 + 2, t, r[k].z);
+                        st_kmajor(AT, 8192, s0 + 3, t, r[k].w);
+                    }
+                }
+                fence_proxy_async();
+                asm volatile("bar.sync 3, 224;" ::: "memory");
+                if (tt == 0) mbar_arrive(&bars[AB_AT0 + b]);
+            }
+            // Qp^T and W^T: element (d, t) of [64 t][128 d] as 2048 float4, t = e % 64, 4 d = 4 (e / 64)
+            float4 r[10];
+#pragma unroll
+            for (int k = 0; k < 10; ++k) {
+                const int e = tt + 224 * k;
+                if (e < 2048) r[k] = __ldg(reinterpret_cast<const float4 *>(S + L.qp) + (e & 63) * 32 + (e >> 6));
+            }
+            // the single Qp^T / W^T buffer has been read by the previous update
+            if (i >= 1 && tcu::bar_or(3, 224, !st_wait(&bars[AB_UP], (uint32_t)((i - 1) & 1), abort_flag, a.err))) break;
+#pragma unroll
+            for (int k = 0; k < 10; ++k) {
+                const int e = tt + 224 * k;
+                if (e < 2048) {
+                    const int t = e & 63, d0 = 4 * (e >> 6);
+                    st_kmajor(sm + AdTc::oQpT, 16384, d0, t, r[k].x);
+                    st_kmajor(sm + AdTc::oQpT, 16384, d0 + 1, t, r[k].y);
+                    st_kmajor(sm + AdTc::oQpT, 16384, d0 + 2, t, r[k].z);
+                    st_kmajor(sm + AdTc::oQpT, 16384, d0 + 3, t, r[k].w);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 10; ++k) {
+                const int e = tt + 224 * k;
+                if (e < 2048) r[k] = __ldg(reinterpret_cast<const float4 *>(S + L.wm) + (e & 63) * 32 + (e >> 6));
+            }
+#pragma unroll
+            for (int k = 0; k < 10; ++k) {
+                const int e = tt + 224 * k;
+                if (e < 2048) {
+                    const int t = e & 63, d0 = 4 * (e >> 6);
+                    st_kmajor(sm + AdTc::oWT, 16384, d0, t, r[k].x);
+                    st_kmajor(sm + AdTc::oWT, 16384, d0 + 1, t, r[k].y);
+                    st_kmajor(sm + AdTc::oWT, 16384, d0 + 2, t, r[k].z);
+                    st_kmajor(sm + AdTc::oWT, 16384, d0 + 3, t, r[k].w);
+                }
+            }
+            fence_proxy_async();
+            asm volatile("bar.sync 3, 224;" ::: "memory");
+            if (tt == 0) mbar_arrive(&bars[AB_QW]);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tmem, kAdCols);
+    }
 }
 
 // ---- grads: every gradient of one chunk ---------------------------------------------------------
@@ -1246,8 +1605,19 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
             }
         }
         if (e == cudaSuccess) {
-            bwd_adjoint_kernel<kSplit><<<dim3(V / 64, a.H_v, a.N), kT, asmem, stream>>>(a);
-            e = cudaGetLastError();
+            CUtensorMap kbmap, domap;
+            if (!kSplit && K == 128 && V == 128 && encode_slot_map(&kbmap, a, L, L.kb, K, 32, true, windows * a.H_v) &&
+                encode_slot_map(&domap, a, L, L.dof, V, 64, false, windows * a.H_v)) {
+                e = cudaFuncSetAttribute(bwd_adjoint_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AdTc::kBytes);
+                if (e == cudaSuccess) {
+                    bwd_adjoint_tc_kernel<<<dim3(2, a.H_v, a.N), kT, AdTc::kBytes, stream>>>(a, kbmap, domap);
+                    e = cudaGetLastError();
+                }
+            } else {
+                bwd_adjoint_kernel<kSplit><<<dim3(V / 64, a.H_v, a.N), kT, asmem, stream>>>(a);
+                e = cudaGetLastError();
+            }
         }
         if (e == cudaSuccess) {
             bwd_grads_kernel<T, GATE_HEAD><<<gw, kT, gsmem, stream>>>(a);
