@@ -49,16 +49,20 @@ constexpr int kT = 512;            // threads of every backward kernel
 constexpr int kKS = 32;             // k step of the GEMM
 constexpr int kLoads = 64 * kKS / kT;  // staged elements of each operand tile per thread and k step
 
-// Per-slot scratch layout (floats). A slot holds one chunk of one unit.
+// Per-slot scratch layout (floats). A slot holds one chunk of one unit. Every array starts
+// on a multiple of 128 floats, so that the slot can be viewed as rows of 64 or 128 floats by
+// the tensor maps of the tcgen05 gradient kernel. The transposed copies (qpt, kpt, kmt: [d][t];
+// tt = T^T, tbt = diag(beta) T^T; dvtt = dVt^T [v][t]) are written only for that kernel.
 struct Lay {
-    int64_t qp, kp, km, kb, wm, gm, u, vf, dof, vt, dvt, m, a, t, eg, bt, se, dsx, total;
+    int64_t qp, kp, km, kb, wm, gm, u, vf, dof, vt, dvt, m, a, t, eg, bt, se, dsx;
+    int64_t qpt, kpt, kmt, tt, tbt, dvtt, total;
 };
 __host__ __device__ inline Lay make_lay(int K, int V) {
     Lay L;
     int64_t o = 0;
     auto take = [&](int64_t n) {
         const int64_t at = o;
-        o += (n + 63) & ~(int64_t)63;
+        o += (n + 127) & ~(int64_t)127;
         return at;
     };
     L.qp = take(64 * K); L.kp = take(64 * K); L.km = take(64 * K); L.kb = take(64 * K);
@@ -67,6 +71,8 @@ __host__ __device__ inline Lay make_lay(int K, int V) {
     L.m = take(64 * 64); L.a = take(64 * 64); L.t = take(64 * 64);
     L.eg = take(K); L.bt = take(64);
     L.se = take((int64_t)K * V); L.dsx = take((int64_t)K * V);
+    L.qpt = take(64 * K); L.kpt = take(64 * K); L.kmt = take(64 * K);
+    L.tt = take(64 * 64); L.tbt = take(64 * 64); L.dvtt = take(64 * V);
     L.total = o;
     return L;
 }
@@ -471,6 +477,29 @@ __global__ void __launch_bounds__(kT, 2) bwd_prep_kernel(const BwdArgs a) {
     }
     float *Tm = S + L.t;
     for (int e = tid; e < 4096; e += kT) Tm[e] = Tsh[(e >> 6) * 65 + (e & 63)];
+    if (a.tc) {
+        // T^T and diag(beta) T^T ([t][r], r fastest: the shared-memory reads are 65 apart)
+        for (int e = tid; e < 4096; e += kT) {
+            const int t = e >> 6, r = e & 63;
+            const float x = Tsh[r * 65 + t];
+            S[L.tt + e] = x;
+            S[L.tbt + e] = S[L.bt + t] * x;
+        }
+        // Qp^T, Kp^T, Km^T [d][t] from the row-major copies this CTA wrote above (plain
+        // loads: they were written in this kernel), t fastest so that the stores coalesce
+        for (int e = tid; e < 16 * K; e += kT) {
+            const int t = e & 63, d0 = 4 * (e >> 6);
+            const float4 x = ld4f(S + L.qp + t * K + d0), y = ld4f(S + L.kp + t * K + d0),
+                         z = ld4f(S + L.km + t * K + d0);
+            const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w}, zs[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                S[L.qpt + (d0 + j) * 64 + t] = xs[j];
+                S[L.kpt + (d0 + j) * 64 + t] = ys[j];
+                S[L.kmt + (d0 + j) * 64 + t] = zs[j];
+            }
+        }
+    }
     // W = T diag(beta) Kp, U = T diag(beta) V (the row-scaled operands were written above)
     block_gemm<SPLIT>(64, V, 64, 1.f, Tsh, 65, 1, Vbeta, V, 1, S + L.u, V, 1, false, stage);
     block_gemm<SPLIT>(64, K, 64, 1.f, Tsh, 65, 1, Kbeta, K, 1, S + L.wm, K, 1, false, stage);
@@ -1185,6 +1214,12 @@ __global__ void __launch_bounds__(kT, 1) bwd_adjoint_tc_kernel(const BwdArgs a, 
                     if (row_lane) S[L.dvt + (int64_t)(32 * hh + j) * V + v] = d2[j];
                     if (j < 16) w0[j] = __float_as_uint(-d2[j]); else w1[j - 16] = __float_as_uint(-d2[j]);
                 }
+                if (a.tc && row_lane) {
+                    // dVt^T row v, tokens 32 hh .. + 31, for the gradient kernel
+                    float4 *dst = reinterpret_cast<float4 *>(S + L.dvtt + (int64_t)v * 64 + 32 * hh);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dst[j] = make_float4(d2[4 * j], d2[4 * j + 1], d2[4 * j + 2], d2[4 * j + 3]);
+                }
                 tmem_st16(tmem + lane_off + kAdN + 32 * hh, w0);
                 tmem_st16(tmem + lane_off + kAdN + 32 * hh + 16, w1);
             }
@@ -1508,6 +1543,554 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
         for (int t = tid; t < nv; t += kT) a.dbeta[(bos + row0 + t) * a.H_v + h] = dbeta[t];
 }
 
+// ---- grads on tcgen05 (bf16 inputs, d_k = d_v = 128, with beta) -------------------------------
+// One CTA per (value head, window): every product of the chunk's gradient is a kind::tf32
+// MMA with its accumulator in TMEM. The four per-token gradients are kept transposed, as
+// [d][t] accumulators of M = 128 rows (d) and N = 64 columns (t), so that they fill TMEM's
+// lanes and the epilogue reads one channel per thread:
+//   G1   S dO^T, S dVt^T      -> dQp^T (then += Km^T dA^T), -dW^T (negated in place)
+//   G2   dS' Vt^T             -> dKb^T
+//   GA   dO Vt^T, dVt V^T     -> dA, dT (64 x 64, M = 64)
+//   dT  += dW Kp^T;  dT <- dT diag(beta), dbeta += column sums of T . dT (before the scaling)
+//   F2a  dW^T (diag(beta) T^T)^T -> dKp^T (= (diag(beta) T^T dW)^T), dv^T = dVt^T (diag(beta) T^T)^T
+//   X    dT T^T;  dL = -T^T X (strictly lower), dbeta += rows of dL . M, dM = diag(beta) dL
+//   F12b Km^T [dA; dM]^T     -> dQp^T, dKp^T (one N = 128 product)
+//   F3   [Qp^T | Kp^T] [dA^T | dM^T]^T -> dKm^T (one K = 128 product)
+// then dq, dk, dgamma and the reverse cumulative sum per channel. Operands come from the
+// scratch by TMA (128-byte swizzle, K-major: the scratch holds the transposed copies these
+// products need) or are written by the read-back warps in the same layout; four of them are
+// read from TMEM. Shared memory is five regions whose tiles follow one another as the
+// products retire (offsets in bytes):
+//   R0 [0, 64K)       S_e -> dS' -> diag(beta) T^T, dVt^T, T -> [Qp^T | Kp^T]
+//   R1 [64K, 128K)    [dVt; dO] -> [dA; dM] and [dA^T | dM^T]
+//   R2 [128K, 160K)   Vt -> T^T, X^T
+//   R3 [160K, 192K)   V -> Kp -> read-back scratch
+//   R4 [192K, 224K)   dW -> Km^T
+// and for the epilogue Qp, Kp, Km, Kb and gamma ([t][d] fp32, plain copies) over R0-R2.
+// Roles: warps 0-7 read back and run the epilogue (warp w: TMEM lanes 32 (w % 4) .., column
+// half w / 4), warp 8 lane 0 issues every copy and MMA. Each barrier completes once.
+struct GrTc {
+    static constexpr int R0 = 0, R1 = 65536, R2 = 131072, R3 = 163840, R4 = 196608;
+    // in R3 once Kp is consumed, past the read-back scratch ([64][65] floats)
+    static constexpr int oDB1 = R3 + 16896;          // dbeta, T . dT part [64]
+    static constexpr int oDB3 = oDB1 + 256;          // dbeta, dL . M part, by column half [2][64]
+    static constexpr int oDGH = oDB3 + 512;          // per-head dg [64]
+    static constexpr int oDEG = 229376;              // dEG [128]
+    static constexpr int oBar = oDEG + 512;
+    static constexpr int kBytes = oBar + 8 * 24 + 1024;  // + alignment slack
+};
+// (the kernel's static shared memory takes 1 KB of the 227 KB)
+static_assert(GrTc::kBytes <= 232448 - 1024 && GrTc::oDGH + 256 <= GrTc::R4, "shared memory");
+// TMEM columns
+constexpr uint32_t tgA = 0, tgT = 64, tgKB = 128, tgKM = 192, tgW = 256, tgQP = 320, tgKP = 384, tgV = 448;
+enum {
+    GB_LA = 0, GB_LV, GB_LDS, GB_LKP, GB_LTB, GB_LTM, GB_LTT, GB_LKMT, GB_LQ, GB_LE,  // copies
+    GB_G1, GB_GA, GB_G2, GB_DT, GB_DV, GB_X, GB_DL, GB_F,                     // MMA commits
+    GB_DW, GB_DTS, GB_XT, GB_DM,                                              // read-backs (8 warps)
+    GB_Z, kGrBars
+};
+constexpr int kGrLoads = GB_LE + 1;
+
+// The four tensor maps view a slot as rows of 128 or 64 floats; boxes of 32 floats x 64 or
+// 128 rows land as 128-byte-swizzled K-major atoms.
+struct GrMaps {
+    CUtensorMap w128r64, w128r128, w64r64, w64r128;
+};
+
+// Element (row, k) of a K-major tile of 32-column atoms `atom_bytes` apart: byte offset.
+__device__ __forceinline__ uint32_t kmaj(int atom_bytes, int row, int k) {
+    const int kk = k & 31;
+    return (uint32_t)((k >> 5) * atom_bytes + row * 128 + (((kk >> 2) ^ (row & 7)) << 4) + (kk & 3) * 4);
+}
+
+template <bool GATE_HEAD>
+__global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, const __grid_constant__ GrMaps mp) {
+    using namespace tc5;
+    using tcu::tmem_ld32;
+    using tcu::mbar_arrive;
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char *sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + GrTc::oBar);
+    float *dEG = reinterpret_cast<float *>(sm + GrTc::oDEG);
+    float *db1 = reinterpret_cast<float *>(sm + GrTc::oDB1);
+    float *db3 = reinterpret_cast<float *>(sm + GrTc::oDB3);
+    float *dgh = reinterpret_cast<float *>(sm + GrTc::oDGH);
+    __shared__ uint32_t tslot;
+    __shared__ int abort_w;
+    volatile int *abort_flag = &abort_w;
+    int n, c, len;
+    int64_t bos;
+    if (!window_owner(a, blockIdx.y, n, c, bos, len)) return;
+    constexpr int K = 128, V = 128;
+    const int h = blockIdx.x, hk = h / a.group, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Lay L = make_lay(K, V);
+    const int64_t sl = slot_of(a, bos, n, c, h);
+    const float *S = a.scratch + sl * L.total;
+    const int row0 = c * 64, nv = min(64, len - row0);
+    if (tid == 0) {
+        for (int i = 0; i < kGrBars; ++i)
+            mbar_init(&bars[i], (i >= GB_DW && i <= GB_DM) ? 8 : 1);
+        abort_w = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tslot, 512);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tslot, sb = smem_u32(sm);
+
+    if (warp == 8) {
+        if (lane > 0 && lane < 15) {
+            // everything read later into L2, one bulk prefetch per lane
+            const int64_t po[14] = {L.dsx, L.kp, L.tbt, L.dvtt, L.t, L.tt, L.kmt, L.qpt, L.kpt, L.qp, L.km, L.kb, L.gm, L.m};
+            const uint32_t pb[14] = {65536, 32768, 16384, 32768, 16384, 16384, 32768, 32768, 32768, 32768, 32768, 32768,
+                                     32768, 16384};
+            prefetch_l2(S + po[lane - 1], pb[lane - 1]);
+        }
+        if (lane == 0) {
+            bool ok = true;
+            bool armed[kGrLoads] = {}, done[kGrLoads] = {};
+            const int z = (int)sl;
+            auto arm = [&](int b, uint32_t bytes) {
+                mbar_arrive_expect_tx(&bars[b], bytes);
+                armed[b] = true;
+            };
+            auto wait_load = [&](int b) {
+                if (ok) ok = st_wait(&bars[b], 0, abort_flag, a.err);
+                if (ok) done[b] = true;
+            };
+            auto wait_bar = [&](int b) {
+                if (ok) ok = st_wait(&bars[b], 0, abort_flag, a.err);
+            };
+            // 128-float rows: S_e, [dVt; dO], Vt, V
+            arm(GB_LA, 131072);
+#pragma unroll
+            for (int at = 0; at < 4; ++at) {
+                tma_load_3d(sm + GrTc::R0 + at * 16384, &mp.w128r128, &bars[GB_LA], 32 * at, (int)(L.se / 128), z);
+                tma_load_3d(sm + GrTc::R1 + at * 16384, &mp.w128r64, &bars[GB_LA], 32 * at, (int)(L.dvt / 128), z);
+                tma_load_3d(sm + GrTc::R1 + at * 16384 + 8192, &mp.w128r64, &bars[GB_LA], 32 * at, (int)(L.dof / 128), z);
+            }
+            arm(GB_LV, 65536);
+#pragma unroll
+            for (int at = 0; at < 4; ++at) {
+                tma_load_3d(sm + GrTc::R2 + at * 8192, &mp.w128r64, &bars[GB_LV], 32 * at, (int)(L.vt / 128), z);
+                tma_load_3d(sm + GrTc::R3 + at * 8192, &mp.w128r64, &bars[GB_LV], 32 * at, (int)(L.vf / 128), z);
+            }
+            const uint32_t i128x128 = idesc_tf32(128, 128), i128x64 = idesc_tf32(128, 64), i64x64 = idesc_tf32(64, 64);
+            // G1: [ -dW^T' | dQp^T ] = S_e [dVt; dO]^T
+            wait_load(GB_LA);
+            if (ok) {
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32(tmem + tgW, tcu::dK(sb + GrTc::R0, 16384, s), tcu::dK(sb + GrTc::R1, 16384, s), i128x128,
+                             s > 0);
+                commit(&bars[GB_G1]);
+            }
+            // GA: dA = dO Vt^T, dT = dVt V^T
+            wait_load(GB_LV);
+            if (ok) {
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32(tmem + tgA, tcu::dK(sb + GrTc::R1 + 8192, 16384, s), tcu::dK(sb + GrTc::R2, 8192, s),
+                             i64x64, s > 0);
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32(tmem + tgT, tcu::dK(sb + GrTc::R1, 16384, s), tcu::dK(sb + GrTc::R3, 8192, s), i64x64,
+                             s > 0);
+                commit(&bars[GB_GA]);
+            }
+            // dS' over S_e; Kp over V
+            wait_bar(GB_G1);
+            if (ok) {
+                arm(GB_LDS, 65536);
+#pragma unroll
+                for (int at = 0; at < 4; ++at)
+                    tma_load_3d(sm + GrTc::R0 + at * 16384, &mp.w128r128, &bars[GB_LDS], 32 * at, (int)(L.dsx / 128), z);
+            }
+            wait_bar(GB_GA);
+            if (ok) {
+                arm(GB_LKP, 32768);
+#pragma unroll
+                for (int at = 0; at < 4; ++at)
+                    tma_load_3d(sm + GrTc::R3 + at * 8192, &mp.w128r64, &bars[GB_LKP], 32 * at, (int)(L.kp / 128), z);
+            }
+            // G2: dKb^T = dS' Vt^T
+            wait_load(GB_LDS);
+            if (ok) {
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32(tmem + tgKB, tcu::dK(sb + GrTc::R0, 16384, s), tcu::dK(sb + GrTc::R2, 8192, s), i128x64,
+                             s > 0);
+                commit(&bars[GB_G2]);
+            }
+            // dT += dW Kp^T
+            wait_bar(GB_DW);
+            wait_load(GB_LKP);
+            if (ok) {
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32(tmem + tgT, tcu::dK(sb + GrTc::R4, 8192, s), tcu::dK(sb + GrTc::R3, 8192, s), i64x64, 1);
+                commit(&bars[GB_DT]);
+            }
+            // diag(beta) T^T, dVt^T, T over dS'; T^T over Vt
+            wait_bar(GB_G2);
+            if (ok) {
+                arm(GB_LTB, 49152);
+                arm(GB_LTM, 16384);
+                arm(GB_LTT, 16384);
+#pragma unroll
+                for (int at = 0; at < 2; ++at) {
+                    tma_load_3d(sm + GrTc::R0 + at * 8192, &mp.w64r64, &bars[GB_LTB], 32 * at, (int)(L.tbt / 64), z);
+                    tma_load_3d(sm + GrTc::R0 + 16384 + at * 16384, &mp.w64r128, &bars[GB_LTB], 32 * at,
+                                (int)(L.dvtt / 64), z);
+                    tma_load_3d(sm + GrTc::R0 + 49152 + at * 8192, &mp.w64r64, &bars[GB_LTM], 32 * at, (int)(L.t / 64), z);
+                    tma_load_3d(sm + GrTc::R2 + at * 8192, &mp.w64r64, &bars[GB_LTT], 32 * at, (int)(L.tt / 64), z);
+                }
+            }
+            // F2a: dKp^T = dW^T (diag(beta) T^T)^T (A: dW^T in TMEM); dv^T = dVt^T (diag(beta) T^T)^T
+            wait_load(GB_LTB);
+            if (ok) {
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32_ts(tmem + tgKP, tmem + tgW + 8 * s, tcu::dK(sb + GrTc::R0, 8192, s), i128x64, s > 0);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32(tmem + tgV, tcu::dK(sb + GrTc::R0 + 16384, 16384, s), tcu::dK(sb + GrTc::R0, 8192, s),
+                             i128x64, s > 0);
+                commit(&bars[GB_DV]);
+            }
+            // Km^T over dW
+            wait_bar(GB_DT);
+            if (ok) {
+                arm(GB_LKMT, 32768);
+#pragma unroll
+                for (int at = 0; at < 2; ++at)
+                    tma_load_3d(sm + GrTc::R4 + at * 16384, &mp.w64r128, &bars[GB_LKMT], 32 * at, (int)(L.kmt / 64), z);
+            }
+            // X = dT T^T (A: the scaled dT in TMEM)
+            wait_bar(GB_DTS);
+            wait_load(GB_LTM);
+            if (ok) {
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32_ts(tmem + tgA, tmem + tgT + 8 * s, tcu::dK(sb + GrTc::R0 + 49152, 8192, s), i64x64, s > 0);
+                commit(&bars[GB_X]);
+            }
+            // [Qp^T | Kp^T] over diag(beta) T^T, dVt^T and T
+            wait_bar(GB_X);
+            wait_bar(GB_DV);
+            if (ok) {
+                arm(GB_LQ, 65536);
+#pragma unroll
+                for (int at = 0; at < 2; ++at) {
+                    tma_load_3d(sm + GrTc::R0 + at * 16384, &mp.w64r128, &bars[GB_LQ], 32 * at, (int)(L.qpt / 64), z);
+                    tma_load_3d(sm + GrTc::R0 + 32768 + at * 16384, &mp.w64r128, &bars[GB_LQ], 32 * at,
+                                (int)(L.kpt / 64), z);
+                }
+            }
+            // T^T X (dL = minus its strict lower part)
+            wait_bar(GB_XT);
+            wait_load(GB_LTT);
+            if (ok) {
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32(tmem + tgA, tcu::dK(sb + GrTc::R2, 8192, s), tcu::dK(sb + GrTc::R2 + 16384, 8192, s), i64x64,
+                             s > 0);
+                commit(&bars[GB_DL]);
+            }
+            // F12b: [dQp^T | dKp^T] += Km^T [dA; dM]^T;  F3: dKm^T = [Qp^T | Kp^T] [dA^T | dM^T]^T
+            wait_bar(GB_DM);
+            wait_load(GB_LKMT);
+            wait_load(GB_LQ);
+            if (ok) {
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32(tmem + tgQP, tcu::dK(sb + GrTc::R4, 16384, s), tcu::dK(sb + GrTc::R1, 16384, s), i128x128, 1);
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    mma_tf32(tmem + tgKM, tcu::dK(sb + GrTc::R0, 16384, s), tcu::dK(sb + GrTc::R1 + 32768, 8192, s),
+                             i128x64, s > 0);
+                commit(&bars[GB_F]);
+            }
+            // the epilogue's operands over the retired tiles
+            wait_bar(GB_F);
+            if (ok) {
+                arm(GB_LE, 5 * 32768);
+                const int64_t eo[5] = {L.qp, L.kp, L.km, L.kb, L.gm};
+#pragma unroll
+                for (int i = 0; i < 5; ++i)
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            sb + GrTc::R0 + 32768 * i),
+                        "l"(S + eo[i]), "r"(32768), "r"(smem_u32(&bars[GB_LE]))
+                        : "memory");
+            }
+            // drain: every MMA issued, every copy armed
+            commit(&bars[GB_Z]);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&bars[GB_Z], 0) && clock64() - t0 < kDefaultWaitCycles) {}
+            for (int b = 0; b < kGrLoads; ++b) {
+                if (armed[b] && !done[b]) {
+                    const long long t1 = clock64();
+                    while (!mbar_try_wait(&bars[b], 0) && clock64() - t1 < kDefaultWaitCycles) {}
+                }
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else {
+        // ---- read-back and epilogue: warps 0-7 ----
+        const int q = warp & 3, hw = warp >> 2;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const int t16 = 16 * q + (lane & 15);  // row of an M = 64 accumulator (lanes 0-15)
+        const bool rl = lane < 16;
+        const int dch = 32 * q + lane;          // row of an M = 128 accumulator
+        const float *Bt = S + L.bt;
+        bool ok = true;
+        auto arrive = [&](int b) {
+            fence_proxy_async();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[b]);
+        };
+        // every wait of the 256 threads ends the same way for all of them (named barrier 1)
+        auto wait_all = [&](int b) { return !tcu::bar_or(1, 256, !st_wait(&bars[b], 0, abort_flag, a.err)); };
+        do {
+            // R1: -dW^T' -> dW^T in place (the A operand of F2a) and dW [t][d] into R4
+            if (!(ok = wait_all(GB_G1))) break;
+            fence_after_sync();
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tgW + 32 * hw, v);
+                uint32_t w0[16], w1[16];
+                unsigned char *DW = sm + GrTc::R4;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float x = -v[j];
+                    if (j < 16) w0[j] = __float_as_uint(x); else w1[j - 16] = __float_as_uint(x);
+                    *reinterpret_cast<uint32_t *>(DW + kmaj(8192, 32 * hw + j, dch)) = tcu::tf32(x);
+                }
+                tmem_st16(tmem + lane_off + tgW + 32 * hw, w0);
+                tmem_st16(tmem + lane_off + tgW + 32 * hw + 16, w1);
+                tmem_st_wait();
+            }
+            arrive(GB_DW);
+            // dA (lower, with the diagonal) -> [dA; .] rows 0-63 and [dA^T | .] atoms 0-1 in R1
+            if (!(ok = wait_all(GB_GA))) break;
+            fence_after_sync();
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tgA + 32 * hw, v);
+                if (rl) {
+                    unsigned char *AM = sm + GrTc::R1, *AMT = sm + GrTc::R1 + 32768;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int s2 = 32 * hw + j;
+                        const float x = s2 <= t16 ? v[j] : 0.f;
+                        *reinterpret_cast<uint32_t *>(AM + kmaj(16384, t16, s2)) = tcu::tf32(x);
+                        *reinterpret_cast<uint32_t *>(AMT + kmaj(8192, s2, t16)) = tcu::tf32(x);
+                    }
+                }
+            }
+            // dT: dbeta += column sums of T . dT, then dT <- dT diag(beta) in place
+            if (!(ok = wait_all(GB_DT))) break;
+            if (!(ok = wait_all(GB_LTM))) break;
+            fence_after_sync();
+            if (tid < 64) dgh[tid] = 0.f;  // R3 is free of Kp now
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tgT + 32 * hw, v);
+                float *P = reinterpret_cast<float *>(sm + GrTc::R3);  // [64 r][65]
+                const unsigned char *TM = sm + GrTc::R0 + 49152;
+                uint32_t w0[16], w1[16];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int s2 = 32 * hw + j;
+                    if (rl) P[t16 * 65 + s2] = v[j] * *reinterpret_cast<const float *>(TM + kmaj(8192, t16, s2));
+                    const float y = v[j] * __ldg(Bt + s2);
+                    if (j < 16) w0[j] = __float_as_uint(y); else w1[j - 16] = __float_as_uint(y);
+                }
+                tmem_st16(tmem + lane_off + tgT + 32 * hw, w0);
+                tmem_st16(tmem + lane_off + tgT + 32 * hw + 16, w1);
+                tmem_st_wait();
+            }
+            arrive(GB_DTS);
+            tcu::bar_named(1, 256);  // P is complete
+            if (tid < 64) {
+                float acc = 0.f;
+                const float *P = reinterpret_cast<const float *>(sm + GrTc::R3);
+                for (int r = 0; r < 64; ++r) acc += P[r * 65 + tid];
+                db1[tid] = acc;
+            }
+            // dv = rows of dv^T, bf16
+            if (!(ok = wait_all(GB_DV))) break;
+            fence_after_sync();
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tgV + 32 * hw, v);
+                __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * hw + j;
+                    if (t < nv) dv[(bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + dch] = __float2bfloat16_rn(v[j]);
+                }
+            }
+            // X -> X^T into R2 (after T^T)
+            if (!(ok = wait_all(GB_X))) break;
+            fence_after_sync();
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tgA + 32 * hw, v);
+                if (rl) {
+                    unsigned char *XT = sm + GrTc::R2 + 16384;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        *reinterpret_cast<uint32_t *>(XT + kmaj(8192, 32 * hw + j, t16)) = tcu::tf32(v[j]);
+                }
+            }
+            arrive(GB_XT);
+            // dL = -(T^T X) strictly lower: dbeta += rows of dL . M; dM = diag(beta) dL
+            if (!(ok = wait_all(GB_DL))) break;
+            fence_after_sync();
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tgA + 32 * hw, v);
+                if (rl) {
+                    unsigned char *AM = sm + GrTc::R1, *AMT = sm + GrTc::R1 + 32768;
+                    const float bt = __ldg(Bt + t16);
+                    const float4 *Mr = reinterpret_cast<const float4 *>(S + L.m + t16 * 64 + 32 * hw);
+                    float part = 0.f;
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 m4 = __ldg(Mr + j4);
+                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = 4 * j4 + jj, s2 = 32 * hw + j;
+                            const float dl = s2 < t16 ? -v[j] : 0.f;
+                            part = fmaf(dl, mm[jj], part);
+                            const float dm = bt * dl;
+                            *reinterpret_cast<uint32_t *>(AM + kmaj(16384, 64 + t16, s2)) = tcu::tf32(dm);
+                            *reinterpret_cast<uint32_t *>(AMT + kmaj(8192, s2, 64 + t16)) = tcu::tf32(dm);
+                        }
+                    }
+                    db3[hw * 64 + t16] = part;
+                }
+            }
+            arrive(GB_DM);
+            // ---- epilogue ----
+            if (!(ok = wait_all(GB_F))) break;
+            fence_after_sync();
+            // dEG[d] = rows of dS' . S_e (a warp per row, eight rows' loads in flight), while
+            // the epilogue's tiles land
+#pragma unroll 1
+            for (int d0 = 8 * warp; d0 < K; d0 += 64) {
+                float4 x[8], y[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    x[i] = __ldg(reinterpret_cast<const float4 *>(S + L.dsx + (d0 + i) * V) + lane);
+                    y[i] = __ldg(reinterpret_cast<const float4 *>(S + L.se + (d0 + i) * V) + lane);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float sdot = warp_sum(x[i].x * y[i].x + x[i].y * y[i].y + x[i].z * y[i].z + x[i].w * y[i].w);
+                    if (lane == 0) dEG[d0 + i] = sdot;
+                }
+            }
+            if (!(ok = wait_all(GB_LE))) break;
+            const float *Eq = reinterpret_cast<const float *>(sm + GrTc::R0);
+            const float *Ekp = Eq + 8192, *Ekm = Eq + 16384, *Ekb = Eq + 24576, *Egm = Eq + 32768;
+            const float gn = Egm[63 * K + dch];
+            float dgam[32];
+            float kbsum = 0.f;
+            float *dqa = a.dq_acc, *dka = a.dk_acc;
+            __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dq), *dk = static_cast<__nv_bfloat16 *>(a.dk);
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                const int tb = 32 * hw + 16 * p;
+                float vq[16], vkp[16], vkm[16], vkb[16];
+                tcu::tmem_ld16(tmem + lane_off + tgQP + tb, vq);
+                tcu::tmem_ld16(tmem + lane_off + tgKP + tb, vkp);
+                tcu::tmem_ld16(tmem + lane_off + tgKM + tb, vkm);
+                tcu::tmem_ld16(tmem + lane_off + tgKB + tb, vkb);
+                tcu::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = tb + j;
+                    const int e = t * K + dch;
+                    const float qp = Eq[e], kp = Ekp[e], km = Ekm[e], kb = Ekb[e], gm = Egm[e];
+                    const float ep = expf(gm), em = expf(-gm), eb = expf(gn - gm);
+                    const float gq = a.scale * ep * vq[j];
+                    const float gk = ep * vkp[j] + em * vkm[j] + eb * vkb[j];
+                    dgam[16 * p + j] = vq[j] * qp + vkp[j] * kp - vkm[j] * km - vkb[j] * kb;
+                    kbsum = fmaf(vkb[j], kb, kbsum);
+                    if (t < nv) {
+                        const int64_t o = ((bos + row0 + t) * a.H_k + hk) * K + dch;
+                        if (a.direct_qk) {
+                            dq[o] = __float2bfloat16_rn(gq);
+                            dk[o] = __float2bfloat16_rn(gk);
+                        } else {
+                            atomicAdd(dqa + o, gq);
+                            atomicAdd(dka + o, gk);
+                        }
+                    }
+                }
+            }
+            // dGn and the reverse cumulative sum over the two column halves (exchange in R3)
+            float *ex = reinterpret_cast<float *>(sm + GrTc::R3);  // [2][128] kb sums, [128] dgamma totals
+            float tot = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tot += dgam[j];
+            ex[hw * 128 + dch] = kbsum;
+            if (hw == 1) ex[256 + dch] = tot;
+            tcu::bar_named(1, 256);
+            float acc = ex[dch] + ex[128 + dch] + dEG[dch] * __ldg(S + L.eg + dch);  // dGn
+            if (hw == 0) acc += ex[256 + dch];
+            float dgo[32];
+#pragma unroll
+            for (int j = 31; j >= 0; --j) {
+                acc += dgam[j];
+                dgo[j] = acc;
+            }
+            if (!GATE_HEAD) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * hw + j;
+                    if (t < nv) a.dg[((bos + row0 + t) * a.H_v + h) * K + dch] = dgo[j];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float sdot = warp_sum(dgo[j]);
+                    if (lane == 0) atomicAdd(&dgh[32 * hw + j], sdot);
+                }
+            }
+            tcu::bar_named(1, 256);  // dgh and every dbeta part are complete
+            if (tid < 64 && tid < nv) {
+                const int t = tid;
+                if (GATE_HEAD) a.dg[(bos + row0 + t) * a.H_v + h] = dgh[t];
+                if (a.dbeta != nullptr) a.dbeta[(bos + row0 + t) * a.H_v + h] = db1[t] + db3[t] + db3[64 + t];
+            }
+        } while (false);
+        if (!ok) *abort_flag = 1;
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kT) bwd_finish_kernel(const float *acc, T *out, int64_t n) {
     for (int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x; i < n; i += (int64_t)gridDim.x * kT)
@@ -1533,6 +2116,20 @@ bool encode_slot_map(CUtensorMap *m, const BwdArgs &a, const Lay &L, int64_t off
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(a.scratch + off), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The slot viewed as rows of `width` floats (64 or 128), boxes of 32 floats x `rows` rows,
+// 128-byte swizzle (the gradient kernel's operand tiles).
+bool encode_view(CUtensorMap *m, const BwdArgs &a, const Lay &L, int width, int rows, int64_t nslots) {
+    auto enc = tcu::tensor_map_encoder();
+    if (enc == nullptr || nslots <= 0 || L.total % width != 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)(L.total / width), (cuuint64_t)nslots};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * sizeof(float), (cuuint64_t)L.total * sizeof(float)};
+    const cuuint32_t box[3] = {32, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.scratch, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename T, bool GATE_HEAD>
@@ -1587,12 +2184,25 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
         e = cudaFuncSetAttribute(bwd_adjoint_kernel<kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)asmem);
     if (e == cudaSuccess && windows > 0 && Ttot > 0) {
         const dim3 gw(a.H_v, (unsigned)windows);
+        // tcgen05 scans for bf16 inputs with d = 128; the tcgen05 gradient kernel with them
+        // when beta is given
+        const int64_t nslots = windows * a.H_v;
+        CUtensorMap wmap, umap, kbmap, domap;
+        GrMaps gmaps;
+        const bool scan_tc = !kSplit && K == 128 && V == 128 &&
+                             encode_slot_map(&wmap, a, L, L.wm, K, 32, true, nslots) &&
+                             encode_slot_map(&umap, a, L, L.u, V, 64, false, nslots) &&
+                             encode_slot_map(&kbmap, a, L, L.kb, K, 32, true, nslots) &&
+                             encode_slot_map(&domap, a, L, L.dof, V, 64, false, nslots);
+        const bool grads_tc = scan_tc && !a.decay_only && encode_view(&gmaps.w128r64, a, L, 128, 64, nslots) &&
+                              encode_view(&gmaps.w128r128, a, L, 128, 128, nslots) &&
+                              encode_view(&gmaps.w64r64, a, L, 64, 64, nslots) &&
+                              encode_view(&gmaps.w64r128, a, L, 64, 128, nslots);
+        a.tc = grads_tc ? 1 : 0;
         bwd_prep_kernel<T, GATE_HEAD><<<gw, kT, psmem, stream>>>(a);
         e = cudaGetLastError();
         if (e == cudaSuccess) {
-            CUtensorMap wmap, umap;
-            if (!kSplit && K == 128 && V == 128 && encode_slot_map(&wmap, a, L, L.wm, K, 32, true, windows * a.H_v) &&
-                encode_slot_map(&umap, a, L, L.u, V, 64, false, windows * a.H_v)) {
+            if (scan_tc) {
                 e = cudaFuncSetAttribute(bwd_states_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          StTc::kBytes);
                 if (e == cudaSuccess) {
@@ -1605,9 +2215,7 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
             }
         }
         if (e == cudaSuccess) {
-            CUtensorMap kbmap, domap;
-            if (!kSplit && K == 128 && V == 128 && encode_slot_map(&kbmap, a, L, L.kb, K, 32, true, windows * a.H_v) &&
-                encode_slot_map(&domap, a, L, L.dof, V, 64, false, windows * a.H_v)) {
+            if (scan_tc) {
                 e = cudaFuncSetAttribute(bwd_adjoint_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          AdTc::kBytes);
                 if (e == cudaSuccess) {
@@ -1620,8 +2228,17 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
             }
         }
         if (e == cudaSuccess) {
-            bwd_grads_kernel<T, GATE_HEAD><<<gw, kT, gsmem, stream>>>(a);
-            e = cudaGetLastError();
+            if (grads_tc) {
+                e = cudaFuncSetAttribute(bwd_grads_tc_kernel<GATE_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GrTc::kBytes);
+                if (e == cudaSuccess) {
+                    bwd_grads_tc_kernel<GATE_HEAD><<<gw, 288, GrTc::kBytes, stream>>>(a, gmaps);
+                    e = cudaGetLastError();
+                }
+            } else {
+                bwd_grads_kernel<T, GATE_HEAD><<<gw, kT, gsmem, stream>>>(a);
+                e = cudaGetLastError();
+            }
         }
         if (e == cudaSuccess && own_acc && acc_elems > 0) {
             const int grid = (int)std::min<int64_t>((int64_t)sms * 8, ((int64_t)acc_elems + kT - 1) / kT);

@@ -20,6 +20,8 @@ struct BwdArgs {
     float *scratch;            // per-chunk factors (set by the launcher)
     float *dq_acc, *dk_acc;    // fp32 accumulators of dq, dk (set by the launcher)
     int direct_qk;             // one value head per key head: dq, dk written directly
+    int tc;                    // the tcgen05 gradient kernel runs: prep and the adjoint scan
+                               // also write the transposed factors it reads
     unsigned int *err;         // device error word (KDA_DEVICE_ERR_*)
 };
 
