@@ -673,8 +673,8 @@ struct StTc {
 constexpr uint32_t kStR = 0, kStD = 128, kStV = 192, kStCols = 256;  // TMEM columns
 enum { SB_LD0 = 0, SB_LD1, SB_KB0, SB_KB1, SB_D1, SB_UP0, SB_UP1, SB_EL, SB_Z, kStBars };
 
-__device__ bool st_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, unsigned int *err) {
-    if (tc5::mbar_try_wait(bar, parity)) return true;
+// (the slow path out of line: the waits of a kernel share one copy of it)
+__device__ __noinline__ bool st_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag, unsigned int *err) {
     const long long t0 = clock64();
     while (!tc5::mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
@@ -685,6 +685,9 @@ __device__ bool st_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag
         }
     }
     return true;
+}
+__device__ __forceinline__ bool st_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, unsigned int *err) {
+    return tc5::mbar_try_wait(bar, parity) || st_wait_slow(bar, parity, abort_flag, err);
 }
 // Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
@@ -1549,47 +1552,69 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
 // [d][t] accumulators of M = 128 rows (d) and N = 64 columns (t), so that they fill TMEM's
 // lanes and the epilogue reads one channel per thread:
 //   G1   S dO^T, S dVt^T      -> dQp^T (then += Km^T dA^T), -dW^T (negated in place)
-//   G2   dS' Vt^T             -> dKb^T
 //   GA   dO Vt^T, dVt V^T     -> dA, dT (64 x 64, M = 64)
 //   dT  += dW Kp^T;  dT <- dT diag(beta), dbeta += column sums of T . dT (before the scaling)
-//   F2a  dW^T (diag(beta) T^T)^T -> dKp^T (= (diag(beta) T^T dW)^T), dv^T = dVt^T (diag(beta) T^T)^T
 //   X    dT T^T;  dL = -T^T X (strictly lower), dbeta += rows of dL . M, dM = diag(beta) dL
 //   F12b Km^T [dA; dM]^T     -> dQp^T, dKp^T (one N = 128 product)
 //   F3   [Qp^T | Kp^T] [dA^T | dM^T]^T -> dKm^T (one K = 128 product)
+// and, off that chain,
+//   G2   dS' Vt^T             -> dKb^T
+//   F2a  dW^T (diag(beta) T^T)^T -> dKp^T (= (diag(beta) T^T dW)^T), dv^T = dVt^T (diag(beta) T^T)^T
 // then dq, dk, dgamma and the reverse cumulative sum per channel. Operands come from the
 // scratch by TMA (128-byte swizzle, K-major: the scratch holds the transposed copies these
-// products need) or are written by the read-back warps in the same layout; four of them are
+// products need) or are written by the read-back warps in the same layout; two of them are
 // read from TMEM. Shared memory is five regions whose tiles follow one another as the
 // products retire (offsets in bytes):
-//   R0 [0, 64K)       S_e -> dS' -> diag(beta) T^T, dVt^T, T -> [Qp^T | Kp^T]
+//   R0 [0, 64K)       S_e -> dS' -> diag(beta) T^T, dVt^T -> [Qp^T | Kp^T]
 //   R1 [64K, 128K)    [dVt; dO] -> [dA; dM] and [dA^T | dM^T]
-//   R2 [128K, 160K)   Vt -> T^T, X^T
-//   R3 [160K, 192K)   V -> Kp -> read-back scratch
-//   R4 [192K, 224K)   dW -> Km^T
-// and for the epilogue Qp, Kp, Km, Kb and gamma ([t][d] fp32, plain copies) over R0-R2.
+//   R2 [128K, 160K)   Vt -> X^T (upper half) -> Km^T
+//   R3 [160K, 192K)   V -> Kp -> T, T^T -> gamma [t][d]
+//   R4 [192K, 224K)   dW -> read-back scratch, dbeta parts, exchanges
+// and Kb [t][d] over [dA; dM] for the epilogue, which reads Qp, Kp and Km from the K-major
+// tiles of the last products.
 // Roles: warps 0-7 read back and run the epilogue (warp w: TMEM lanes 32 (w % 4) .., column
-// half w / 4), warp 8 lane 0 issues every copy and MMA. Each barrier completes once.
+// half w / 4); warp 8 lane 0 issues every copy and MMA, the chain's products first. Each
+// barrier completes once. (Bulk L2 prefetches of the later operands, issued early from a warp
+// of their own, made the kernel slower: they delay the copies issued after them.)
+// n tf32 MMAs along K (8 elements each) into D: A and B K-major in shared memory with their
+// 32-element atoms a_atom / b_atom bytes apart (mma_run_ss), or A in TMEM, 8 columns per step
+// (mma_run_ts); the first one overwrites D unless acc. Out of line: one copy serves every
+// product of the kernel.
+__device__ __noinline__ void mma_run_ss(uint32_t d, uint32_t a, uint32_t a_atom, uint32_t b, uint32_t b_atom,
+                                        uint32_t idesc, int n, bool acc) {
+#pragma unroll 1
+    for (int s = 0; s < n; ++s) tc5::mma_tf32(d, tcu::dK(a, a_atom, s), tcu::dK(b, b_atom, s), idesc, acc || s > 0);
+}
+__device__ __noinline__ void mma_run_ts(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t b_atom, uint32_t idesc, int n,
+                                        bool acc) {
+#pragma unroll 1
+    for (int s = 0; s < n; ++s) tc5::mma_tf32_ts(d, a_tmem + 8 * s, tcu::dK(b, b_atom, s), idesc, acc || s > 0);
+}
+
 struct GrTc {
     static constexpr int R0 = 0, R1 = 65536, R2 = 131072, R3 = 163840, R4 = 196608;
-    // in R3 once Kp is consumed, past the read-back scratch ([64][65] floats)
-    static constexpr int oDB1 = R3 + 16896;          // dbeta, T . dT part [64]
+    // in R4 once dW is consumed, past the read-back scratch ([64][65] floats)
+    static constexpr int oDB1 = R4 + 16896;          // dbeta, T . dT part [64]
     static constexpr int oDB3 = oDB1 + 256;          // dbeta, dL . M part, by column half [2][64]
     static constexpr int oDGH = oDB3 + 512;          // per-head dg [64]
     static constexpr int oDEG = 229376;              // dEG [128]
     static constexpr int oBar = oDEG + 512;
-    static constexpr int kBytes = oBar + 8 * 24 + 1024;  // + alignment slack
+    static constexpr int oBT = oBar + 8 * 24;        // beta [64]
+    static constexpr int kBytes = oBT + 256 + 1024;  // + alignment slack
 };
 // (the kernel's static shared memory takes 1 KB of the 227 KB)
-static_assert(GrTc::kBytes <= 232448 - 1024 && GrTc::oDGH + 256 <= GrTc::R4, "shared memory");
+static_assert(GrTc::kBytes <= 232448 - 1024 && GrTc::oDGH + 256 <= GrTc::oDEG, "shared memory");
+constexpr int kGrThreads = 288;
 // TMEM columns
 constexpr uint32_t tgA = 0, tgT = 64, tgKB = 128, tgKM = 192, tgW = 256, tgQP = 320, tgKP = 384, tgV = 448;
 enum {
-    GB_LA = 0, GB_LV, GB_LDS, GB_LKP, GB_LTB, GB_LTM, GB_LTT, GB_LKMT, GB_LQ, GB_LE,  // copies
-    GB_G1, GB_GA, GB_G2, GB_DT, GB_DV, GB_X, GB_DL, GB_F,                     // MMA commits
-    GB_DW, GB_DTS, GB_XT, GB_DM,                                              // read-backs (8 warps)
+    GB_LA = 0, GB_LV, GB_LDS, GB_LKP, GB_LTB, GB_LTM, GB_LKMT, GB_LQ, GB_LG, GB_LKB,  // copies
+    GB_G1, GB_GT, GB_GA, GB_G2, GB_DT, GB_DV, GB_X, GB_DL, GB_F,              // MMA commits
+    GB_DW, GB_DTS, GB_XT, GB_DM,                                       // read-backs (8 warps)
     GB_Z, kGrBars
 };
-constexpr int kGrLoads = GB_LE + 1;
+constexpr int kGrLoads = GB_LKB + 1;
+static_assert(kGrBars <= 24, "barrier area");
 
 // The four tensor maps view a slot as rows of 128 or 64 floats; boxes of 32 floats x 64 or
 // 128 rows land as 128-byte-swizzled K-major atoms.
@@ -1604,7 +1629,8 @@ __device__ __forceinline__ uint32_t kmaj(int atom_bytes, int row, int k) {
 }
 
 template <bool GATE_HEAD>
-__global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, const __grid_constant__ GrMaps mp) {
+__global__ void __launch_bounds__(kGrThreads, 1) bwd_grads_tc_kernel(const BwdArgs a,
+                                                                      const __grid_constant__ GrMaps mp) {
     using namespace tc5;
     using tcu::tmem_ld32;
     using tcu::mbar_arrive;
@@ -1643,13 +1669,6 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
     const uint32_t tmem = tslot, sb = smem_u32(sm);
 
     if (warp == 8) {
-        if (lane > 0 && lane < 15) {
-            // everything read later into L2, one bulk prefetch per lane
-            const int64_t po[14] = {L.dsx, L.kp, L.tbt, L.dvtt, L.t, L.tt, L.kmt, L.qpt, L.kpt, L.qp, L.km, L.kb, L.gm, L.m};
-            const uint32_t pb[14] = {65536, 32768, 16384, 32768, 16384, 16384, 32768, 32768, 32768, 32768, 32768, 32768,
-                                     32768, 16384};
-            prefetch_l2(S + po[lane - 1], pb[lane - 1]);
-        }
         if (lane == 0) {
             bool ok = true;
             bool armed[kGrLoads] = {}, done[kGrLoads] = {};
@@ -1680,27 +1699,19 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                 tma_load_3d(sm + GrTc::R3 + at * 8192, &mp.w128r64, &bars[GB_LV], 32 * at, (int)(L.vf / 128), z);
             }
             const uint32_t i128x128 = idesc_tf32(128, 128), i128x64 = idesc_tf32(128, 64), i64x64 = idesc_tf32(64, 64);
-            // G1: [ -dW^T' | dQp^T ] = S_e [dVt; dO]^T
+            // G1: [ -dW^T | dQp^T ] = S_e [dVt; dO]^T
             wait_load(GB_LA);
             if (ok) {
                 fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    mma_tf32(tmem + tgW, tcu::dK(sb + GrTc::R0, 16384, s), tcu::dK(sb + GrTc::R1, 16384, s), i128x128,
-                             s > 0);
+                mma_run_ss(tmem + tgW, sb + GrTc::R0, 16384, sb + GrTc::R1, 16384, i128x128, 16, false);
                 commit(&bars[GB_G1]);
             }
-            // GA: dA = dO Vt^T, dT = dVt V^T
+            // dT = dVt V^T (V is then free for Kp), dA = dO Vt^T
             wait_load(GB_LV);
             if (ok) {
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    mma_tf32(tmem + tgA, tcu::dK(sb + GrTc::R1 + 8192, 16384, s), tcu::dK(sb + GrTc::R2, 8192, s),
-                             i64x64, s > 0);
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    mma_tf32(tmem + tgT, tcu::dK(sb + GrTc::R1, 16384, s), tcu::dK(sb + GrTc::R3, 8192, s), i64x64,
-                             s > 0);
+                mma_run_ss(tmem + tgT, sb + GrTc::R1, 16384, sb + GrTc::R3, 8192, i64x64, 16, false);
+                commit(&bars[GB_GT]);
+                mma_run_ss(tmem + tgA, sb + GrTc::R1 + 8192, 16384, sb + GrTc::R2, 8192, i64x64, 16, false);
                 commit(&bars[GB_GA]);
             }
             // dS' over S_e; Kp over V
@@ -1711,81 +1722,71 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                 for (int at = 0; at < 4; ++at)
                     tma_load_3d(sm + GrTc::R0 + at * 16384, &mp.w128r128, &bars[GB_LDS], 32 * at, (int)(L.dsx / 128), z);
             }
-            wait_bar(GB_GA);
+            wait_bar(GB_GT);
             if (ok) {
                 arm(GB_LKP, 32768);
 #pragma unroll
                 for (int at = 0; at < 4; ++at)
                     tma_load_3d(sm + GrTc::R3 + at * 8192, &mp.w128r64, &bars[GB_LKP], 32 * at, (int)(L.kp / 128), z);
             }
-            // G2: dKb^T = dS' Vt^T
-            wait_load(GB_LDS);
-            if (ok) {
-                fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    mma_tf32(tmem + tgKB, tcu::dK(sb + GrTc::R0, 16384, s), tcu::dK(sb + GrTc::R2, 8192, s), i128x64,
-                             s > 0);
-                commit(&bars[GB_G2]);
-            }
             // dT += dW Kp^T
             wait_bar(GB_DW);
             wait_load(GB_LKP);
             if (ok) {
                 fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    mma_tf32(tmem + tgT, tcu::dK(sb + GrTc::R4, 8192, s), tcu::dK(sb + GrTc::R3, 8192, s), i64x64, 1);
+                mma_run_ss(tmem + tgT, sb + GrTc::R4, 8192, sb + GrTc::R3, 8192, i64x64, 16, true);
                 commit(&bars[GB_DT]);
             }
-            // diag(beta) T^T, dVt^T, T over dS'; T^T over Vt
+            // G2: dKb^T = dS' Vt^T (runs while dT is read back)
+            wait_load(GB_LDS);
+            if (ok) {
+                mma_run_ss(tmem + tgKB, sb + GrTc::R0, 16384, sb + GrTc::R2, 8192, i128x64, 16, false);
+                commit(&bars[GB_G2]);
+            }
+            // T and T^T over Kp
+            wait_bar(GB_DT);
+            if (ok) {
+                arm(GB_LTM, 32768);
+#pragma unroll
+                for (int at = 0; at < 2; ++at) {
+                    tma_load_3d(sm + GrTc::R3 + at * 8192, &mp.w64r64, &bars[GB_LTM], 32 * at, (int)(L.t / 64), z);
+                    tma_load_3d(sm + GrTc::R3 + 16384 + at * 8192, &mp.w64r64, &bars[GB_LTM], 32 * at, (int)(L.tt / 64), z);
+                }
+            }
+            // diag(beta) T^T and dVt^T over dS'
             wait_bar(GB_G2);
             if (ok) {
                 arm(GB_LTB, 49152);
-                arm(GB_LTM, 16384);
-                arm(GB_LTT, 16384);
 #pragma unroll
                 for (int at = 0; at < 2; ++at) {
                     tma_load_3d(sm + GrTc::R0 + at * 8192, &mp.w64r64, &bars[GB_LTB], 32 * at, (int)(L.tbt / 64), z);
                     tma_load_3d(sm + GrTc::R0 + 16384 + at * 16384, &mp.w64r128, &bars[GB_LTB], 32 * at,
                                 (int)(L.dvtt / 64), z);
-                    tma_load_3d(sm + GrTc::R0 + 49152 + at * 8192, &mp.w64r64, &bars[GB_LTM], 32 * at, (int)(L.t / 64), z);
-                    tma_load_3d(sm + GrTc::R2 + at * 8192, &mp.w64r64, &bars[GB_LTT], 32 * at, (int)(L.tt / 64), z);
                 }
+            }
+            // X = dT T^T (A: the scaled dT in TMEM; the read-back waited for T)
+            wait_bar(GB_DTS);
+            if (ok) {
+                done[GB_LTM] = true;
+                fence_after_sync();
+                mma_run_ts(tmem + tgA, tmem + tgT, sb + GrTc::R3, 8192, i64x64, 8, false);
+                commit(&bars[GB_X]);
             }
             // F2a: dKp^T = dW^T (diag(beta) T^T)^T (A: dW^T in TMEM); dv^T = dVt^T (diag(beta) T^T)^T
             wait_load(GB_LTB);
             if (ok) {
-                fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_tf32_ts(tmem + tgKP, tmem + tgW + 8 * s, tcu::dK(sb + GrTc::R0, 8192, s), i128x64, s > 0);
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_tf32(tmem + tgV, tcu::dK(sb + GrTc::R0 + 16384, 16384, s), tcu::dK(sb + GrTc::R0, 8192, s),
-                             i128x64, s > 0);
+                mma_run_ts(tmem + tgKP, tmem + tgW, sb + GrTc::R0, 8192, i128x64, 8, false);
+                mma_run_ss(tmem + tgV, sb + GrTc::R0 + 16384, 16384, sb + GrTc::R0, 8192, i128x64, 8, false);
                 commit(&bars[GB_DV]);
             }
-            // Km^T over dW
-            wait_bar(GB_DT);
-            if (ok) {
-                arm(GB_LKMT, 32768);
-#pragma unroll
-                for (int at = 0; at < 2; ++at)
-                    tma_load_3d(sm + GrTc::R4 + at * 16384, &mp.w64r128, &bars[GB_LKMT], 32 * at, (int)(L.kmt / 64), z);
-            }
-            // X = dT T^T (A: the scaled dT in TMEM)
-            wait_bar(GB_DTS);
-            wait_load(GB_LTM);
+            // T^T X (dL = minus its strict lower part)
+            wait_bar(GB_XT);
             if (ok) {
                 fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_tf32_ts(tmem + tgA, tmem + tgT + 8 * s, tcu::dK(sb + GrTc::R0 + 49152, 8192, s), i64x64, s > 0);
-                commit(&bars[GB_X]);
+                mma_run_ss(tmem + tgA, sb + GrTc::R3 + 16384, 8192, sb + GrTc::R2 + 16384, 8192, i64x64, 8, false);
+                commit(&bars[GB_DL]);
             }
-            // [Qp^T | Kp^T] over diag(beta) T^T, dVt^T and T
-            wait_bar(GB_X);
+            // [Qp^T | Kp^T] over diag(beta) T^T and dVt^T; Km^T over X^T
             wait_bar(GB_DV);
             if (ok) {
                 arm(GB_LQ, 65536);
@@ -1796,44 +1797,39 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                                 (int)(L.kpt / 64), z);
                 }
             }
-            // T^T X (dL = minus its strict lower part)
-            wait_bar(GB_XT);
-            wait_load(GB_LTT);
+            wait_bar(GB_DL);
             if (ok) {
-                fence_after_sync();
+                arm(GB_LKMT, 32768);
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_tf32(tmem + tgA, tcu::dK(sb + GrTc::R2, 8192, s), tcu::dK(sb + GrTc::R2 + 16384, 8192, s), i64x64,
-                             s > 0);
-                commit(&bars[GB_DL]);
+                for (int at = 0; at < 2; ++at)
+                    tma_load_3d(sm + GrTc::R2 + at * 16384, &mp.w64r128, &bars[GB_LKMT], 32 * at, (int)(L.kmt / 64), z);
+                // gamma [t][d] for the epilogue over T and T^T
+                arm(GB_LG, 32768);
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                 sb + GrTc::R3),
+                             "l"(S + L.gm), "r"(32768), "r"(smem_u32(&bars[GB_LG]))
+                             : "memory");
             }
             // F12b: [dQp^T | dKp^T] += Km^T [dA; dM]^T;  F3: dKm^T = [Qp^T | Kp^T] [dA^T | dM^T]^T
             wait_bar(GB_DM);
-            wait_load(GB_LKMT);
             wait_load(GB_LQ);
             if (ok) {
                 fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_tf32(tmem + tgQP, tcu::dK(sb + GrTc::R4, 16384, s), tcu::dK(sb + GrTc::R1, 16384, s), i128x128, 1);
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    mma_tf32(tmem + tgKM, tcu::dK(sb + GrTc::R0, 16384, s), tcu::dK(sb + GrTc::R1 + 32768, 8192, s),
-                             i128x64, s > 0);
+                mma_run_ss(tmem + tgKM, sb + GrTc::R0, 16384, sb + GrTc::R1 + 32768, 8192, i128x64, 16, false);
+            }
+            wait_load(GB_LKMT);
+            if (ok) {
+                mma_run_ss(tmem + tgQP, sb + GrTc::R2, 16384, sb + GrTc::R1, 16384, i128x128, 8, true);
                 commit(&bars[GB_F]);
             }
-            // the epilogue's operands over the retired tiles
+            // Kb [t][d] for the epilogue over [dA; dM]
             wait_bar(GB_F);
             if (ok) {
-                arm(GB_LE, 5 * 32768);
-                const int64_t eo[5] = {L.qp, L.kp, L.km, L.kb, L.gm};
-#pragma unroll
-                for (int i = 0; i < 5; ++i)
-                    asm volatile(
-                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                            sb + GrTc::R0 + 32768 * i),
-                        "l"(S + eo[i]), "r"(32768), "r"(smem_u32(&bars[GB_LE]))
-                        : "memory");
+                arm(GB_LKB, 32768);
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                 sb + GrTc::R1),
+                             "l"(S + L.kb), "r"(32768), "r"(smem_u32(&bars[GB_LKB]))
+                             : "memory");
             }
             // drain: every MMA issued, every copy armed
             commit(&bars[GB_Z]);
@@ -1854,7 +1850,9 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
         const int t16 = 16 * q + (lane & 15);  // row of an M = 64 accumulator (lanes 0-15)
         const bool rl = lane < 16;
         const int dch = 32 * q + lane;          // row of an M = 128 accumulator
-        const float *Bt = S + L.bt;
+        float *Bt = reinterpret_cast<float *>(sm + GrTc::oBT);
+        if (tid < 64) Bt[tid] = __ldg(S + L.bt + tid);
+        tcu::bar_named(1, 256);
         bool ok = true;
         auto arrive = [&](int b) {
             fence_proxy_async();
@@ -1865,7 +1863,7 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
         // every wait of the 256 threads ends the same way for all of them (named barrier 1)
         auto wait_all = [&](int b) { return !tcu::bar_or(1, 256, !st_wait(&bars[b], 0, abort_flag, a.err)); };
         do {
-            // R1: -dW^T' -> dW^T in place (the A operand of F2a) and dW [t][d] into R4
+            // -dW^T -> dW^T in place (the A operand of F2a) and dW [t][d] into R4
             if (!(ok = wait_all(GB_G1))) break;
             fence_after_sync();
             {
@@ -1905,18 +1903,17 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
             if (!(ok = wait_all(GB_DT))) break;
             if (!(ok = wait_all(GB_LTM))) break;
             fence_after_sync();
-            if (tid < 64) dgh[tid] = 0.f;  // R3 is free of Kp now
             {
                 float v[32];
                 tmem_ld32(tmem + lane_off + tgT + 32 * hw, v);
-                float *P = reinterpret_cast<float *>(sm + GrTc::R3);  // [64 r][65]
-                const unsigned char *TM = sm + GrTc::R0 + 49152;
+                float *P = reinterpret_cast<float *>(sm + GrTc::R4);  // [64 r][65]
+                const unsigned char *TM = sm + GrTc::R3;
                 uint32_t w0[16], w1[16];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int s2 = 32 * hw + j;
                     if (rl) P[t16 * 65 + s2] = v[j] * *reinterpret_cast<const float *>(TM + kmaj(8192, t16, s2));
-                    const float y = v[j] * __ldg(Bt + s2);
+                    const float y = v[j] * Bt[s2];
                     if (j < 16) w0[j] = __float_as_uint(y); else w1[j - 16] = __float_as_uint(y);
                 }
                 tmem_st16(tmem + lane_off + tgT + 32 * hw, w0);
@@ -1927,24 +1924,12 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
             tcu::bar_named(1, 256);  // P is complete
             if (tid < 64) {
                 float acc = 0.f;
-                const float *P = reinterpret_cast<const float *>(sm + GrTc::R3);
+                const float *P = reinterpret_cast<const float *>(sm + GrTc::R4);
                 for (int r = 0; r < 64; ++r) acc += P[r * 65 + tid];
                 db1[tid] = acc;
+                dgh[tid] = 0.f;
             }
-            // dv = rows of dv^T, bf16
-            if (!(ok = wait_all(GB_DV))) break;
-            fence_after_sync();
-            {
-                float v[32];
-                tmem_ld32(tmem + lane_off + tgV + 32 * hw, v);
-                __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = 32 * hw + j;
-                    if (t < nv) dv[(bos + row0 + t) * (int64_t)a.H_v * V + (int64_t)h * V + dch] = __float2bfloat16_rn(v[j]);
-                }
-            }
-            // X -> X^T into R2 (after T^T)
+            // X -> X^T into R2's upper half (Vt is consumed: X follows G2)
             if (!(ok = wait_all(GB_X))) break;
             fence_after_sync();
             {
@@ -1958,7 +1943,8 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                 }
             }
             arrive(GB_XT);
-            // dL = -(T^T X) strictly lower: dbeta += rows of dL . M; dM = diag(beta) dL
+            // dL = -(T^T X) strictly lower: dM = diag(beta) dL; then (off the chain) dbeta +=
+            // rows of dL . M
             if (!(ok = wait_all(GB_DL))) break;
             fence_after_sync();
             {
@@ -1966,32 +1952,46 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                 tmem_ld32(tmem + lane_off + tgA + 32 * hw, v);
                 if (rl) {
                     unsigned char *AM = sm + GrTc::R1, *AMT = sm + GrTc::R1 + 32768;
-                    const float bt = __ldg(Bt + t16);
+                    const float bt = Bt[t16];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int s2 = 32 * hw + j;
+                        v[j] = s2 < t16 ? -v[j] : 0.f;
+                        const float dm = bt * v[j];
+                        *reinterpret_cast<uint32_t *>(AM + kmaj(16384, 64 + t16, s2)) = tcu::tf32(dm);
+                        *reinterpret_cast<uint32_t *>(AMT + kmaj(8192, s2, 64 + t16)) = tcu::tf32(dm);
+                    }
+                }
+                arrive(GB_DM);
+                if (rl) {
                     const float4 *Mr = reinterpret_cast<const float4 *>(S + L.m + t16 * 64 + 32 * hw);
                     float part = 0.f;
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         const float4 m4 = __ldg(Mr + j4);
-                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            const int j = 4 * j4 + jj, s2 = 32 * hw + j;
-                            const float dl = s2 < t16 ? -v[j] : 0.f;
-                            part = fmaf(dl, mm[jj], part);
-                            const float dm = bt * dl;
-                            *reinterpret_cast<uint32_t *>(AM + kmaj(16384, 64 + t16, s2)) = tcu::tf32(dm);
-                            *reinterpret_cast<uint32_t *>(AMT + kmaj(8192, s2, 64 + t16)) = tcu::tf32(dm);
-                        }
+                        part = fmaf(v[4 * j4], m4.x, part);
+                        part = fmaf(v[4 * j4 + 1], m4.y, part);
+                        part = fmaf(v[4 * j4 + 2], m4.z, part);
+                        part = fmaf(v[4 * j4 + 3], m4.w, part);
                     }
                     db3[hw * 64 + t16] = part;
                 }
             }
-            arrive(GB_DM);
-            // ---- epilogue ----
-            if (!(ok = wait_all(GB_F))) break;
+            // dv = rows of dv^T, bf16 (off the chain)
+            if (!(ok = wait_all(GB_DV))) break;
             fence_after_sync();
-            // dEG[d] = rows of dS' . S_e (a warp per row, eight rows' loads in flight), while
-            // the epilogue's tiles land
+            {
+                float v[32];
+                tmem_ld32(tmem + lane_off + tgV + 32 * hw, v);
+                __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv) + (bos + row0) * (int64_t)a.H_v * V + (int64_t)h * V + dch;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * hw + j;
+                    if (t < nv) dv[(int64_t)t * a.H_v * V] = __float2bfloat16_rn(v[j]);
+                }
+            }
+
+            // dEG[d] = rows of dS' . S_e (a warp per row, eight rows' loads in flight)
 #pragma unroll 1
             for (int d0 = 8 * warp; d0 < K; d0 += 64) {
                 float4 x[8], y[8];
@@ -2006,9 +2006,14 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                     if (lane == 0) dEG[d0 + i] = sdot;
                 }
             }
-            if (!(ok = wait_all(GB_LE))) break;
-            const float *Eq = reinterpret_cast<const float *>(sm + GrTc::R0);
-            const float *Ekp = Eq + 8192, *Ekm = Eq + 16384, *Ekb = Eq + 24576, *Egm = Eq + 32768;
+            // ---- epilogue ----
+            if (!(ok = wait_all(GB_F))) break;
+            if (!(ok = wait_all(GB_LG))) break;
+            if (!(ok = wait_all(GB_LKB))) break;
+            fence_after_sync();
+            const unsigned char *QKT = sm + GrTc::R0, *KMT = sm + GrTc::R2;
+            const float *Ekb = reinterpret_cast<const float *>(sm + GrTc::R1);
+            const float *Egm = reinterpret_cast<const float *>(sm + GrTc::R3);
             const float gn = Egm[63 * K + dch];
             float dgam[32];
             float kbsum = 0.f;
@@ -2027,8 +2032,11 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                 for (int j = 0; j < 16; ++j) {
                     const int t = tb + j;
                     const int e = t * K + dch;
-                    const float qp = Eq[e], kp = Ekp[e], km = Ekm[e], kb = Ekb[e], gm = Egm[e];
-                    const float ep = expf(gm), em = expf(-gm), eb = expf(gn - gm);
+                    const float qp = *reinterpret_cast<const float *>(QKT + kmaj(16384, dch, t));
+                    const float kp = *reinterpret_cast<const float *>(QKT + kmaj(16384, dch, 64 + t));
+                    const float km = *reinterpret_cast<const float *>(KMT + kmaj(16384, dch, t));
+                    const float kb = Ekb[e], gm = Egm[e];
+                    const float ep = __expf(gm), em = __expf(-gm), eb = __expf(gn - gm);
                     const float gq = a.scale * ep * vq[j];
                     const float gk = ep * vkp[j] + em * vkm[j] + eb * vkb[j];
                     dgam[16 * p + j] = vq[j] * qp + vkp[j] * kp - vkm[j] * km - vkb[j] * kb;
@@ -2045,8 +2053,8 @@ __global__ void __launch_bounds__(288, 1) bwd_grads_tc_kernel(const BwdArgs a, c
                     }
                 }
             }
-            // dGn and the reverse cumulative sum over the two column halves (exchange in R3)
-            float *ex = reinterpret_cast<float *>(sm + GrTc::R3);  // [2][128] kb sums, [128] dgamma totals
+            // dGn and the reverse cumulative sum over the two column halves (exchange in R4)
+            float *ex = reinterpret_cast<float *>(sm + GrTc::R4);  // [2][128] kb sums, [128] dgamma totals
             float tot = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) tot += dgam[j];
@@ -2232,7 +2240,7 @@ cudaError_t launch_typed(const BwdArgs &a0, cudaStream_t stream) {
                 e = cudaFuncSetAttribute(bwd_grads_tc_kernel<GATE_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          GrTc::kBytes);
                 if (e == cudaSuccess) {
-                    bwd_grads_tc_kernel<GATE_HEAD><<<gw, 288, GrTc::kBytes, stream>>>(a, gmaps);
+                    bwd_grads_tc_kernel<GATE_HEAD><<<gw, kGrThreads, GrTc::kBytes, stream>>>(a, gmaps);
                     e = cudaGetLastError();
                 }
             } else {
