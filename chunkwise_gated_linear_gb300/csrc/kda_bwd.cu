@@ -39,6 +39,7 @@
 
 #include "kda_bwd.h"
 #include "kda_common.cuh"
+#include "tc5_tf32.cuh"
 #include "tc_util.cuh"
 
 namespace kda {
@@ -1576,6 +1577,17 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
 // half w / 4); warp 8 lane 0 issues every copy and MMA, the chain's products first. Each
 // barrier completes once. (Bulk L2 prefetches of the later operands, issued early from a warp
 // of their own, made the kernel slower: they delay the copies issued after them.)
+// D[tmem] (+)= A[smem] * B[smem], tf32 (K = 8 per instruction); issued by one thread.
+__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // n tf32 MMAs along K (8 elements each) into D: A and B K-major in shared memory with their
 // 32-element atoms a_atom / b_atom bytes apart (mma_run_ss), or A in TMEM, 8 columns per step
 // (mma_run_ts); the first one overwrites D unless acc. Out of line: one copy serves every
@@ -1583,7 +1595,7 @@ __global__ void __launch_bounds__(kT) bwd_grads_kernel(const BwdArgs a) {
 __device__ __noinline__ void mma_run_ss(uint32_t d, uint32_t a, uint32_t a_atom, uint32_t b, uint32_t b_atom,
                                         uint32_t idesc, int n, bool acc) {
 #pragma unroll 1
-    for (int s = 0; s < n; ++s) tc5::mma_tf32(d, tcu::dK(a, a_atom, s), tcu::dK(b, b_atom, s), idesc, acc || s > 0);
+    for (int s = 0; s < n; ++s) mma_tf32_ss(d, tcu::dK(a, a_atom, s), tcu::dK(b, b_atom, s), idesc, acc || s > 0);
 }
 __device__ __noinline__ void mma_run_ts(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t b_atom, uint32_t idesc, int n,
                                         bool acc) {
