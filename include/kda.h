@@ -269,7 +269,9 @@ int kda_recurrent_fwd_fused(const kda_fwd_params *p, const kda_frontend *fe, cud
  * Malformed cu_seqlens (decreasing, negative, or past T) are caught on the device: the
  * sequence is skipped, its outputs are left undefined and KDA_DEVICE_ERR_SEQLENS is raised.
  * Outputs are fully overwritten. Scratch: about 540 KB per (64-token chunk, value head)
- * at d = 128 (the chunk factors, entry states and their adjoints), plus fp32 accumulators
+ * at d = 128 (the chunk factors, entry states and their adjoints; about 700 KB for bf16
+ * inputs with d_k = d_v = 128 and beta, whose tensor-core path also keeps transposed copies
+ * of the factors), plus fp32 accumulators
  * of dq and dk for bf16 outputs, all stream-ordered from the library's pool and freed on
  * the same stream; the pool gives it back to the device at the next synchronisation (it
  * keeps at most 64 MiB between calls). Errors as kda_chunk_fwd_ex (flags must be 0).

@@ -170,7 +170,7 @@ def test_more_shapes(case):
 
 
 def test_backward_scratch_goes_back_to_the_device():
-    """The backward's scratch (about 4.5 GB on the benchmark shape) comes from the library's
+    """The backward's scratch (about 5.8 GB on the benchmark shape) comes from the library's
     pool and is freed on the stream; at the next synchronisation the pool gives back all
     but at most 64 MiB, so the device's free memory returns to within that of its value
     before the call."""
