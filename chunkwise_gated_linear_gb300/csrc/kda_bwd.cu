@@ -22,17 +22,19 @@
 // (decay-only: Kp = 0, beta = 1, so T = I, W = 0, U = V and dV = dVt).
 //
 // Five kernels, all on stream-ordered scratch from the library's pool:
-//   prep     (chunk, unit) parallel: gamma, Qp, Kp, Km, Kb, EG, M, A, T, W, U, V, dO
-//   states   (unit, 64 columns of d_v): the forward state scan, storing S and Vt per chunk;
-//            for bf16 inputs with d_k = d_v = 128 on tcgen05 (tf32, the state in TMEM)
+//   prep     (chunk, unit) parallel: gamma, Qp, Kp, Km, Kb, EG, M, A, T, W, U, V, dO (and
+//            the transposed copies the tcgen05 gradient kernel reads)
+//   states   (unit, 64 columns of d_v): the forward state scan, storing S and Vt per chunk
 //   adjoint  (unit, 64 columns of d_v): the reverse scan of dS, storing dS' and dVt per
 //            chunk, and dh0
 //   grads    (chunk, unit) parallel: every gradient above; dq and dk written directly when
 //            each key head has one value head, else added atomically into fp32
 //            accumulators (value heads that share a key head add into the same rows)
 //   finish   the accumulators to the output dtype (grouped heads, bf16 outputs)
-// The other contractions go through one CTA-wide GEMM on tf32 tensor cores (block_gemm:
-// 64 x 64 output tiles, 32-deep k steps staged in shared memory, fp32 accumulation).
+// For bf16 inputs with d_k = d_v = 128 the two scans run on tcgen05 (kind::tf32, the state
+// or its adjoint in TMEM), and with beta the gradient kernel as well (bwd_*_tc_kernel). The
+// other contractions go through one CTA-wide GEMM on tf32 mma.sync (block_gemm: 64 x 64
+// output tiles, 32-deep k steps staged in shared memory, fp32 accumulation).
 #include <algorithm>
 #include <cstdint>
 #include <type_traits>
