@@ -93,3 +93,12 @@ def test_kernel_hash_ignores_comments_and_layout_only():
     assert bench._code_only(code) != bench._code_only(code.replace('"x // y"', '"x /* y"'))
     assert "'/'" in bench._code_only("char c = '/'; // slash")
     assert len(bench.kernel_source_hash("kda_fwd_pc_kernel")) == 16
+
+
+def test_headline_traffic_is_keyed_to_the_current_kernel():
+    """The headline workload's measured DRAM traffic is stored under the hash of the kernel's
+    sources it was captured with; a change to those sources must come with a new capture
+    (else bench.py reports the traffic as null). This fails when the two drift apart."""
+    keys = [h for (w, h) in bench.MEASURED_TRAFFIC if w == "kda_b2_t8192_h32_d128_bf16"]
+    assert keys, "no traffic capture for the headline workload"
+    assert bench.kernel_source_hash("kda_fwd_pc_kernel") in keys
