@@ -267,8 +267,27 @@ def oracle_sample(x, n_units, threads=0):
     return dt, unit_tokens / x.H_v, used
 
 
+def oracle_bwd_sample(x, do, dht, n_units, threads=0):
+    """Time the fp64 backward oracle on the first n_units (sequence, head) units; returns
+    (seconds, equivalent tokens, threads used)."""
+    from oracle import kda_recurrence_bwd, oracle_threads
+
+    units = [(n, h) for n in range(x.N) for h in range(x.H_v)][:n_units]
+    t0 = time.perf_counter()
+    kda_recurrence_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, do, dht, x.cu_seqlens, x.scale, units=units,
+                       threads=threads)
+    dt = time.perf_counter() - t0
+    lens = x.lengths()
+    unit_tokens = sum(int(lens[n]) for n, _ in units)
+    used = min(threads if threads > 0 else oracle_threads(), len(units))
+    return dt, unit_tokens / x.H_v, used
+
+
 def run_reference(args, world, rank, pg):
-    """--impl reference: the oracle as it stands, on the host cores, bounded samples."""
+    """--impl reference: the oracle as it stands, on the host cores, bounded samples (the
+    token recurrence, or its reverse-mode gradients with --entry backward)."""
+    import numpy as np
+
     from inputs import workload_inputs
     from oracle import oracle_threads
 
@@ -276,19 +295,30 @@ def run_reference(args, world, rank, pg):
         return
     x = workload_inputs(args.workload)
     n_units = max(1, min(oracle_threads(), x.N * x.H_v))
+    backward = getattr(args, "entry", "chunk") == "backward"
+    if backward:
+        # the cotangents of the backward benchmark (seeded as there)
+        rng = np.random.default_rng(2000)
+        do = rng.standard_normal(x.v.shape, dtype=np.float32)
+        dht = rng.standard_normal((x.N, x.H_v, x.d_k, x.d_v), dtype=np.float32)
+        sample_fn = lambda: oracle_bwd_sample(x, do, dht, n_units)  # noqa: E731
+        what = "fp64 reverse-mode gradients of the token recurrence"
+    else:
+        sample_fn = lambda: oracle_sample(x, n_units)  # noqa: E731
+        what = "fp64 token recurrence"
     for _ in range(args.warmup):
-        oracle_sample(x, n_units)
+        sample_fn()
     tot_t, tot_tok, used = 0.0, 0.0, 1
     for _ in range(args.steps):
-        dt, tok, used = oracle_sample(x, n_units)
+        dt, tok, used = sample_fn()
         tot_t += dt
         tot_tok += tok
     value = tot_tok / tot_t
     sample = (f"{n_units} of {x.N * x.H_v} (sequence, head) units of {args.workload} per step "
-              f"({x.lengths()[0]} tokens each), fp64 token recurrence")
+              f"({x.lengths()[0]} tokens each), {what}")
     line = {
-        "impl": "reference", "metric": metric_name("chunk", args.workload), "value": value, "unit": "tokens/s",
-        "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_name("backward" if backward else "chunk", args.workload),
+        "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * tot_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload, "sample": sample},

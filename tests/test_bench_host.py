@@ -102,3 +102,17 @@ def test_headline_traffic_is_keyed_to_the_current_kernel():
     keys = [h for (w, h) in bench.MEASURED_TRAFFIC if w == "kda_b2_t8192_h32_d128_bf16"]
     assert keys, "no traffic capture for the headline workload"
     assert bench.kernel_source_hash("kda_fwd_pc_kernel") in keys
+
+
+@pytest.mark.parametrize("entry", ["chunk", "backward"])
+def test_reference_arm_times_the_entry_it_names(entry):
+    """--impl reference times the oracle of the entry it is given (the token recurrence, or
+    its reverse-mode gradients), on the host, with the contract's line."""
+    args = argparse.Namespace(workload="kda_b1_t256_h1_d64_f32", entry=entry, steps=1, warmup=3, gpus=1)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.run_reference(args, 1, 0, None)
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["dtype"] == "f64"
+    assert ("bwd" in line["metric"]) == (entry == "backward")
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
