@@ -235,14 +235,11 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
         want = (H_v, d_k) if gate == KDA_GATE_PER_CHANNEL else (H_v,)
         if dt_bias is not None and (dt_bias.dtype != torch.float32 or tuple(dt_bias.shape) != want):
             raise ValueError(f"dt_bias must be fp32 {list(want)}")
-    for t in (q, k, v, g, beta, h0, cu_seqlens, A_log, dt_bias):
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError("every tensor must be a contiguous CUDA tensor")
     if cu_seqlens is not None:
         if B != 1:
             raise ValueError("packed sequences need B == 1")
-        if cu_seqlens.dtype != torch.int32:
-            raise TypeError("cu_seqlens must be int32")
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+            raise TypeError("cu_seqlens must be int32 [N + 1]")
         N = cu_seqlens.numel() - 1
         nb, nt = N, T
     else:
@@ -250,6 +247,14 @@ def chunk_kda_fwd(q, k, v, g, beta, *, h0=None, scale=None, cu_seqlens=None,
         nb, nt = B, T
     if h0 is not None and (h0.dtype != torch.float32 or tuple(h0.shape) != (N, H_v, d_k, d_v)):
         raise ValueError("h0 must be fp32 [N, H_v, d_k, d_v]")
+    # caller-provided outputs: the kernels write every element of the documented shape
+    if o is not None and (o.dtype != q.dtype or tuple(o.shape) != (B, T, H_v, d_v)):
+        raise ValueError("o must be [B, T, H_v, d_v] in the dtype of q")
+    if ht is not None and output_final_state and (ht.dtype != torch.float32 or tuple(ht.shape) != (N, H_v, d_k, d_v)):
+        raise ValueError("ht must be fp32 [N, H_v, d_k, d_v]")
+    for t in (q, k, v, g, beta, h0, cu_seqlens, A_log, dt_bias, o, ht if output_final_state else None):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("every tensor must be a contiguous CUDA tensor")
     if o is None:
         o = torch.empty((B, T, H_v, d_v), dtype=q.dtype, device=q.device)
     if output_final_state and ht is None:
@@ -296,6 +301,8 @@ def chunk_kda_bwd(q, k, v, g, beta, do, *, h0=None, dht=None, scale=None, cu_seq
         raise ValueError("q, k must be [B, T, H_k, d_k]; v and do [B, T, H_v, d_v]")
     B, T, H_k, d_k = q.shape
     _, _, H_v, d_v = v.shape
+    if v.shape[:2] != (B, T):
+        raise ValueError("v and do must share B and T with q")
     if q.dtype == torch.bfloat16:
         dtype = KDA_DTYPE_BF16
     elif q.dtype == torch.float32:
@@ -304,19 +311,29 @@ def chunk_kda_bwd(q, k, v, g, beta, do, *, h0=None, dht=None, scale=None, cu_seq
         raise TypeError("q, k, v must be bf16 or fp32")
     if k.dtype != q.dtype or v.dtype != q.dtype or do.dtype != q.dtype:
         raise TypeError("q, k, v and do must share one dtype")
+    if g.dtype != torch.float32 or (beta is not None and beta.dtype != torch.float32):
+        raise TypeError("g and beta must be fp32")
     if g.shape == (B, T, H_v, d_k):
         gate = KDA_GATE_PER_CHANNEL
     elif g.shape == (B, T, H_v):
         gate = KDA_GATE_PER_HEAD
     else:
         raise ValueError("g must be [B, T, H_v, d_k] or [B, T, H_v]")
+    if beta is not None and beta.shape != (B, T, H_v):
+        raise ValueError("beta must be [B, T, H_v] (or None: the decay-only recurrence)")
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("packed sequences need B == 1")
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+            raise TypeError("cu_seqlens must be int32 [N + 1]")
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    nb = N
+    for name, t in (("h0", h0), ("dht", dht)):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (N, H_v, d_k, d_v)):
+            raise ValueError(f"{name} must be fp32 [N, H_v, d_k, d_v]")
     for t in (q, k, v, g, beta, do, h0, dht, cu_seqlens):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("every tensor must be a contiguous CUDA tensor")
-    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
-    nb = N
-    if cu_seqlens is not None and B != 1:
-        raise ValueError("packed sequences need B == 1")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg = torch.empty_like(g)
     dbeta = None if beta is None else torch.empty_like(beta)
