@@ -295,7 +295,8 @@ def run_reference(args, world, rank, pg):
         return
     x = workload_inputs(args.workload)
     n_units = max(1, min(oracle_threads(), x.N * x.H_v))
-    backward = getattr(args, "entry", "chunk") == "backward"
+    entry = getattr(args, "entry", "chunk")
+    backward = entry == "backward"
     if backward:
         # the cotangents of the backward benchmark (seeded as there)
         rng = np.random.default_rng(2000)
@@ -317,7 +318,7 @@ def run_reference(args, world, rank, pg):
     sample = (f"{n_units} of {x.N * x.H_v} (sequence, head) units of {args.workload} per step "
               f"({x.lengths()[0]} tokens each), {what}")
     line = {
-        "impl": "reference", "metric": metric_name("backward" if backward else "chunk", args.workload),
+        "impl": "reference", "metric": metric_name(entry, args.workload),
         "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * tot_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

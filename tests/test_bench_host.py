@@ -104,7 +104,7 @@ def test_headline_traffic_is_keyed_to_the_current_kernel():
     assert bench.kernel_source_hash("kda_fwd_pc_kernel") in keys
 
 
-@pytest.mark.parametrize("entry", ["chunk", "backward"])
+@pytest.mark.parametrize("entry", ["chunk", "recurrent", "backward"])
 def test_reference_arm_times_the_entry_it_names(entry):
     """--impl reference times the oracle of the entry it is given (the token recurrence, or
     its reverse-mode gradients), on the host, with the contract's line."""
@@ -115,4 +115,5 @@ def test_reference_arm_times_the_entry_it_names(entry):
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["dtype"] == "f64"
     assert ("bwd" in line["metric"]) == (entry == "backward")
+    assert ("recurrent" in line["metric"]) == (entry == "recurrent")
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
